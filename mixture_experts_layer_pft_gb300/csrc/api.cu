@@ -1,0 +1,287 @@
+// The exported C ABI (include/moe_pft.h): host-side argument checks, workspace layout and
+// launches.  Every check happens before any launch; the library allocates nothing.
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* msg) {
+  snprintf(g_err, sizeof(g_err), "%s", msg);
+  return code;
+}
+
+int check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    snprintf(g_err, sizeof(g_err), "%s: %s", what, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+size_t esize(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
+bool dtype_ok(int dtype) { return dtype == MOE_F32 || dtype == MOE_BF16; }
+
+int* status_of(void* ws) { return &static_cast<WsHeader*>(ws)->status; }
+
+#define REQUIRE(cond, code, msg)                                        \
+  do {                                                                  \
+    if (!(cond)) return fail(code, msg);                                \
+  } while (0)
+
+#define REQUIRE_PTR(p) REQUIRE((p) != nullptr && aligned16(p), MOE_ERR_INVALID_ARG, \
+                               #p " is NULL or not 16-byte aligned")
+
+}  // namespace
+
+static std::atomic<unsigned long long> g_launches{0};
+
+void count_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_PFT_ABI_VERSION; }
+
+uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_last_error(void) { return g_err; }
+
+size_t moe_workspace_size(int op, int T, int h, int E, int k, int f, int dtype) {
+  const size_t hdr = sizeof(WsHeader);
+  const long long Tk = (long long)std::max(T, 0) * std::max(k, 0);
+  switch (op) {
+    case MOE_OP_PFT_BUILD:
+      return hdr + round256(pft_scratch_bytes(std::max(Tk, 1LL), std::max(E, 1)));
+    case MOE_OP_EXPERT_FFN_BWD:
+      return hdr + 2 * round256((size_t)Tk * std::max(f, 0) * esize(dtype));
+    case MOE_OP_ALL: {
+      size_t m = 0;
+      for (int o = 0; o < MOE_OP_ALL; ++o) m = std::max(m, moe_workspace_size(o, T, h, E, k, f, dtype));
+      return m;
+    }
+    default:
+      return hdr;
+  }
+}
+
+int moe_status_reset(void* ws, void* stream) {
+  REQUIRE(ws != nullptr, MOE_ERR_WORKSPACE, "workspace is NULL");
+  cudaMemsetAsync(ws, 0, sizeof(WsHeader), (cudaStream_t)stream);
+  return check_launch("moe_status_reset");
+}
+
+int moe_check_status(const void* ws, void* stream, int* code) {
+  REQUIRE(ws != nullptr && code != nullptr, MOE_ERR_INVALID_ARG, "ws or code is NULL");
+  int host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, ws, sizeof(int), cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    snprintf(g_err, sizeof(g_err), "moe_check_status: %s", cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+  }
+  *code = host;
+  return host == 0 ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+int moe_route(const void* x, const float* Wg, const float* bias, int T, int h, int E, int k,
+              int dtype, int flags, float* logits, float* probs, int32_t* topk_idx,
+              float* topk_w, void* ws, size_t ws_bytes, void* stream) {
+  const cudaStream_t st = (cudaStream_t)stream;
+  const bool from_logits = (flags & MOE_ROUTE_FROM_LOGITS) != 0;
+  REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E, MOE_ERR_INVALID_ARG,
+          "moe_route: need T >= 0 and 1 <= k <= E <= 1024");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_route: bad dtype");
+  REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_ROUTE, T, h, E, k, 0, dtype),
+          MOE_ERR_WORKSPACE, "moe_route: workspace too small");
+  if (T == 0) return MOE_OK;
+  REQUIRE_PTR(logits); REQUIRE_PTR(probs); REQUIRE_PTR(topk_idx); REQUIRE_PTR(topk_w);
+  if (!from_logits) {
+    REQUIRE_PTR(x); REQUIRE_PTR(Wg);
+    REQUIRE(h >= 8 && h % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_route: h must be a multiple of 8");
+    REQUIRE(E % 4 == 0, MOE_ERR_UNSUPPORTED, "moe_route: E must be a multiple of 4");
+    REQUIRE(bias == nullptr || aligned16(bias), MOE_ERR_INVALID_ARG, "moe_route: bias not aligned");
+    simt_router_logits(dtype, x, Wg, bias, T, h, E, logits, st);
+  }
+  launch_softmax_topk(logits, T, E, k, probs, topk_idx, topk_w, st);
+  return check_launch("moe_route");
+}
+
+int moe_route_bwd(const void* x, const float* Wg, const float* probs, const int32_t* topk_idx,
+                  const float* d_topk_w, int T, int h, int E, int k, int dtype, float* d_logits,
+                  float* dWg, float* dx_router, void* ws, size_t ws_bytes, void* stream) {
+  const cudaStream_t st = (cudaStream_t)stream;
+  REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E && h >= 8, MOE_ERR_INVALID_ARG,
+          "moe_route_bwd: need T >= 0, 1 <= k <= E <= 1024, h >= 8");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_route_bwd: bad dtype");
+  REQUIRE(h % 8 == 0 && E % 4 == 0, MOE_ERR_UNSUPPORTED,
+          "moe_route_bwd: h must be a multiple of 8 and E of 4");
+  REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_ROUTE_BWD, T, h, E, k, 0, dtype),
+          MOE_ERR_WORKSPACE, "moe_route_bwd: workspace too small");
+  REQUIRE_PTR(Wg); REQUIRE_PTR(dWg); REQUIRE_PTR(x);
+  if (T == 0) {
+    cudaMemsetAsync(dWg, 0, sizeof(float) * (size_t)h * E, st);
+    return check_launch("moe_route_bwd");
+  }
+  REQUIRE_PTR(probs); REQUIRE_PTR(topk_idx); REQUIRE_PTR(d_topk_w); REQUIRE_PTR(d_logits);
+  REQUIRE(dx_router == nullptr || aligned16(dx_router), MOE_ERR_INVALID_ARG,
+          "moe_route_bwd: dx_router not aligned");
+  launch_route_dlogits(probs, topk_idx, d_topk_w, T, E, k, d_logits, status_of(ws), st);
+  simt_router_dwg(dtype, x, d_logits, T, h, E, dWg, st);
+  if (dx_router) simt_router_dx(d_logits, Wg, T, h, E, dx_router, st);
+  return check_launch("moe_route_bwd");
+}
+
+int moe_pft_build(const int32_t* topk_idx, int T, int E, int k, int32_t* num_ids,
+                  int32_t* offsets, int32_t* token_ids, int32_t* expert_ids, int32_t* slot_of,
+                  void* ws, size_t ws_bytes, void* stream) {
+  const cudaStream_t st = (cudaStream_t)stream;
+  REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E, MOE_ERR_INVALID_ARG,
+          "moe_pft_build: need T >= 0 and 1 <= k <= E <= 1024");
+  REQUIRE((long long)T * k <= (1LL << 30), MOE_ERR_UNSUPPORTED, "moe_pft_build: T*k above 2^30");
+  REQUIRE(ws != nullptr && aligned16(ws) &&
+              ws_bytes >= moe_workspace_size(MOE_OP_PFT_BUILD, T, 0, E, k, 0, MOE_F32),
+          MOE_ERR_WORKSPACE, "moe_pft_build: workspace too small");
+  REQUIRE_PTR(num_ids); REQUIRE_PTR(offsets);
+  if (T == 0) {
+    cudaMemsetAsync(num_ids, 0, sizeof(int) * E, st);
+    cudaMemsetAsync(offsets, 0, sizeof(int) * (E + 1), st);
+    return check_launch("moe_pft_build");
+  }
+  REQUIRE_PTR(topk_idx); REQUIRE_PTR(token_ids); REQUIRE_PTR(expert_ids); REQUIRE_PTR(slot_of);
+  launch_pft_build(topk_idx, T, E, k, num_ids, offsets, token_ids, expert_ids, slot_of, ws, st);
+  return check_launch("moe_pft_build");
+}
+
+int moe_dispatch(const void* x, const int32_t* token_ids, int T, int k, int h, int dtype,
+                 void* xbuf, void* ws, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 0 && k >= 1 && h >= 8, MOE_ERR_INVALID_ARG, "moe_dispatch: need T >= 0, k >= 1, h >= 8");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_dispatch: bad dtype");
+  REQUIRE(h % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_dispatch: h must be a multiple of 8");
+  REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_DISPATCH, T, h, 1, k, 0, dtype),
+          MOE_ERR_WORKSPACE, "moe_dispatch: workspace too small");
+  if (T == 0) return MOE_OK;
+  REQUIRE_PTR(x); REQUIRE_PTR(token_ids); REQUIRE_PTR(xbuf);
+  launch_dispatch(dtype, x, token_ids, T, T * k, h, xbuf, status_of(ws), (cudaStream_t)stream);
+  return check_launch("moe_dispatch");
+}
+
+int moe_dispatch_bwd(const void* dxbuf, const int32_t* slot_of, const float* dx_add, int T,
+                     int k, int h, int dtype, void* dx, void* ws, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 0 && k >= 1 && h >= 8, MOE_ERR_INVALID_ARG, "moe_dispatch_bwd: need T >= 0, k >= 1, h >= 8");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_dispatch_bwd: bad dtype");
+  REQUIRE(h % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_dispatch_bwd: h must be a multiple of 8");
+  REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_DISPATCH_BWD, T, h, 1, k, 0, dtype),
+          MOE_ERR_WORKSPACE, "moe_dispatch_bwd: workspace too small");
+  if (T == 0) return MOE_OK;
+  REQUIRE_PTR(dxbuf); REQUIRE_PTR(slot_of); REQUIRE_PTR(dx);
+  REQUIRE(dx_add == nullptr || aligned16(dx_add), MOE_ERR_INVALID_ARG, "moe_dispatch_bwd: dx_add not aligned");
+  launch_dispatch_bwd(dtype, dxbuf, slot_of, dx_add, T, k, h, dx, status_of(ws), (cudaStream_t)stream);
+  return check_launch("moe_dispatch_bwd");
+}
+
+int moe_expert_ffn(const void* xbuf, const int32_t* offsets, const void* W1, const void* W3,
+                   const void* W2, int Tk, int E, int h, int f, int dtype, void* ybuf, void* h1,
+                   void* h3, void* a, void* ws, size_t ws_bytes, void* stream) {
+  REQUIRE(Tk >= 0 && E >= 1 && E <= 1024 && h >= 8 && f >= 8, MOE_ERR_INVALID_ARG,
+          "moe_expert_ffn: need Tk >= 0, 1 <= E <= 1024, h >= 8, f >= 8");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_expert_ffn: bad dtype");
+  REQUIRE(h % 8 == 0 && f % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_expert_ffn: h and f must be multiples of 8");
+  REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_EXPERT_FFN, Tk, h, E, 1, f, dtype),
+          MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace too small");
+  if (Tk == 0) return MOE_OK;
+  REQUIRE_PTR(xbuf); REQUIRE_PTR(offsets); REQUIRE_PTR(W1); REQUIRE_PTR(W3); REQUIRE_PTR(W2);
+  REQUIRE_PTR(ybuf); REQUIRE_PTR(h1); REQUIRE_PTR(h3); REQUIRE_PTR(a);
+  simt_expert_ffn(dtype, xbuf, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, (cudaStream_t)stream);
+  return check_launch("moe_expert_ffn");
+}
+
+int moe_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const void* h3,
+                       const void* a, const int32_t* offsets, const void* W1, const void* W3,
+                       const void* W2, int Tk, int E, int h, int f, int dtype, void* dxbuf,
+                       void* dW1, void* dW3, void* dW2, void* ws, size_t ws_bytes, void* stream) {
+  const cudaStream_t st = (cudaStream_t)stream;
+  REQUIRE(Tk >= 0 && E >= 1 && E <= 1024 && h >= 8 && f >= 8, MOE_ERR_INVALID_ARG,
+          "moe_expert_ffn_bwd: need Tk >= 0, 1 <= E <= 1024, h >= 8, f >= 8");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_expert_ffn_bwd: bad dtype");
+  REQUIRE(h % 8 == 0 && f % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_expert_ffn_bwd: h and f must be multiples of 8");
+  REQUIRE(ws != nullptr && aligned16(ws) &&
+              ws_bytes >= moe_workspace_size(MOE_OP_EXPERT_FFN_BWD, Tk, h, E, 1, f, dtype),
+          MOE_ERR_WORKSPACE, "moe_expert_ffn_bwd: workspace too small");
+  REQUIRE_PTR(dW1); REQUIRE_PTR(dW3); REQUIRE_PTR(dW2);
+  if (Tk == 0) {
+    const size_t wb = (size_t)E * h * f * esize(dtype);
+    cudaMemsetAsync(dW1, 0, wb, st);
+    cudaMemsetAsync(dW3, 0, wb, st);
+    cudaMemsetAsync(dW2, 0, wb, st);
+    return check_launch("moe_expert_ffn_bwd");
+  }
+  REQUIRE_PTR(dybuf); REQUIRE_PTR(xbuf); REQUIRE_PTR(h1); REQUIRE_PTR(h3); REQUIRE_PTR(a);
+  REQUIRE_PTR(offsets); REQUIRE_PTR(W1); REQUIRE_PTR(W3); REQUIRE_PTR(W2); REQUIRE_PTR(dxbuf);
+  char* base = static_cast<char*>(ws) + sizeof(WsHeader);
+  void* dh1 = base;
+  void* dh3 = base + round256((size_t)Tk * f * esize(dtype));
+  simt_expert_ffn_bwd(dtype, dybuf, xbuf, h1, h3, a, offsets, W1, W3, W2, Tk, E, h, f, dxbuf, dW1,
+                      dW3, dW2, dh1, dh3, st);
+  return check_launch("moe_expert_ffn_bwd");
+}
+
+int moe_combine(const void* ybuf, const int32_t* slot_of, const float* topk_w, int T, int k,
+                int h, int dtype, void* y, void* ws, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 0 && k >= 1 && h >= 8, MOE_ERR_INVALID_ARG, "moe_combine: need T >= 0, k >= 1, h >= 8");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_combine: bad dtype");
+  REQUIRE(h % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_combine: h must be a multiple of 8");
+  REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_COMBINE, T, h, 1, k, 0, dtype),
+          MOE_ERR_WORKSPACE, "moe_combine: workspace too small");
+  if (T == 0) return MOE_OK;
+  REQUIRE_PTR(ybuf); REQUIRE_PTR(slot_of); REQUIRE_PTR(topk_w); REQUIRE_PTR(y);
+  launch_combine(dtype, ybuf, slot_of, topk_w, T, k, h, y, status_of(ws), (cudaStream_t)stream);
+  return check_launch("moe_combine");
+}
+
+int moe_combine_bwd(const void* dy, const void* ybuf, const int32_t* slot_of,
+                    const float* topk_w, int T, int k, int h, int dtype, void* dybuf,
+                    float* d_topk_w, void* ws, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 0 && k >= 1 && k <= 32 && h >= 8, MOE_ERR_INVALID_ARG,
+          "moe_combine_bwd: need T >= 0, 1 <= k <= 32, h >= 8");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_combine_bwd: bad dtype");
+  REQUIRE(h % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_combine_bwd: h must be a multiple of 8");
+  REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_COMBINE_BWD, T, h, 1, k, 0, dtype),
+          MOE_ERR_WORKSPACE, "moe_combine_bwd: workspace too small");
+  if (T == 0) return MOE_OK;
+  REQUIRE_PTR(dy); REQUIRE_PTR(ybuf); REQUIRE_PTR(slot_of); REQUIRE_PTR(topk_w);
+  REQUIRE_PTR(dybuf); REQUIRE_PTR(d_topk_w);
+  launch_combine_bwd(dtype, dy, ybuf, slot_of, topk_w, T, k, h, dybuf, d_topk_w, status_of(ws),
+                     (cudaStream_t)stream);
+  return check_launch("moe_combine_bwd");
+}
+
+}  // extern "C"

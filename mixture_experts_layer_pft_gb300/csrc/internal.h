@@ -1,0 +1,51 @@
+// Host-side launchers behind the C ABI (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+namespace moe {
+
+int num_sms();  // SM count of the current device (cached per device)
+void count_launch(int n = 1);  // adds to the moe_kernel_launches counter
+
+// gather.cu
+void launch_dispatch(int dtype, const void* x, const int* token_ids, int T, int rows, int h,
+                     void* xbuf, int* status, cudaStream_t st);
+void launch_combine(int dtype, const void* ybuf, const int* slot_of, const float* w, int T, int k,
+                    int h, void* y, int* status, cudaStream_t st);
+void launch_dispatch_bwd(int dtype, const void* dxbuf, const int* slot_of, const float* dx_add,
+                         int T, int k, int h, void* dx, int* status, cudaStream_t st);
+void launch_combine_bwd(int dtype, const void* dy, const void* ybuf, const int* slot_of,
+                        const float* w, int T, int k, int h, void* dybuf, float* d_w,
+                        int* status, cudaStream_t st);
+
+// route.cu
+void launch_softmax_topk(const float* logits, int T, int E, int k, float* probs, int* topk_idx,
+                         float* topk_w, cudaStream_t st);
+void launch_route_dlogits(const float* probs, const int* topk_idx, const float* d_topk_w, int T,
+                          int E, int k, float* d_logits, int* status, cudaStream_t st);
+
+// pft.cu
+int pft_num_chunks(long long Tk);
+int pft_chunk_size(long long Tk);
+size_t pft_scratch_bytes(long long Tk, int E);
+void launch_pft_build(const int* topk_idx, int T, int E, int k, int* num_ids, int* offsets,
+                      int* token_ids, int* expert_ids, int* slot_of, void* ws, cudaStream_t st);
+
+// gemm_simt.cu -- fp32-accumulating SIMT GEMMs (all shapes, both dtypes)
+void simt_router_logits(int dtype, const void* x, const float* Wg, const float* bias, int T, int h,
+                        int E, float* logits, cudaStream_t st);
+void simt_router_dwg(int dtype, const void* x, const float* d_logits, int T, int h, int E,
+                     float* dWg, cudaStream_t st);
+void simt_router_dx(const float* d_logits, const float* Wg, int T, int h, int E, float* dx,
+                    cudaStream_t st);
+void simt_expert_ffn(int dtype, const void* xbuf, const int* offsets, const void* W1,
+                     const void* W3, const void* W2, int Tk, int E, int h, int f, void* ybuf,
+                     void* h1, void* h3, void* a, cudaStream_t st);
+void simt_expert_ffn_bwd(int dtype, const void* dybuf, const void* xbuf, const void* h1,
+                         const void* h3, const void* a, const int* offsets, const void* W1,
+                         const void* W3, const void* W2, int Tk, int E, int h, int f, void* dxbuf,
+                         void* dW1, void* dW3, void* dW2, void* dh1, void* dh3, cudaStream_t st);
+
+}  // namespace moe

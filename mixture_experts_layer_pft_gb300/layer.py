@@ -1,0 +1,77 @@
+"""One padding-free MoE layer step (forward + backward) over the C ABI.
+
+``LayerBuffers`` allocates every device buffer of the layer once (PyTorch owns the memory);
+``forward`` and ``backward`` issue the stage calls in order on the current stream.  Each stage
+runs in the library's kernels; this module only sequences them.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class LayerBuffers:
+    def __init__(self, T: int, h: int, E: int, k: int, f: int, dtype: torch.dtype, device="cuda",
+                 backward: bool = True):
+        self.T, self.h, self.E, self.k, self.f, self.dtype = T, h, E, k, f, dtype
+        Tk = T * k
+        f32, i32 = torch.float32, torch.int32
+        d = dict(device=device)
+        self.logits = torch.empty(T, E, dtype=f32, **d)
+        self.probs = torch.empty(T, E, dtype=f32, **d)
+        self.topk_idx = torch.empty(T, k, dtype=i32, **d)
+        self.topk_w = torch.empty(T, k, dtype=f32, **d)
+        self.num_ids = torch.empty(E, dtype=i32, **d)
+        self.offsets = torch.empty(E + 1, dtype=i32, **d)
+        self.token_ids = torch.empty(Tk, dtype=i32, **d)
+        self.expert_ids = torch.empty(Tk, dtype=i32, **d)
+        self.slot_of = torch.empty(Tk, dtype=i32, **d)
+        self.xbuf = torch.empty(Tk, h, dtype=dtype, **d)
+        self.h1 = torch.empty(Tk, f, dtype=dtype, **d)
+        self.h3 = torch.empty(Tk, f, dtype=dtype, **d)
+        self.a = torch.empty(Tk, f, dtype=dtype, **d)
+        self.ybuf = torch.empty(Tk, h, dtype=dtype, **d)
+        self.y = torch.empty(T, h, dtype=dtype, **d)
+        self.backward = backward
+        if backward:
+            self.dybuf = torch.empty(Tk, h, dtype=dtype, **d)
+            self.d_topk_w = torch.empty(T, k, dtype=f32, **d)
+            self.dxbuf = torch.empty(Tk, h, dtype=dtype, **d)
+            self.dW1 = torch.empty(E, h, f, dtype=dtype, **d)
+            self.dW3 = torch.empty(E, h, f, dtype=dtype, **d)
+            self.dW2 = torch.empty(E, f, h, dtype=dtype, **d)
+            self.d_logits = torch.empty(T, E, dtype=f32, **d)
+            self.dWg = torch.empty(h, E, dtype=f32, **d)
+            self.dx_router = torch.empty(T, h, dtype=f32, **d)
+            self.dx = torch.empty(T, h, dtype=dtype, **d)
+        self.ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, dtype, device)
+
+
+def forward(inp: dict, b: LayerBuffers):
+    """Gate -> PFT build -> dispatch -> experts -> combine.  Returns b.y."""
+    B.moe_route(inp["x"], inp["Wg"], inp.get("bias"), b.k, b.logits, b.probs, b.topk_idx, b.topk_w, b.ws)
+    B.moe_pft_build(b.topk_idx, b.E, b.num_ids, b.offsets, b.token_ids, b.expert_ids, b.slot_of, b.ws)
+    B.moe_dispatch(inp["x"], b.token_ids, b.k, b.xbuf, b.ws)
+    B.moe_expert_ffn(b.xbuf, b.offsets, inp["W1"], inp["W3"], inp["W2"], b.ybuf, b.h1, b.h3, b.a, b.ws)
+    B.moe_combine(b.ybuf, b.slot_of, b.topk_w, b.y, b.ws)
+    return b.y
+
+
+def backward(inp: dict, dy: torch.Tensor, b: LayerBuffers):
+    """Combine bwd -> experts bwd -> gate bwd -> dispatch bwd.  Returns b.dx."""
+    B.moe_combine_bwd(dy, b.ybuf, b.slot_of, b.topk_w, b.dybuf, b.d_topk_w, b.ws)
+    B.moe_expert_ffn_bwd(b.dybuf, b.xbuf, b.h1, b.h3, b.a, b.offsets, inp["W1"], inp["W3"], inp["W2"],
+                         b.dxbuf, b.dW1, b.dW3, b.dW2, b.ws)
+    B.moe_route_bwd(inp["x"], inp["Wg"], b.probs, b.topk_idx, b.d_topk_w, b.d_logits, b.dWg,
+                    b.dx_router, b.ws)
+    B.moe_dispatch_bwd(b.dxbuf, b.slot_of, b.dx_router, b.k, b.dx, b.ws)
+    return b.dx
+
+
+def step(inp: dict, b: LayerBuffers):
+    """One full layer step: forward, then (if the buffers have it) backward of inp['dy']."""
+    forward(inp, b)
+    if b.backward:
+        backward(inp, inp["dy"], b)

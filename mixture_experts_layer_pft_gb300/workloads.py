@@ -65,18 +65,25 @@ def _normal(gen, shape, std, device, out_dtype):
     return (torch.randn(*shape, generator=gen, device=device, dtype=torch.float32) * std).to(out_dtype)
 
 
-def make_inputs(w: Workload, device="cpu", T: int | None = None, seed: int | None = None):
+def make_inputs(w: Workload, device="cpu", T: int | None = None, seed: int | None = None,
+                token_seed: int | None = None):
     """Draw x, W_g, bias, W1, W3, W2, dy for workload ``w`` on ``device``.
 
-    ``T`` overrides the token count (expert weights are drawn identically); ``seed``
-    overrides the workload's seed.
+    ``T`` overrides the token count; ``seed`` overrides the workload's seed.  With
+    ``token_seed`` the tokens x and dy come from a second generator seeded with it (x, then
+    dy) while the weights keep the workload's draws: the data-parallel replicas of one
+    layer see different tokens and identical weights.
     """
     T = w.T if T is None else T
     seed = w.seed if seed is None else seed
     dt = w.torch_dtype()
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
-    x = _normal(gen, (T, w.h), 1.0, device, dt)
+    tgen = gen
+    if token_seed is not None:
+        tgen = torch.Generator(device=device)
+        tgen.manual_seed(token_seed)
+    x = _normal(tgen, (T, w.h), 1.0, device, dt)
     Wg = _normal(gen, (w.h, w.E), 1.0 / math.sqrt(w.h), device, torch.float32)
     W1 = torch.empty(w.E, w.h, w.f, dtype=dt, device=device)
     W3 = torch.empty(w.E, w.h, w.f, dtype=dt, device=device)
@@ -88,7 +95,7 @@ def make_inputs(w: Workload, device="cpu", T: int | None = None, seed: int | Non
         W3[e] = _normal(gen, (w.h, w.f), 1.0 / math.sqrt(w.h), device, dt)
     for e in range(w.E):
         W2[e] = _normal(gen, (w.f, w.h), 1.0 / math.sqrt(w.f), device, dt)
-    dy = _normal(gen, (T, w.h), 1.0, device, dt)
+    dy = _normal(tgen, (T, w.h), 1.0, device, dt)
     bias = skew_bias(w.E, device) if w.skew else None
     return {"x": x, "Wg": Wg, "bias": bias, "W1": W1, "W3": W3, "W2": W2, "dy": dy}
 

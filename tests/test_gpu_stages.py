@@ -1,0 +1,276 @@
+"""Per-stage parity: each C-ABI call against the oracle on identical seeded inputs.
+
+Each stage gets generated inputs (never another stage's GPU output), so a failure points at
+one kernel.  Integer outputs (top-k ids, PFT arrays) and copies are compared bit-exactly;
+floating outputs by rel-L2 against the oracle's fp64 result (1e-5 fp32, 1e-2 bf16).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from helpers import TOL, dtype_name, np64, npi, rel_l2
+from oracle import moe_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from mixture_experts_layer_pft_gb300 import binding, build
+
+    build.build()
+    assert torch.cuda.is_available(), "these tests need a CUDA GPU"
+    return binding
+
+
+def gen_logits(T, E, seed, skew=False, ties=False):
+    from mixture_experts_layer_pft_gb300.workloads import random_logits, skew_bias
+
+    l = random_logits(T, E, seed, "cuda")
+    if ties:
+        l = torch.round(l * 2.0) / 2.0  # many exact ties
+    if skew:
+        l = l + skew_bias(E, "cuda")[None, :]
+    return l.contiguous()
+
+
+def oracle_routing(T, E, k, seed, skew=False):
+    """top-k ids from the oracle on generated logits (an oracle-derived input)."""
+    l = gen_logits(T, E, seed, skew).cpu().numpy()
+    return O.topk(l, k)
+
+
+def route_from_logits(B, logits, k):
+    T, E = logits.shape
+    probs = torch.empty(T, E, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_ROUTE, T, 8, E, k, 8, torch.float32)
+    B.moe_route(None, None, None, k, logits, probs, idx, w, ws, from_logits=True)
+    return probs, idx, w, ws
+
+
+# ----------------------------------------------------------------------------- gate
+
+
+@pytest.mark.parametrize("T,E,k,ties", [(1, 8, 2, False), (37, 8, 2, False), (300, 64, 6, False),
+                                        (513, 128, 6, True), (257, 256, 8, False), (64, 256, 8, True),
+                                        (33, 1000, 7, False), (20, 16, 16, True), (100, 4, 1, False)])
+def test_topk_bitexact_given_the_same_logits(B, T, E, k, ties):
+    logits = gen_logits(T, E, T + E + k, ties=ties)
+    probs, idx, w, _ = route_from_logits(B, logits, k)
+    r = O.route_from_logits(logits.cpu().numpy(), k, "f32")
+    np.testing.assert_array_equal(npi(idx), r["topk_idx"])
+    assert rel_l2(np64(probs), r["probs"]) <= TOL["f32"]
+    assert rel_l2(np64(w), r["topk_w"]) <= TOL["f32"]
+    # the gate weight is exactly the stored probability of the chosen expert
+    np.testing.assert_array_equal(np64(w), np.take_along_axis(np64(probs), npi(idx), axis=1))
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T,h,E,skew", [(130, 128, 8, False), (300, 2048, 64, False), (77, 512, 128, True)])
+def test_router_logits_and_topk_of_them(B, dt, T, h, E, skew):
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor, skew_bias
+
+    x = random_tensor((T, h), 5, dt, "cuda")
+    Wg = random_tensor((h, E), 6, torch.float32, "cuda", std=h ** -0.5)
+    bias = skew_bias(E, "cuda") if skew else None
+    k = 2
+    logits = torch.empty(T, E, device="cuda")
+    probs = torch.empty(T, E, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_ROUTE, T, h, E, k, 8, dt)
+    B.moe_route(x, Wg, bias, k, logits, probs, idx, w, ws)
+    want = O.router_logits(np64(x), np64(Wg), None if bias is None else np64(bias), "f32")
+    assert rel_l2(np64(logits), want) <= TOL["f32"]
+    # the selection on the GPU's own logits is the oracle's selection on those logits
+    np.testing.assert_array_equal(npi(idx), O.topk(logits.cpu().numpy(), k))
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T,h,E,k", [(200, 128, 8, 2), (129, 256, 64, 6), (64, 512, 256, 8)])
+def test_route_bwd(B, dt, T, h, E, k):
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    x = random_tensor((T, h), 11, dt, "cuda")
+    Wg = random_tensor((h, E), 12, torch.float32, "cuda", std=h ** -0.5)
+    logits = gen_logits(T, E, 13)
+    probs, idx, w, ws = route_from_logits(B, logits, k)
+    d_w = random_tensor((T, k), 14, torch.float32, "cuda")
+    d_logits = torch.empty(T, E, device="cuda")
+    dWg = torch.empty(h, E, device="cuda")
+    dxr = torch.empty(T, h, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_ROUTE_BWD, T, h, E, k, 8, dt)
+    B.moe_route_bwd(x, Wg, probs, idx, d_w, d_logits, dWg, dxr, ws)
+    r = O.route_bwd(np64(x), np64(Wg), np64(probs), npi(idx), np64(d_w), "f32")
+    assert rel_l2(np64(d_logits), r["d_logits"]) <= TOL["f32"]
+    assert rel_l2(np64(dWg), r["dWg"]) <= TOL["f32"]
+    assert rel_l2(np64(dxr), r["dx_router"]) <= TOL["f32"]
+    assert B.moe_check_status(ws) == 0
+
+
+# ----------------------------------------------------------------------------- PFT
+
+
+def run_pft(B, idx_np, E):
+    T, k = idx_np.shape
+    idx = torch.from_numpy(idx_np.astype(np.int32)).cuda()
+    Tk = T * k
+    out = {n: torch.full((Tk,), -7, dtype=torch.int32, device="cuda") for n in ("token_ids", "expert_ids", "slot_of")}
+    out["num_ids"] = torch.empty(E, dtype=torch.int32, device="cuda")
+    out["offsets"] = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_PFT_BUILD, T, 8, E, k, 8, torch.float32)
+    B.moe_pft_build(idx, E, out["num_ids"], out["offsets"], out["token_ids"], out["expert_ids"],
+                    out["slot_of"], ws)
+    return out, ws
+
+
+@pytest.mark.parametrize("T,E,k,skew", [(1, 8, 2, False), (37, 8, 2, False), (2048, 64, 6, False),
+                                        (4096, 128, 6, True), (4096, 256, 8, False), (5000, 7, 7, False),
+                                        (333, 1, 1, False), (16384, 128, 2, True), (131072, 256, 8, False),
+                                        (999, 1000, 3, False)])
+def test_pft_build_bitexact(B, T, E, k, skew):
+    idx = oracle_routing(T, E, k, 100 + T, skew)
+    out, ws = run_pft(B, idx, E)
+    want = O.pft_build(idx, E)
+    for n in ("num_ids", "offsets", "token_ids", "expert_ids", "slot_of"):
+        np.testing.assert_array_equal(npi(out[n]), want[n], err_msg=n)
+    assert B.moe_check_status(ws) == 0
+    # the workspace is left clean: a second build on it gives the same arrays
+    out2, _ = run_pft(B, idx, E)
+    for n in ("token_ids", "slot_of"):
+        np.testing.assert_array_equal(npi(out2[n]), want[n])
+
+
+def test_pft_build_all_tokens_to_one_expert(B):
+    T, E = 3000, 16
+    idx = np.zeros((T, 1), np.int32)
+    out, _ = run_pft(B, idx, E)
+    want = O.pft_build(idx, E)
+    for n in want:
+        np.testing.assert_array_equal(npi(out[n]), want[n], err_msg=n)
+
+
+def test_pft_build_flags_an_out_of_range_expert_id(B):
+    idx = oracle_routing(64, 8, 2, 3)
+    idx[10, 1] = 8  # an expert id equal to E: reported, not dereferenced
+    out, ws = run_pft(B, idx, 8)
+    assert B.moe_check_status(ws) & B.MOE_STATUS_BAD_INDEX
+    assert npi(out["slot_of"])[21] == -1
+    assert npi(out["offsets"])[8] == 64 * 2 - 1
+
+
+# ----------------------------------------------------------------------------- dispatch / combine
+
+
+def pft_inputs(T, E, k, seed, skew=False):
+    idx = oracle_routing(T, E, k, seed, skew)
+    return idx, O.pft_build(idx, E)
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T,h,E,k", [(1, 8, 4, 2), (77, 136, 8, 2), (2048, 2048, 64, 6), (512, 7168, 256, 8)])
+def test_dispatch_bitexact_and_bwd(B, dt, T, h, E, k):
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    idx, p = pft_inputs(T, E, k, T + h)
+    x = random_tensor((T, h), 21, dt, "cuda")
+    tok = torch.from_numpy(p["token_ids"]).cuda()
+    slot = torch.from_numpy(p["slot_of"]).cuda()
+    xbuf = torch.empty(T * k, h, dtype=dt, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, 8, dt)
+    B.moe_dispatch(x, tok, k, xbuf, ws)
+    np.testing.assert_array_equal(np64(xbuf), O.dispatch(np64(x), p["token_ids"]))
+    dxbuf = random_tensor((T * k, h), 22, dt, "cuda")
+    dx_add = random_tensor((T, h), 23, torch.float32, "cuda")
+    dx = torch.empty(T, h, dtype=dt, device="cuda")
+    for add in (None, dx_add):
+        B.moe_dispatch_bwd(dxbuf, slot, add, k, dx, ws)
+        want = O.dispatch_bwd(np64(dxbuf), p["slot_of"], k, None if add is None else np64(add), dtype_name(dt))
+        assert rel_l2(np64(dx), want) <= TOL[dtype_name(dt)] / 10
+    assert B.moe_check_status(ws) == 0
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("T,h,E,k", [(1, 8, 4, 2), (77, 136, 8, 2), (2048, 2048, 64, 6), (300, 7168, 256, 8),
+                                     (65, 64, 40, 32)])
+def test_combine_and_combine_bwd(B, dt, T, h, E, k):
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    logits = gen_logits(T, E, 31 + T)
+    r = O.route_from_logits(logits.cpu().numpy(), k, "f32")
+    p = O.pft_build(r["topk_idx"], E)
+    slot = torch.from_numpy(p["slot_of"]).cuda()
+    w = torch.from_numpy(r["topk_w"].astype(np.float32)).cuda()
+    ybuf = random_tensor((T * k, h), 32, dt, "cuda")
+    y = torch.empty(T, h, dtype=dt, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, 8, dt)
+    B.moe_combine(ybuf, slot, w, y, ws)
+    tol = TOL[dtype_name(dt)] / 10
+    assert rel_l2(np64(y), O.combine(np64(ybuf), p["slot_of"], r["topk_w"], dtype_name(dt))) <= tol
+    dy = random_tensor((T, h), 33, dt, "cuda")
+    dybuf = torch.empty(T * k, h, dtype=dt, device="cuda")
+    d_w = torch.empty(T, k, device="cuda")
+    B.moe_combine_bwd(dy, ybuf, slot, w, dybuf, d_w, ws)
+    want_dyb, want_dw = O.combine_bwd(np64(dy), np64(ybuf), p["slot_of"], r["topk_w"], dtype_name(dt))
+    assert rel_l2(np64(dybuf), want_dyb) <= tol
+    assert rel_l2(np64(d_w), want_dw) <= TOL["f32"]
+    assert B.moe_check_status(ws) == 0
+
+
+# ----------------------------------------------------------------------------- experts
+
+
+def expert_inputs(T, h, E, k, f, dt, seed, skew=False):
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    idx, p = pft_inputs(T, E, k, seed, skew)
+    Tk = T * k
+    d = {
+        "offsets": torch.from_numpy(p["offsets"]).cuda(),
+        "xbuf": random_tensor((Tk, h), seed + 1, dt, "cuda"),
+        "W1": random_tensor((E, h, f), seed + 2, dt, "cuda", std=h ** -0.5),
+        "W3": random_tensor((E, h, f), seed + 3, dt, "cuda", std=h ** -0.5),
+        "W2": random_tensor((E, f, h), seed + 4, dt, "cuda", std=f ** -0.5),
+        "dybuf": random_tensor((Tk, h), seed + 5, dt, "cuda"),
+    }
+    return p, d
+
+
+EXPERT_SHAPES = [
+    # T, h, E, k, f, dtype, skew
+    (256, 128, 8, 2, 64, torch.float32, False),     # the tiny fp32 layer
+    (300, 256, 8, 2, 192, torch.bfloat16, False),   # several tiles, ragged segment tails
+    (200, 512, 16, 4, 256, torch.bfloat16, True),   # Zipf load: empty experts
+    (97, 384, 40, 6, 128, torch.float32, True),     # many small segments at every residue
+    (64, 256, 4, 1, 136, torch.bfloat16, False),    # f not a multiple of the tile
+]
+
+
+@pytest.mark.parametrize("T,h,E,k,f,dt,skew", EXPERT_SHAPES)
+def test_expert_ffn_forward_and_backward(B, T, h, E, k, f, dt, skew):
+    p, d = expert_inputs(T, h, E, k, f, dt, 40 + T, skew)
+    Tk = T * k
+    z = lambda *s: torch.empty(*s, dtype=dt, device="cuda")  # noqa: E731
+    ybuf, h1, h3, a = z(Tk, h), z(Tk, f), z(Tk, f), z(Tk, f)
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, dt)
+    B.moe_expert_ffn(d["xbuf"], d["offsets"], d["W1"], d["W3"], d["W2"], ybuf, h1, h3, a, ws)
+    dn = dtype_name(dt)
+    want = O.expert_ffn(np64(d["xbuf"]), p["offsets"], np64(d["W1"]), np64(d["W3"]), np64(d["W2"]), dn)
+    for n, got in (("ybuf", ybuf), ("h1", h1), ("h3", h3), ("a", a)):
+        assert rel_l2(np64(got), want[n]) <= TOL[dn], n
+    dxbuf, dW1, dW3, dW2 = z(Tk, h), z(E, h, f), z(E, h, f), z(E, f, h)
+    # both sides of the backward get the oracle forward's saved tensors (exact in dtype)
+    sv = {n: torch.from_numpy(want[n]).to(dt).cuda() for n in ("h1", "h3", "a")}
+    B.moe_expert_ffn_bwd(d["dybuf"], d["xbuf"], sv["h1"], sv["h3"], sv["a"], d["offsets"], d["W1"],
+                         d["W3"], d["W2"], dxbuf, dW1, dW3, dW2, ws)
+    wb = O.expert_ffn_bwd(np64(d["dybuf"]), np64(d["xbuf"]), want["h1"], want["h3"], want["a"],
+                          p["offsets"], np64(d["W1"]), np64(d["W3"]), np64(d["W2"]), dn)
+    for n, got in (("dxbuf", dxbuf), ("dW1", dW1), ("dW3", dW3), ("dW2", dW2)):
+        assert rel_l2(np64(got), wb[n]) <= TOL[dn], n
+    empty = np.nonzero(p["num_ids"] == 0)[0]
+    for e in empty:
+        assert (np64(dW1[e]) == 0).all() and (np64(dW2[e]) == 0).all()
+    assert B.moe_check_status(ws) == 0
