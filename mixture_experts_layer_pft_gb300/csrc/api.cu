@@ -36,6 +36,21 @@ bool dtype_ok(int dtype) { return dtype == MOE_F32 || dtype == MOE_BF16; }
 
 int* status_of(void* ws) { return &static_cast<WsHeader*>(ws)->status; }
 
+// bf16 expert GEMMs with h and f multiples of 128 run on the tcgen05 engine; everything else
+// (fp32, other shapes) on the SIMT engine.  MOE_PFT_GEMM=simt forces the SIMT engine.
+int tc_failure(const char* what) {
+  const int rc = check_launch(what);
+  if (rc != MOE_OK) return rc;
+  snprintf(g_err, sizeof(g_err), "%s: tensor map encoding or kernel attribute setup failed", what);
+  return MOE_ERR_CUDA;
+}
+
+bool use_tensor_cores(int dtype, int h, int f) {
+  const char* env = getenv("MOE_PFT_GEMM");
+  if (env && strcmp(env, "simt") == 0) return false;
+  return tc_supported(dtype, h, f);
+}
+
 #define REQUIRE(cond, code, msg)                                        \
   do {                                                                  \
     if (!(cond)) return fail(code, msg);                                \
@@ -220,7 +235,13 @@ int moe_expert_ffn(const void* xbuf, const int32_t* offsets, const void* W1, con
   if (Tk == 0) return MOE_OK;
   REQUIRE_PTR(xbuf); REQUIRE_PTR(offsets); REQUIRE_PTR(W1); REQUIRE_PTR(W3); REQUIRE_PTR(W2);
   REQUIRE_PTR(ybuf); REQUIRE_PTR(h1); REQUIRE_PTR(h3); REQUIRE_PTR(a);
-  simt_expert_ffn(dtype, xbuf, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, (cudaStream_t)stream);
+  if (use_tensor_cores(dtype, h, f)) {
+    if (tc_expert_ffn(xbuf, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, status_of(ws),
+                      (cudaStream_t)stream) != 0)
+      return tc_failure("moe_expert_ffn");
+  } else {
+    simt_expert_ffn(dtype, xbuf, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, (cudaStream_t)stream);
+  }
   return check_launch("moe_expert_ffn");
 }
 
@@ -249,8 +270,14 @@ int moe_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, cons
   char* base = static_cast<char*>(ws) + sizeof(WsHeader);
   void* dh1 = base;
   void* dh3 = base + round256((size_t)Tk * f * esize(dtype));
-  simt_expert_ffn_bwd(dtype, dybuf, xbuf, h1, h3, a, offsets, W1, W3, W2, Tk, E, h, f, dxbuf, dW1,
-                      dW3, dW2, dh1, dh3, st);
+  if (use_tensor_cores(dtype, h, f)) {
+    if (tc_expert_ffn_bwd(dybuf, xbuf, h1, h3, a, offsets, W1, W3, W2, Tk, E, h, f, dxbuf, dW1, dW3, dW2,
+                          dh1, dh3, status_of(ws), st) != 0)
+      return tc_failure("moe_expert_ffn_bwd");
+  } else {
+    simt_expert_ffn_bwd(dtype, dybuf, xbuf, h1, h3, a, offsets, W1, W3, W2, Tk, E, h, f, dxbuf, dW1,
+                        dW3, dW2, dh1, dh3, st);
+  }
   return check_launch("moe_expert_ffn_bwd");
 }
 

@@ -1,0 +1,635 @@
+// Tensor-core grouped GEMM engine for the bf16 expert FFN (sm_103a: tcgen05 + TMEM + TMA).
+//
+// One persistent, warp-specialised kernel template serves the six GEMMs of the expert FFN
+// forward and backward over the padding-free buffer.  Every GEMM is arranged so that a weight
+// (or weight-gradient) dimension is the MMA's M = 128 and the expert's tokens are either the
+// MMA's N (forward, dgrad) or its K (wgrad).  With tokens on N, an expert segment of n rows
+// costs round_up(n, 16) columns: the in-place tile padding is at most 15 columns per segment
+// and each 128-row weight tile streams from HBM once per 256 tokens of its expert.
+//
+//   mode      D (fp32 in TMEM)            A operand (M x K)          B operand (N x K)
+//   GATEUP    H1^T, H3^T [f x n]          W1[e], W3[e] ([h,f]: MN)   xbuf rows   (K-major)
+//   DOWN      Y^T [h x n]                 W2[e] ([f,h]: MN)          a rows      (K-major)
+//   DA        dA^T [f x n]                W2[e] ([f,h]: K-major)     dybuf rows  (K-major)
+//   DX        dX^T [h x n], K = 2f        W1[e] then W3[e] (K-maj)   dh1 then dh3 rows (K-major)
+//   WGRAD13   dW1^T, dW3^T [f x h-tile]   dh1, dh3 rows ([n,f]: MN)  xbuf rows ([n,h]: MN), K = n
+//   WGRAD2    dW2^T [h x f-tile]          dybuf rows ([n,h]: MN)     a rows ([n,f]: MN), K = n
+//
+// Warp roles (192 threads, one CTA per SM): warp 0 issues TMA loads into a ring of shared-
+// memory stages; warp 1 owns the TMEM allocation and one lane issues tcgen05.mma into fp32
+// accumulators in TMEM; warps 2-5 drain TMEM (tcgen05.ld), apply the epilogue (SwiGLU, its
+// derivative, or a plain store) and write bf16 results with 64-byte coalesced stores.  Stages
+// and accumulators hand over through mbarriers.  Every wait is bounded (about two seconds of
+// %globaltimer): on expiry the kernel sets MOE_STATUS_TIMEOUT, every role unwinds, and the
+// TMEM is released before the CTA exits.  No cluster, no multicast.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int BM = 128;           // MMA M: rows of the weight dimension per tile
+constexpr int BK = 64;            // K per stage: one 128-byte swizzle row of bf16
+constexpr uint32_t kBox = 8192;   // bytes of one 64 x 64 bf16 box
+constexpr uint32_t kATile = 16384;  // bytes of one 128 x 64 A tile
+constexpr int kTmemCols = 512;
+constexpr int kMaxE = 1024;
+constexpr uint32_t kStageRegion = 196608;  // shared memory given to the stage ring
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+enum Mode { GATEUP = 0, DOWN = 1, DA = 2, DX = 3, WGRAD13 = 4, WGRAD2 = 5 };
+
+template <int MODE> struct Cfg {
+  static constexpr int NUM_A = (MODE == GATEUP || MODE == WGRAD13) ? 2 : 1;
+  static constexpr bool A_MN = (MODE == GATEUP || MODE == DOWN || MODE == WGRAD13 || MODE == WGRAD2);
+  static constexpr bool B_MN = (MODE == WGRAD13 || MODE == WGRAD2);
+  static constexpr bool TOKEN_N = (MODE <= DX);
+  static constexpr int BN = (MODE == WGRAD13) ? 128 : 256;
+  static constexpr uint32_t A_BYTES = NUM_A * kATile;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + (BN / 64) * kBox;
+  static constexpr int STAGES = kStageRegion / STAGE_BYTES;
+  static constexpr int ACC_BUFS = kTmemCols / (NUM_A * BN);
+  static_assert(ACC_BUFS >= 1 && STAGES >= 2, "tile configuration");
+};
+
+struct TcParams {
+  CUtensorMap mapA0;  // GATEUP W1 | DOWN W2 | DA W2 | DX W1 | WGRAD13 dh1 | WGRAD2 dybuf
+  CUtensorMap mapA1;  // GATEUP W3 | DX W3 | WGRAD13 dh3
+  CUtensorMap mapB0;  // GATEUP xbuf | DOWN a | DA dybuf | DX dh1 | WGRAD13 xbuf | WGRAD2 a
+  CUtensorMap mapB1;  // DX dh3
+  const int* offsets;
+  int E;
+  int M;           // total rows of the M (weight) dimension per expert
+  int K;           // token-N modes: K of one operand pair (DX: f per half)
+  int Nw;          // wgrad modes: total N (weight) columns
+  int a_rows;      // rows per expert in the 2D view of the weight map(s) (token-N modes)
+  __nv_bfloat16* out0;
+  __nv_bfloat16* out1;
+  __nv_bfloat16* out2;
+  const __nv_bfloat16* in0;
+  const __nv_bfloat16* in1;
+  int ld_out;
+  long long out_expert_stride;  // wgrad: elements between consecutive experts' outputs
+  int* status;
+};
+
+// ---------------------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of `bar` with parity `parity`.  Gives up after kWaitLimitNs or when
+// another role has already given up; then returns false.
+__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                       int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        atomicOr(status, MOE_STATUS_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
+                                            int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = n.
+__device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          tmem_d),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit TMEM columns -> 16 registers per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t addr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(addr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------- work units
+
+struct Unit {
+  int e;        // expert
+  int m0;       // first row of the weight (M) dimension
+  int row0;     // token-N: first buffer row of the chunk; wgrad: first buffer row of the expert
+  int rows;     // token-N: rows in the chunk; wgrad: rows of the expert (K)
+  int n0;       // wgrad: first N column
+  int ncols;    // columns of D to produce (token-N: rows; wgrad: N tile width)
+  int nmma;     // MMA N (multiple of 16)
+  int nk;       // K steps of BK
+};
+
+// Token-N modes: expert e has nc_e = ceil(n_e / 256) chunks of about equal size (a multiple of
+// 16 rows, the last one shorter); its units are (m-tile, chunk) pairs, chunks innermost, so
+// the CTAs that stream one weight tile for different chunks run side by side.
+struct Sched {
+  int total;
+  int mt;  // M tiles per expert
+  int nt;  // wgrad: N tiles
+};
+
+template <int MODE>
+__device__ __forceinline__ Unit decode(int u, const Sched& sc, const int* s_pref, const int* s_off,
+                                       const TcParams& p) {
+  using C = Cfg<MODE>;
+  Unit w;
+  if (C::TOKEN_N) {
+    int lo = 0, hi = p.E - 1;  // largest e with s_pref[e] <= u
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pref[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int n = s_off[e + 1] - s_off[e];
+    const int nc = (n + 255) / 256;
+    const int cs = ((n + nc - 1) / nc + 15) & ~15;
+    const int local = u - s_pref[e];
+    const int mtile = local / nc, c = local % nc;
+    w.e = e;
+    w.m0 = mtile * BM;
+    w.row0 = s_off[e] + c * cs;
+    w.rows = min(cs, n - c * cs);
+    w.n0 = 0;
+    w.ncols = w.rows;
+    w.nmma = (w.rows + 15) & ~15;
+    w.nk = (MODE == DX) ? 2 * p.K / BK : p.K / BK;
+  } else {
+    const int per = sc.mt * sc.nt;
+    w.e = u / per;
+    const int r = u % per;
+    w.m0 = (r / sc.nt) * BM;
+    w.n0 = (r % sc.nt) * C::BN;
+    w.row0 = s_off[w.e];
+    w.rows = s_off[w.e + 1] - s_off[w.e];
+    w.ncols = min(C::BN, p.Nw - w.n0);
+    w.nmma = w.ncols;
+    w.nk = (w.rows + BK - 1) / BK;
+  }
+  return w;
+}
+
+// ---------------------------------------------------------------------------- the kernel
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using C = Cfg<MODE>;
+  extern __shared__ __align__(1024) uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t full_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[C::ACC_BUFS];
+  __shared__ __align__(8) uint64_t tempty_bar[C::ACC_BUFS];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ uint32_t s_tmem;
+  __shared__ volatile int s_abort;
+  __shared__ int s_off[kMaxE + 1];
+  __shared__ int s_pref[kMaxE + 1];
+  __shared__ Sched s_sched;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  // stage ring aligned to 1024 bytes (the swizzle atom)
+  const uint32_t ring = (smem_u32(dsmem) + 1023u) & ~1023u;
+  uint8_t* ring_ptr = dsmem + (ring - smem_u32(dsmem));
+
+  // ------------------------------------------------------------------ schedule
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = __ldg(p.offsets + i);
+  __syncthreads();
+  if (warp == 0) {
+    // units per expert, then an inclusive scan into s_pref[1..E] (s_pref[0] = 0)
+    const int per = (p.E + 31) / 32;
+    const int b0 = min(lane * per, p.E), b1 = min(b0 + per, p.E);
+    const int mt = p.M / BM;
+    int local = 0;
+    for (int e = b0; e < b1; ++e) {
+      int ue;
+      if (C::TOKEN_N) ue = ((s_off[e + 1] - s_off[e] + 255) / 256) * mt;
+      else ue = mt * ((p.Nw + C::BN - 1) / C::BN);
+      s_pref[e + 1] = ue;
+      local += ue;
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - local;
+    for (int e = b0; e < b1; ++e) {
+      const int ue = s_pref[e + 1];
+      s_pref[e] = run;
+      run += ue;
+    }
+    if (lane == 31) {
+      s_pref[p.E] = incl;
+      s_sched.total = incl;
+      s_sched.mt = mt;
+      s_sched.nt = (p.Nw + C::BN - 1) / C::BN;
+    }
+  }
+  __syncthreads();
+  const Sched sc = s_sched;
+  if ((int)blockIdx.x >= sc.total) return;  // nothing for this CTA (before any TMEM use)
+
+  // ------------------------------------------------------------------ barriers + TMEM
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    for (int b = 0; b < C::ACC_BUFS; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
+    mbar_init(&drain_bar, 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem;
+
+  if (warp == 0) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < sc.total && ok; u += gridDim.x) {
+        const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
+        const int nbB = C::TOKEN_N ? (w.nmma + 63) / 64 : C::BN / 64;
+        const uint32_t tx = C::A_BYTES + (uint32_t)nbB * kBox;
+        for (int ks = 0; ks < w.nk; ++ks) {
+          if (!mbar_wait(&empty_bar[s], ph ^ 1u, &s_abort, p.status)) { ok = false; break; }
+          mbar_expect_tx(&full_bar[s], tx);
+          const uint32_t a_sm = ring + s * C::STAGE_BYTES;
+          const uint32_t b_sm = a_sm + C::A_BYTES;
+          const int k0 = ks * BK;
+          if (MODE == GATEUP || MODE == DOWN) {
+            const int y = w.e * p.a_rows + k0;
+            tma_load_2d(a_sm, &p.mapA0, &full_bar[s], w.m0, y);
+            tma_load_2d(a_sm + kBox, &p.mapA0, &full_bar[s], w.m0 + 64, y);
+            if (MODE == GATEUP) {
+              tma_load_2d(a_sm + kATile, &p.mapA1, &full_bar[s], w.m0, y);
+              tma_load_2d(a_sm + kATile + kBox, &p.mapA1, &full_bar[s], w.m0 + 64, y);
+            }
+            for (int j = 0; j < nbB; ++j) tma_load_2d(b_sm + j * kBox, &p.mapB0, &full_bar[s], k0, w.row0 + 64 * j);
+          } else if (MODE == DA) {
+            tma_load_2d(a_sm, &p.mapA0, &full_bar[s], k0, w.e * p.a_rows + w.m0);
+            for (int j = 0; j < nbB; ++j) tma_load_2d(b_sm + j * kBox, &p.mapB0, &full_bar[s], k0, w.row0 + 64 * j);
+          } else if (MODE == DX) {
+            const bool second = k0 >= p.K;
+            const int kk = second ? k0 - p.K : k0;
+            tma_load_2d(a_sm, second ? &p.mapA1 : &p.mapA0, &full_bar[s], kk, w.e * p.a_rows + w.m0);
+            for (int j = 0; j < nbB; ++j)
+              tma_load_2d(b_sm + j * kBox, second ? &p.mapB1 : &p.mapB0, &full_bar[s], kk, w.row0 + 64 * j);
+          } else {  // wgrad: K runs over the expert's token rows
+            const int y = w.row0 + k0;
+            tma_load_2d(a_sm, &p.mapA0, &full_bar[s], w.m0, y);
+            tma_load_2d(a_sm + kBox, &p.mapA0, &full_bar[s], w.m0 + 64, y);
+            if (MODE == WGRAD13) {
+              tma_load_2d(a_sm + kATile, &p.mapA1, &full_bar[s], w.m0, y);
+              tma_load_2d(a_sm + kATile + kBox, &p.mapA1, &full_bar[s], w.m0 + 64, y);
+            }
+            for (int j = 0; j < nbB; ++j) tma_load_2d(b_sm + j * kBox, &p.mapB0, &full_bar[s], w.n0 + 64 * j, y);
+          }
+          if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (!ok) {
+        // give the loads already in flight (a few microseconds each) time to land
+        const unsigned long long t0 = globaltimer();
+        while (globaltimer() - t0 < 2000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    int s = 0;
+    uint32_t ph = 0;
+    int it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < sc.total && ok; u += gridDim.x, ++it) {
+      const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
+      const int b = it % C::ACC_BUFS;
+      const uint32_t aph = (uint32_t)(it / C::ACC_BUFS) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tempty_bar[b], aph ^ 1u, &s_abort, p.status))) { ok = false; break; }
+      tc_fence_after();
+      if (w.nk == 0) {  // an expert without rows (wgrad): nothing to multiply
+        if (lane == 0) mbar_arrive(&tfull_bar[b]);
+        continue;
+      }
+      const uint32_t idesc = idesc_bf16(w.nmma, C::A_MN, C::B_MN);
+      const uint32_t d0 = tmem_base + (uint32_t)(b * C::NUM_A * C::BN);
+      for (int ks = 0; ks < w.nk; ++ks) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], ph, &s_abort, p.status))) { ok = false; break; }
+        const uint32_t a_sm = ring + s * C::STAGE_BYTES;
+        const uint32_t b_sm = a_sm + C::A_BYTES;
+        if (!C::TOKEN_N && ks == w.nk - 1 && (w.rows & (BK - 1)) != 0) {
+          // the last K step straddles the next expert's rows: zero token rows >= rows
+          const int valid = w.rows & (BK - 1);
+          const int nbox = C::NUM_A * 2 + C::BN / 64;
+          const int zrows = BK - valid;
+          for (int q = lane; q < nbox * zrows * 8; q += 32) {
+            const int box = q / (zrows * 8);
+            const int r = valid + (q / 8) % zrows;
+            const int c16 = q % 8;
+            uint4* dst = reinterpret_cast<uint4*>(ring_ptr + (a_sm - ring) + box * kBox + r * 128 + c16 * 16);
+            *dst = make_uint4(0, 0, 0, 0);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int a = 0; a < C::NUM_A; ++a) {
+            const uint32_t a_base = a_sm + a * kATile;
+#pragma unroll
+            for (int kk = 0; kk < BK / 16; ++kk) {
+              uint64_t ad, bd;
+              if (C::A_MN) ad = sdesc(a_base + kk * 2048, kBox, 1024);
+              else ad = sdesc(a_base + kk * 32, 16, 1024);
+              if (C::B_MN) bd = sdesc(b_sm + kk * 2048, kBox, 1024);
+              else bd = sdesc(b_sm + kk * 32, 16, 1024);
+              umma(d0 + a * C::BN, ad, bd, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(&empty_bar[s]);  // the stage is free once these MMAs have read it
+        }
+        __syncwarp();
+        if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+      if (lane == 0) umma_commit(&tfull_bar[b]);
+      __syncwarp();
+    }
+    // make sure no MMA is still writing TMEM before the teardown
+    if (lane == 0) {
+      umma_commit(&drain_bar);
+      const unsigned long long t0 = globaltimer();
+      while (!mbar_try_wait(&drain_bar, 0) && globaltimer() - t0 < kWaitLimitNs) {
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ epilogue (warps 2..5)
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int m_local = q * 32 + lane;
+    int it = 0;
+    for (int u = blockIdx.x; u < sc.total; u += gridDim.x, ++it) {
+      const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
+      const int b = it % C::ACC_BUFS;
+      const uint32_t aph = (uint32_t)(it / C::ACC_BUFS) & 1u;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[b], aph, &s_abort, p.status))) break;
+      tc_fence_after();
+      const int m = w.m0 + m_local;
+      const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::NUM_A * C::BN);
+      const bool zero = (w.nk == 0);
+      for (int c0 = 0; c0 < w.ncols; c0 += 16) {
+        float v0[16], v1[16];
+        if (!zero) {
+          tmem_ld16(t0 + c0, v0);
+          if (C::NUM_A == 2) tmem_ld16(t0 + C::BN + c0, v1);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) { v0[i] = 0.f; v1[i] = 0.f; }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int c = c0 + i;
+          if (c >= w.ncols) break;
+          if (MODE == GATEUP) {
+            const size_t o = (size_t)(w.row0 + c) * p.ld_out + m;
+            const float h1 = v0[i], h3 = v1[i];
+            p.out0[o] = __float2bfloat16_rn(h1);
+            p.out1[o] = __float2bfloat16_rn(h3);
+            p.out2[o] = __float2bfloat16_rn(h1 * sigmoidf_(h1) * h3);
+          } else if (MODE == DOWN || MODE == DX) {
+            p.out0[(size_t)(w.row0 + c) * p.ld_out + m] = __float2bfloat16_rn(v0[i]);
+          } else if (MODE == DA) {
+            const size_t o = (size_t)(w.row0 + c) * p.ld_out + m;
+            const float z1 = __bfloat162float(p.in0[o]);
+            const float z3 = __bfloat162float(p.in1[o]);
+            const float sg = sigmoidf_(z1);
+            const float da = v0[i];
+            p.out0[o] = __float2bfloat16_rn(da * z3 * sg * (1.f + z1 * (1.f - sg)));
+            p.out1[o] = __float2bfloat16_rn(da * z1 * sg);
+          } else {  // wgrad: D[m][c] is dW^T, stored at [n0 + c][m] of expert e
+            const size_t o = (size_t)w.e * p.out_expert_stride + (size_t)(w.n0 + c) * p.ld_out + m;
+            p.out0[o] = __float2bfloat16_rn(v0[i]);
+            if (MODE == WGRAD13) p.out1[o] = __float2bfloat16_rn(v1[i]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[b]);
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2D bf16 map over a row-major [rows, cols] matrix, box = box_cols x box_rows, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int MODE>
+int launch(const TcParams& p, cudaStream_t st) {
+  using C = Cfg<MODE>;
+  const int smem = (int)(C::STAGES * C::STAGE_BYTES + 1024);
+  if (cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return -1;
+  tc_gemm_kernel<MODE><<<num_sms(), kThreads, smem, st>>>(p);
+  count_launch();
+  return 0;
+}
+
+TcParams blank_params() {
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  return p;
+}
+
+}  // namespace
+
+bool tc_supported(int dtype, int h, int f) {
+  return dtype == MOE_BF16 && h % 128 == 0 && f % 128 == 0 && encode_fn() != nullptr;
+}
+
+int tc_expert_ffn(const void* xbuf, const int* offsets, const void* W1, const void* W3, const void* W2, int Tk,
+                  int E, int h, int f, void* ybuf, void* h1, void* h3, void* a, int* status, cudaStream_t st) {
+  TcParams g = blank_params();
+  bool ok = make_map(&g.mapA0, W1, (long long)E * h, f, 64, 64) &&
+            make_map(&g.mapA1, W3, (long long)E * h, f, 64, 64) && make_map(&g.mapB0, xbuf, Tk, h, 64, 64);
+  if (!ok) return -1;
+  g.offsets = offsets; g.E = E; g.M = f; g.K = h; g.a_rows = h;
+  g.out0 = static_cast<__nv_bfloat16*>(h1); g.out1 = static_cast<__nv_bfloat16*>(h3);
+  g.out2 = static_cast<__nv_bfloat16*>(a); g.ld_out = f; g.status = status;
+  if (launch<GATEUP>(g, st)) return -1;
+
+  TcParams d = blank_params();
+  ok = make_map(&d.mapA0, W2, (long long)E * f, h, 64, 64) && make_map(&d.mapB0, a, Tk, f, 64, 64);
+  if (!ok) return -1;
+  d.offsets = offsets; d.E = E; d.M = h; d.K = f; d.a_rows = f;
+  d.out0 = static_cast<__nv_bfloat16*>(ybuf); d.ld_out = h; d.status = status;
+  return launch<DOWN>(d, st);
+}
+
+int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const void* h3, const void* a,
+                      const int* offsets, const void* W1, const void* W3, const void* W2, int Tk, int E, int h,
+                      int f, void* dxbuf, void* dW1, void* dW3, void* dW2, void* dh1, void* dh3, int* status,
+                      cudaStream_t st) {
+  // dA^T = W2[e] dY^T, fused with the SwiGLU backward -> dh1, dh3
+  TcParams da = blank_params();
+  bool ok = make_map(&da.mapA0, W2, (long long)E * f, h, 64, 128) && make_map(&da.mapB0, dybuf, Tk, h, 64, 64);
+  if (!ok) return -1;
+  da.offsets = offsets; da.E = E; da.M = f; da.K = h; da.a_rows = f;
+  da.out0 = static_cast<__nv_bfloat16*>(dh1); da.out1 = static_cast<__nv_bfloat16*>(dh3);
+  da.in0 = static_cast<const __nv_bfloat16*>(h1); da.in1 = static_cast<const __nv_bfloat16*>(h3);
+  da.ld_out = f; da.status = status;
+  if (launch<DA>(da, st)) return -1;
+
+  // dX^T = W1[e] dh1^T + W3[e] dh3^T
+  TcParams dx = blank_params();
+  ok = make_map(&dx.mapA0, W1, (long long)E * h, f, 64, 128) && make_map(&dx.mapA1, W3, (long long)E * h, f, 64, 128) &&
+       make_map(&dx.mapB0, dh1, Tk, f, 64, 64) && make_map(&dx.mapB1, dh3, Tk, f, 64, 64);
+  if (!ok) return -1;
+  dx.offsets = offsets; dx.E = E; dx.M = h; dx.K = f; dx.a_rows = h;
+  dx.out0 = static_cast<__nv_bfloat16*>(dxbuf); dx.ld_out = h; dx.status = status;
+  if (launch<DX>(dx, st)) return -1;
+
+  // dW1[e]^T = dh1^T X, dW3[e]^T = dh3^T X  (stored as dW1[e][h][f])
+  TcParams w13 = blank_params();
+  ok = make_map(&w13.mapA0, dh1, Tk, f, 64, 64) && make_map(&w13.mapA1, dh3, Tk, f, 64, 64) &&
+       make_map(&w13.mapB0, xbuf, Tk, h, 64, 64);
+  if (!ok) return -1;
+  w13.offsets = offsets; w13.E = E; w13.M = f; w13.Nw = h;
+  w13.out0 = static_cast<__nv_bfloat16*>(dW1); w13.out1 = static_cast<__nv_bfloat16*>(dW3);
+  w13.ld_out = f; w13.out_expert_stride = (long long)h * f; w13.status = status;
+  if (launch<WGRAD13>(w13, st)) return -1;
+
+  // dW2[e]^T = dY^T a  (stored as dW2[e][f][h])
+  TcParams w2 = blank_params();
+  ok = make_map(&w2.mapA0, dybuf, Tk, h, 64, 64) && make_map(&w2.mapB0, a, Tk, f, 64, 64);
+  if (!ok) return -1;
+  w2.offsets = offsets; w2.E = E; w2.M = h; w2.Nw = f;
+  w2.out0 = static_cast<__nv_bfloat16*>(dW2); w2.ld_out = h; w2.out_expert_stride = (long long)f * h;
+  w2.status = status;
+  return launch<WGRAD2>(w2, st);
+}
+
+}  // namespace moe

@@ -48,4 +48,14 @@ void simt_expert_ffn_bwd(int dtype, const void* dybuf, const void* xbuf, const v
                          const void* W3, const void* W2, int Tk, int E, int h, int f, void* dxbuf,
                          void* dW1, void* dW3, void* dW2, void* dh1, void* dh3, cudaStream_t st);
 
+// gemm_tc.cu -- tcgen05/TMEM/TMA grouped GEMMs (bf16; h and f multiples of 128)
+bool tc_supported(int dtype, int h, int f);
+int tc_expert_ffn(const void* xbuf, const int* offsets, const void* W1, const void* W3, const void* W2,
+                  int Tk, int E, int h, int f, void* ybuf, void* h1, void* h3, void* a, int* status,
+                  cudaStream_t st);
+int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const void* h3, const void* a,
+                      const int* offsets, const void* W1, const void* W3, const void* W2, int Tk, int E,
+                      int h, int f, void* dxbuf, void* dW1, void* dW3, void* dW2, void* dh1, void* dh3,
+                      int* status, cudaStream_t st);
+
 }  // namespace moe

@@ -246,7 +246,36 @@ EXPERT_SHAPES = [
     (200, 512, 16, 4, 256, torch.bfloat16, True),   # Zipf load: empty experts
     (97, 384, 40, 6, 128, torch.float32, True),     # many small segments at every residue
     (64, 256, 4, 1, 136, torch.bfloat16, False),    # f not a multiple of the tile
+    # tensor-core engine (bf16, h and f multiples of 128)
+    (333, 384, 12, 3, 256, torch.bfloat16, False),  # ragged segments below one chunk
+    (1000, 256, 4, 2, 128, torch.bfloat16, True),   # segments of several 256-row chunks, Zipf
+    (96, 640, 64, 6, 384, torch.bfloat16, True),    # many empty and tiny segments
 ]
+
+
+@pytest.mark.parametrize("T,h,E,k,f,skew", [(512, 256, 8, 2, 256, False), (700, 384, 16, 4, 128, True)])
+def test_tensor_core_engine_matches_simt_engine(B, monkeypatch, T, h, E, k, f, skew):
+    dt = torch.bfloat16
+    p, d = expert_inputs(T, h, E, k, f, dt, 90 + T, skew)
+    Tk = T * k
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, dt)
+    outs = {}
+    for engine in ("tc", "simt"):
+        if engine == "simt":
+            monkeypatch.setenv("MOE_PFT_GEMM", "simt")
+        else:
+            monkeypatch.delenv("MOE_PFT_GEMM", raising=False)
+        z = lambda *s: torch.empty(*s, dtype=dt, device="cuda")  # noqa: E731
+        o = {"ybuf": z(Tk, h), "h1": z(Tk, f), "h3": z(Tk, f), "a": z(Tk, f), "dxbuf": z(Tk, h),
+             "dW1": z(E, h, f), "dW3": z(E, h, f), "dW2": z(E, f, h)}
+        B.moe_expert_ffn(d["xbuf"], d["offsets"], d["W1"], d["W3"], d["W2"], o["ybuf"], o["h1"], o["h3"], o["a"], ws)
+        B.moe_expert_ffn_bwd(d["dybuf"], d["xbuf"], o["h1"], o["h3"], o["a"], d["offsets"], d["W1"], d["W3"],
+                             d["W2"], o["dxbuf"], o["dW1"], o["dW3"], o["dW2"], ws)
+        torch.cuda.synchronize()
+        outs[engine] = o
+    assert B.moe_check_status(ws) == 0
+    for n in outs["tc"]:
+        assert rel_l2(np64(outs["tc"][n]), np64(outs["simt"][n])) <= TOL["bf16"], n
 
 
 @pytest.mark.parametrize("T,h,E,k,f,dt,skew", EXPERT_SHAPES)
