@@ -2,7 +2,8 @@
 //
 // All four are row gathers: every row of h elements moves as 16-byte vectors, a group of
 // `tpr` threads per row (tpr is a power of two, 32..256, chosen so each thread handles at
-// most four vectors), `256 / tpr` rows per 256-thread block.  Loads are issued before the
+// most four vectors per pass; rows wider than 256 x 4 vectors take several passes),
+// `256 / tpr` rows per 256-thread block.  Loads are issued before the
 // dependent stores so that each thread keeps several 16-byte requests in flight.  Sums run
 // in fp32 in a fixed order (j ascending), so results are bitwise reproducible; no atomics.
 #include "common.cuh"
@@ -45,16 +46,18 @@ __global__ void __launch_bounds__(kBlock) dispatch_kernel(const T* __restrict__ 
     return;
   }
   const uint4* src = reinterpret_cast<const uint4*>(x) + (size_t)t * nvec;
-  uint4 r[kMaxVecPerThread];
+  for (int vb = 0; vb < nvec; vb += tpr * kMaxVecPerThread) {
+    uint4 r[kMaxVecPerThread];
 #pragma unroll
-  for (int u = 0; u < kMaxVecPerThread; ++u) {
-    const int v = lt + u * tpr;
-    if (v < nvec) r[u] = __ldg(src + v);
-  }
+    for (int u = 0; u < kMaxVecPerThread; ++u) {
+      const int v = vb + lt + u * tpr;
+      if (v < nvec) r[u] = __ldg(src + v);
+    }
 #pragma unroll
-  for (int u = 0; u < kMaxVecPerThread; ++u) {
-    const int v = lt + u * tpr;
-    if (v < nvec) dst[v] = r[u];
+    for (int u = 0; u < kMaxVecPerThread; ++u) {
+      const int v = vb + lt + u * tpr;
+      if (v < nvec) dst[v] = r[u];
+    }
   }
 }
 
@@ -72,40 +75,42 @@ __global__ void __launch_bounds__(kBlock) combine_kernel(const T* __restrict__ y
   const int lt = threadIdx.x % tpr;
   if (t >= T_) return;
   const uint4* yb = reinterpret_cast<const uint4*>(ybuf);
-  float acc[kMaxVecPerThread][VN];
+  uint4* dst = reinterpret_cast<uint4*>(y) + (size_t)t * nvec;
+  for (int vb = 0; vb < nvec; vb += tpr * kMaxVecPerThread) {
+    float acc[kMaxVecPerThread][VN];
 #pragma unroll
-  for (int u = 0; u < kMaxVecPerThread; ++u)
+    for (int u = 0; u < kMaxVecPerThread; ++u)
 #pragma unroll
-    for (int q = 0; q < VN; ++q) acc[u][q] = 0.f;
-  for (int j = 0; j < k; ++j) {
-    const int s = __ldg(slot_of + (size_t)t * k + j);
-    const float wj = __ldg(w + (size_t)t * k + j);
-    if ((unsigned)s >= (unsigned)Tk) {
-      if (lt == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
-      continue;
-    }
-    uint4 r[kMaxVecPerThread];
+      for (int q = 0; q < VN; ++q) acc[u][q] = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int s = __ldg(slot_of + (size_t)t * k + j);
+      const float wj = __ldg(w + (size_t)t * k + j);
+      if ((unsigned)s >= (unsigned)Tk) {
+        if (lt == 0 && vb == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
+        continue;
+      }
+      uint4 r[kMaxVecPerThread];
 #pragma unroll
-    for (int u = 0; u < kMaxVecPerThread; ++u) {
-      const int v = lt + u * tpr;
-      if (v < nvec) r[u] = __ldg(yb + (size_t)s * nvec + v);
-    }
+      for (int u = 0; u < kMaxVecPerThread; ++u) {
+        const int v = vb + lt + u * tpr;
+        if (v < nvec) r[u] = __ldg(yb + (size_t)s * nvec + v);
+      }
 #pragma unroll
-    for (int u = 0; u < kMaxVecPerThread; ++u) {
-      const int v = lt + u * tpr;
-      if (v < nvec) {
-        float f[VN];
-        unpack(r[u], f, T());
+      for (int u = 0; u < kMaxVecPerThread; ++u) {
+        const int v = vb + lt + u * tpr;
+        if (v < nvec) {
+          float f[VN];
+          unpack(r[u], f, T());
 #pragma unroll
-        for (int q = 0; q < VN; ++q) acc[u][q] = fmaf(wj, f[q], acc[u][q]);
+          for (int q = 0; q < VN; ++q) acc[u][q] = fmaf(wj, f[q], acc[u][q]);
+        }
       }
     }
-  }
-  uint4* dst = reinterpret_cast<uint4*>(y) + (size_t)t * nvec;
 #pragma unroll
-  for (int u = 0; u < kMaxVecPerThread; ++u) {
-    const int v = lt + u * tpr;
-    if (v < nvec) dst[v] = pack(acc[u], T());
+    for (int u = 0; u < kMaxVecPerThread; ++u) {
+      const int v = vb + lt + u * tpr;
+      if (v < nvec) dst[v] = pack(acc[u], T());
+    }
   }
 }
 
@@ -121,49 +126,51 @@ __global__ void __launch_bounds__(kBlock) dispatch_bwd_kernel(
   const int lt = threadIdx.x % tpr;
   if (t >= T_) return;
   const uint4* src = reinterpret_cast<const uint4*>(dxbuf);
-  float acc[kMaxVecPerThread][VN];
-#pragma unroll
-  for (int u = 0; u < kMaxVecPerThread; ++u) {
-    const int v = lt + u * tpr;
-#pragma unroll
-    for (int q = 0; q < VN; ++q) acc[u][q] = 0.f;
-    if (dx_add != nullptr && v < nvec) {
-      const float4* a4 = reinterpret_cast<const float4*>(dx_add + ((size_t)t * nvec + v) * VN);
-#pragma unroll
-      for (int q = 0; q < VN / 4; ++q) {
-        const float4 a = __ldg(a4 + q);
-        acc[u][4 * q] = a.x; acc[u][4 * q + 1] = a.y; acc[u][4 * q + 2] = a.z; acc[u][4 * q + 3] = a.w;
-      }
-    }
-  }
-  for (int j = 0; j < k; ++j) {
-    const int s = __ldg(slot_of + (size_t)t * k + j);
-    if ((unsigned)s >= (unsigned)Tk) {
-      if (lt == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
-      continue;
-    }
-    uint4 r[kMaxVecPerThread];
-#pragma unroll
-    for (int u = 0; u < kMaxVecPerThread; ++u) {
-      const int v = lt + u * tpr;
-      if (v < nvec) r[u] = __ldg(src + (size_t)s * nvec + v);
-    }
-#pragma unroll
-    for (int u = 0; u < kMaxVecPerThread; ++u) {
-      const int v = lt + u * tpr;
-      if (v < nvec) {
-        float f[VN];
-        unpack(r[u], f, T());
-#pragma unroll
-        for (int q = 0; q < VN; ++q) acc[u][q] += f[q];
-      }
-    }
-  }
   uint4* dst = reinterpret_cast<uint4*>(dx) + (size_t)t * nvec;
+  for (int vb = 0; vb < nvec; vb += tpr * kMaxVecPerThread) {
+    float acc[kMaxVecPerThread][VN];
 #pragma unroll
-  for (int u = 0; u < kMaxVecPerThread; ++u) {
-    const int v = lt + u * tpr;
-    if (v < nvec) dst[v] = pack(acc[u], T());
+    for (int u = 0; u < kMaxVecPerThread; ++u) {
+      const int v = vb + lt + u * tpr;
+#pragma unroll
+      for (int q = 0; q < VN; ++q) acc[u][q] = 0.f;
+      if (dx_add != nullptr && v < nvec) {
+        const float4* a4 = reinterpret_cast<const float4*>(dx_add + ((size_t)t * nvec + v) * VN);
+#pragma unroll
+        for (int q = 0; q < VN / 4; ++q) {
+          const float4 a = __ldg(a4 + q);
+          acc[u][4 * q] = a.x; acc[u][4 * q + 1] = a.y; acc[u][4 * q + 2] = a.z; acc[u][4 * q + 3] = a.w;
+        }
+      }
+    }
+    for (int j = 0; j < k; ++j) {
+      const int s = __ldg(slot_of + (size_t)t * k + j);
+      if ((unsigned)s >= (unsigned)Tk) {
+        if (lt == 0 && vb == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
+        continue;
+      }
+      uint4 r[kMaxVecPerThread];
+#pragma unroll
+      for (int u = 0; u < kMaxVecPerThread; ++u) {
+        const int v = vb + lt + u * tpr;
+        if (v < nvec) r[u] = __ldg(src + (size_t)s * nvec + v);
+      }
+#pragma unroll
+      for (int u = 0; u < kMaxVecPerThread; ++u) {
+        const int v = vb + lt + u * tpr;
+        if (v < nvec) {
+          float f[VN];
+          unpack(r[u], f, T());
+#pragma unroll
+          for (int q = 0; q < VN; ++q) acc[u][q] += f[q];
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kMaxVecPerThread; ++u) {
+      const int v = vb + lt + u * tpr;
+      if (v < nvec) dst[v] = pack(acc[u], T());
+    }
   }
 }
 
@@ -184,12 +191,12 @@ __global__ void __launch_bounds__(kBlock) combine_bwd_kernel(
   float dwp[KMAX];
 #pragma unroll
   for (int j = 0; j < KMAX; ++j) dwp[j] = 0.f;
-  if (active) {
+  for (int vb = 0; active && vb < nvec; vb += tpr * kMaxVecPerThread) {
     float g[kMaxVecPerThread][VN];
     const uint4* dyv = reinterpret_cast<const uint4*>(dy) + (size_t)t * nvec;
 #pragma unroll
     for (int u = 0; u < kMaxVecPerThread; ++u) {
-      const int v = lt + u * tpr;
+      const int v = vb + lt + u * tpr;
       if (v < nvec) unpack(__ldg(dyv + v), g[u], T());
     }
     const uint4* yb = reinterpret_cast<const uint4*>(ybuf);
@@ -200,18 +207,18 @@ __global__ void __launch_bounds__(kBlock) combine_bwd_kernel(
       const int s = __ldg(slot_of + (size_t)t * k + j);
       const float wj = __ldg(w + (size_t)t * k + j);
       if ((unsigned)s >= (unsigned)Tk) {
-        if (lt == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
+        if (lt == 0 && vb == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
         continue;
       }
       uint4 r[kMaxVecPerThread];
 #pragma unroll
       for (int u = 0; u < kMaxVecPerThread; ++u) {
-        const int v = lt + u * tpr;
+        const int v = vb + lt + u * tpr;
         if (v < nvec) r[u] = __ldg(yb + (size_t)s * nvec + v);
       }
 #pragma unroll
       for (int u = 0; u < kMaxVecPerThread; ++u) {
-        const int v = lt + u * tpr;
+        const int v = vb + lt + u * tpr;
         if (v < nvec) {
           float f[VN], o[VN];
           unpack(r[u], f, T());
