@@ -82,8 +82,12 @@ def test_full_layer_small_workloads(M, cfg):
     for n in ("num_ids", "offsets", "token_ids", "expert_ids", "slot_of"):
         np.testing.assert_array_equal(npi(getattr(b, n)), fw[n], err_msg=n)
     np.testing.assert_array_equal(np64(b.xbuf), fw["xbuf"])
-    for n in ("probs", "topk_w", "d_topk_w", "d_logits", "dWg", "dx_router"):
-        assert rel_l2(np64(getattr(b, n)), fw[n] if n in fw else bw[n]) <= TOL["f32"], n
+    for n in ("probs", "topk_w"):
+        assert rel_l2(np64(getattr(b, n)), fw[n]) <= TOL["f32"], n
+    # stored in fp32, but d_topk_w = <dy, ybuf> carries ybuf's rounding in the layer's dtype,
+    # and the gate gradients below it inherit that
+    for n in ("d_topk_w", "d_logits", "dWg", "dx_router"):
+        assert rel_l2(np64(getattr(b, n)), bw[n]) <= TOL[dn], n
     for n in ("h1", "h3", "a", "ybuf", "y"):
         assert rel_l2(np64(getattr(b, n)), fw[n]) <= TOL[dn], n
     for n in ("dybuf", "dxbuf", "dW1", "dW3", "dW2", "dx"):
@@ -125,7 +129,7 @@ def test_full_size_layer_sampled(M, cfg, ntok, nexp):
     dy = np64(inp["dy"])
     bw = O.layer_backward(fw, x[S], Wg, W1, W3, W2, dy[S], dn)
     assert rel_l2(np64(b.dx[S]), bw["dx"]) <= TOL[dn]
-    assert rel_l2(np64(b.d_topk_w[S]), bw["d_topk_w"]) <= TOL["f32"]
+    assert rel_l2(np64(b.d_topk_w[S]), bw["d_topk_w"]) <= TOL[dn]
 
     # weight gradients of sampled experts whose token set is unambiguous
     ex_idx = O.topk(exact, w.k)
@@ -173,7 +177,7 @@ def test_edge_case_layers(M, T, h, E, k, f, dt):
     assert rel_l2(np64(b.y), fw["y"]) <= TOL[dn]
     for n in ("dx", "dW1", "dW3", "dW2"):
         assert rel_l2(np64(getattr(b, n)), bw[n]) <= TOL[dn], n
-    assert rel_l2(np64(b.dWg), bw["dWg"]) <= TOL["f32"]
+    assert rel_l2(np64(b.dWg), bw["dWg"]) <= TOL[dn]
 
 
 def test_layer_step_is_bitwise_deterministic(M):
