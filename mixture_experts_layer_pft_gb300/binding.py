@@ -36,6 +36,7 @@ SIGNATURES = {
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_route_bwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_pft_build": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_pft_build_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_dispatch_bwd": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
@@ -142,6 +143,14 @@ def moe_pft_build(topk_idx, E, num_ids, offsets, token_ids, expert_ids, slot_of,
     T, k = topk_idx.shape
     _call("moe_pft_build", _p(topk_idx), T, E, k, _p(num_ids), _p(offsets), _p(token_ids),
           _p(expert_ids), _p(slot_of), _p(ws), ws.numel(), _stream())
+
+
+def moe_pft_build_noalloc(topk_idx, E, num_ids, offsets, token_ids, expert_ids, slot_of):
+    """moe_pft_build without a workspace: its scratch is the library's static device array,
+    for callers that cannot allocate.  Calls that overlap on the GPU race."""
+    T, k = topk_idx.shape
+    _call("moe_pft_build_noalloc", _p(topk_idx), T, E, k, _p(num_ids), _p(offsets), _p(token_ids),
+          _p(expert_ids), _p(slot_of), _stream())
 
 
 def moe_dispatch(x, token_ids, k, xbuf, ws):

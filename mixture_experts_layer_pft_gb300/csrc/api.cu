@@ -65,6 +65,8 @@ static std::atomic<unsigned long long> g_launches{0};
 
 void count_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
+void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 int num_sms() {
   static int cached[64] = {0};
   int dev = 0;

@@ -8,6 +8,7 @@ namespace moe {
 
 int num_sms();  // SM count of the current device (cached per device)
 void count_launch(int n = 1);  // adds to the moe_kernel_launches counter
+void set_last_error(const char* msg);  // the text moe_last_error() returns on this thread
 
 // gather.cu
 void launch_dispatch(int dtype, const void* x, const int* token_ids, int T, int rows, int h,
