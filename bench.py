@@ -256,6 +256,66 @@ def workload_desc(w):
             f"{'fwd+bwd' if w.backward else 'fwd only'}{', Zipf router bias' if w.skew else ''}")
 
 
+CSRC = "mixture_experts_layer_pft_gb300/csrc/"
+
+
+def kernel_names(stage, n, w):
+    """Names (and source file) of the n launches one stage call makes, in launch order."""
+    tc = w.dtype == "bf16" and w.h % 128 == 0 and w.f % 128 == 0 and os.environ.get("MOE_PFT_GEMM") != "simt"
+    table = {
+        "route": (["router_gemm", "softmax_topk"] if n == 2 else ["router_gemm", "router_splitk_reduce", "softmax_topk"],
+                  CSRC + "gemm_simt.cu"),
+        "pft_build": (["pft_hist", "pft_scatter"], CSRC + "pft.cu"),
+        "dispatch": (["dispatch"], CSRC + "gather.cu"),
+        "expert_ffn": ((["tc_GATEUP", "tc_DOWN"], CSRC + "gemm_tc.cu") if tc
+                       else (["simt_gateup", "simt_down"], CSRC + "gemm_simt.cu")),
+        "combine": (["combine"], CSRC + "gather.cu"),
+        "combine_bwd": (["combine_bwd"], CSRC + "gather.cu"),
+        "expert_ffn_bwd": ((["tc_DA", "tc_DX", "tc_WGRAD13", "tc_WGRAD2"], CSRC + "gemm_tc.cu") if tc
+                           else (["simt_dA", "simt_dX", "simt_dW13", "simt_dW2"], CSRC + "gemm_simt.cu")),
+        "route_bwd": ((["route_dlogits", "router_dwg", "router_dx"] if n == 3
+                       else ["route_dlogits", "router_dwg", "router_dwg_splitk_reduce", "router_dx"]),
+                      CSRC + "gemm_simt.cu"),
+        "dispatch_bwd": (["dispatch_bwd"], CSRC + "gather.cu"),
+    }
+    names, src = table[stage]
+    assert len(names) == n, (stage, n, names)
+    return names, src
+
+
+def kernel_counts(w, T, e_active, binding=None):
+    """Algorithmic FLOPs and HBM bytes of one launch of each kernel."""
+    s = 2 if w.dtype == "bf16" else 4
+    h, E, k, f = w.h, w.E, w.k, w.f
+    Tk = T * k
+    Wb = h * f * s  # bytes of one expert's weight matrix
+    d = {
+        "router_gemm": {"flops": 2 * T * h * E, "bytes": T * h * s + h * E * 4 + T * E * 4},
+        "router_splitk_reduce": {"flops": 0, "bytes": 2 * T * E * 4},
+        "softmax_topk": {"flops": 0, "bytes": 2 * T * E * 4 + 8 * Tk},
+        "pft_hist": {"flops": 0, "bytes": 4 * Tk},
+        "pft_scatter": {"flops": 0, "bytes": 16 * Tk},
+        "dispatch": {"flops": 0, "bytes": T * h * s + Tk * h * s + 4 * Tk},
+        "tc_GATEUP": {"flops": 4 * Tk * h * f, "bytes": 2 * e_active * Wb + Tk * h * s + 3 * Tk * f * s},
+        "tc_DOWN": {"flops": 2 * Tk * h * f, "bytes": e_active * Wb + Tk * f * s + Tk * h * s},
+        "combine": {"flops": 2 * Tk * h, "bytes": Tk * h * s + T * h * s + 8 * Tk},
+        "combine_bwd": {"flops": 3 * Tk * h, "bytes": T * h * s + 2 * Tk * h * s + 12 * Tk},
+        "tc_DA": {"flops": 2 * Tk * h * f, "bytes": e_active * Wb + Tk * h * s + 4 * Tk * f * s},
+        "tc_DX": {"flops": 4 * Tk * h * f, "bytes": 2 * e_active * Wb + 2 * Tk * f * s + Tk * h * s},
+        "tc_WGRAD13": {"flops": 4 * Tk * h * f, "bytes": Tk * h * s + 2 * Tk * f * s + 2 * E * Wb},
+        "tc_WGRAD2": {"flops": 2 * Tk * h * f, "bytes": Tk * h * s + Tk * f * s + E * Wb},
+        "route_dlogits": {"flops": 0, "bytes": 2 * T * E * 4 + 12 * Tk},
+        "router_dwg": {"flops": 2 * T * h * E, "bytes": T * h * s + T * E * 4 + h * E * 4},
+        "router_dwg_splitk_reduce": {"flops": 0, "bytes": 2 * h * E * 4},
+        "router_dx": {"flops": 2 * T * h * E, "bytes": T * E * 4 + h * E * 4 + T * h * 4},
+        "dispatch_bwd": {"flops": 0, "bytes": Tk * h * s + T * h * s + T * h * 4 + 4 * Tk},
+    }
+    for a, bname in (("simt_gateup", "tc_GATEUP"), ("simt_down", "tc_DOWN"), ("simt_dA", "tc_DA"),
+                     ("simt_dX", "tc_DX"), ("simt_dW13", "tc_WGRAD13"), ("simt_dW2", "tc_WGRAD2")):
+        d[a] = d[bname]
+    return d
+
+
 def run_ours(args, w):
     import torch
 
@@ -279,8 +339,9 @@ def run_ours(args, w):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)  # 2x the 129 MB L2
     stream = torch.cuda.current_stream()
 
-    def run_stages(ev):
-        """One step with an event before each stage call and one after the last."""
+    def run_stages(ev, timer=None, spans=None):
+        """One step with an event before each stage call and one after the last.  With a
+        kernel timer, spans[i] = (first, last) ring index of the launches call i made."""
         calls = [
             lambda: binding.moe_route(inp["x"], inp["Wg"], inp["bias"], w.k, b.logits, b.probs,
                                       b.topk_idx, b.topk_w, b.ws),
@@ -305,7 +366,10 @@ def run_ours(args, w):
         for i, c in enumerate(calls):
             if ev is not None:
                 ev[i].record(stream)
+            n0 = timer.count() if timer else 0
             c()
+            if timer is not None:
+                spans.append((n0, timer.count()))
         if ev is not None:
             ev[len(calls)].record(stream)
 
@@ -316,16 +380,19 @@ def run_ours(args, w):
     assert binding.moe_check_status(b.ws) == 0, "device status set during warm-up"
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    timer = binding.KernelTimer(64 * args.steps)
+    spans = [[] for _ in range(args.steps)]
     clocks = ClockSampler(device.index)
     clocks.start()
     n_launch0 = lib.moe_kernel_launches()
-    barrier(world)
-    torch.cuda.synchronize()
-    for s in range(args.steps):
-        flush.zero_()  # evict L2 between steps (not timed: outside the step's events)
-        run_stages(events[s])
-    torch.cuda.synchronize()
-    barrier(world)
+    with timer:
+        barrier(world)
+        torch.cuda.synchronize()
+        for s in range(args.steps):
+            flush.zero_()  # evict L2 between steps (not timed: outside the step's events)
+            run_stages(events[s], timer, spans[s])
+        torch.cuda.synchronize()
+        barrier(world)
     launches = lib.moe_kernel_launches() - n_launch0
     clk = clocks.stop()
     assert binding.moe_check_status(b.ws) == 0, "device status set during the timed region"
@@ -347,33 +414,58 @@ def run_ours(args, w):
         if c["flops"] and n.startswith(("expert", "route")):
             stages[n]["TFLOP/s"] = round(c["flops"] / (avg * 1e-3) / 1e12, 2)
 
-    # ---------------------------------------------------------------- roofline of the dominant call
+    # ---------------------------------------------------------------- per-kernel times (event ring)
+    e_active = int((b.num_ids > 0).sum().item())
+    kern_ms = {}  # kernel name -> list of durations (ms)
+    kern_src = {}
+    for s in range(args.steps):
+        for i, (a0, a1) in enumerate(spans[s]):
+            names, src = kernel_names(STAGES[i], a1 - a0, w)
+            prev = events[s][i]
+            for j, q in enumerate(range(a0, a1)):
+                ev = timer.event(q)
+                kern_ms.setdefault(names[j], []).append(prev.elapsed_time(ev))
+                kern_src[names[j]] = src
+                prev = ev
+    kernels = {}
+    kc = kernel_counts(w, T, e_active, binding)
+    for n, ms in kern_ms.items():
+        avg = sum(ms) / len(ms)
+        c = kc.get(n, {"flops": 0, "bytes": 0})
+        kernels[n] = {"us": round(1e3 * avg, 2), "GB/s": round(c["bytes"] / (avg * 1e-3) / 1e9, 1)}
+        if c["flops"]:
+            kernels[n]["TFLOP/s"] = round(c["flops"] / (avg * 1e-3) / 1e12, 2)
+
+    # ---------------------------------------------------------------- roofline of the dominant kernel
     peaks, peak_src = read_peaks()
-    dom = max(stage_ms, key=lambda n: sum(stage_ms[n]))
-    dom_ms = sum(stage_ms[dom]) / len(stage_ms[dom])
-    c = counts[dom]
-    gemm_src = ["mixture_experts_layer_pft_gb300/csrc/gemm_simt.cu",
-                "mixture_experts_layer_pft_gb300/csrc/common.cuh"]
-    if dom.startswith("expert") and w.dtype == "bf16":
-        peak = float(peaks.get("bf16_tflops_sustained" if args.steps * dom_ms > 2000 else "bf16_tflops"))
-        roof = {"bound": "tensor", "achieved": c["flops"] / (dom_ms * 1e-3) / 1e12, "peak": peak,
-                "unit": "TFLOP/s"}
-        which = "bf16_tflops (burst)" if args.steps * dom_ms <= 2000 else "bf16_tflops_sustained"
-    elif dom.startswith("expert"):
+    dom = max(kern_ms, key=lambda n: sum(kern_ms[n]) / len(kern_ms[n]))
+    dom_ms = sum(kern_ms[dom]) / len(kern_ms[dom])
+    c = kc[dom]
+    region_ms = ms_per_step * args.steps
+    fkey = "bf16_tflops_sustained" if region_ms > 2000 else "bf16_tflops"
+    if dom.startswith("simt") or (dom.startswith("router") and not dom.endswith("reduce")):
         roof = {"bound": "alu", "achieved": c["flops"] / (dom_ms * 1e-3) / 1e12,
                 "peak": FP32_ALU_TFLOPS_NOMINAL, "unit": "TFLOP/s"}
-        which = "FP32 FMA: 152 SMs x 128 lanes x 2 x 2.07 GHz (derived)"
+        which = "derived FP32 FMA peak: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (nominal)"
     else:
-        roof = {"bound": "hbm", "achieved": c["bytes"] / (dom_ms * 1e-3) / 1e9,
-                "peak": float(peaks.get("hbm_gbs")), "unit": "GB/s"}
-        which = "hbm_gbs"
+        t_tensor = c["flops"] / (float(peaks[fkey]) * 1e12) if c["flops"] else 0.0
+        t_hbm = c["bytes"] / (float(peaks["hbm_gbs"]) * 1e9)
+        if t_tensor > t_hbm:
+            roof = {"bound": "tensor", "achieved": c["flops"] / (dom_ms * 1e-3) / 1e12,
+                    "peak": float(peaks[fkey]), "unit": "TFLOP/s"}
+            which = f"MEASURED_PEAKS.json {fkey} ({'of measured' if peak_src == 'measured' else 'of fallback'})"
+        else:
+            roof = {"bound": "hbm", "achieved": c["bytes"] / (dom_ms * 1e-3) / 1e9,
+                    "peak": float(peaks["hbm_gbs"]), "unit": "GB/s"}
+            which = f"MEASURED_PEAKS.json hbm_gbs ({'of measured' if peak_src == 'measured' else 'of fallback'})"
+        if c["flops"]:
+            roof["tensor_frac"] = c["flops"] / (dom_ms * 1e-3) / (float(peaks[fkey]) * 1e12)
     roof["frac"] = roof["achieved"] / roof["peak"]
-    key = f"{dom}:{w.name}"
-    roof["traffic"] = recorded_traffic(key, source_hash(gemm_src))
-    roof["kernel"] = f"moe_{dom} call ({'2' if dom == 'expert_ffn' else '4'} grouped-GEMM launches)" \
-        if dom.startswith("expert") else f"moe_{dom} call"
-    roof["peak_source"] = f"{'MEASURED_PEAKS.json' if peak_src == 'measured' and roof['bound'] != 'alu' else 'derived'} {which} ({'of measured' if peak_src == 'measured' and roof['bound'] != 'alu' else 'of fallback' if roof['bound'] != 'alu' else 'nominal'})"
-    roof["algorithmic_per_launch"] = c["flops"] if roof["unit"] == "TFLOP/s" else c["bytes"]
+    roof["traffic"] = recorded_traffic(f"{dom}:{w.name}", source_hash([kern_src[dom]]))
+    roof["kernel"] = dom
+    roof["launch_us"] = round(1e3 * dom_ms, 2)
+    roof["peak_source"] = which
+    roof["algorithmic_per_launch"] = {"flops": c["flops"], "bytes": c["bytes"]}
 
     # ---------------------------------------------------------------- end to end through host buffers
     e2e = None
@@ -429,6 +521,7 @@ def run_ours(args, w):
                        "l2": "flushed between timed steps (256 MB write, outside the step events)",
                        "parallelism": f"replicas x{world} (independent tokens, no data-path collective)"},
             "stages": stages,
+            "kernels": kernels,
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -97,6 +97,17 @@ int moe_abi_version(void);
  * devices, all host threads; an atomic counter, the only process-wide state it keeps). */
 uint64_t moe_kernel_launches(void);
 
+/* Diagnostic per-kernel timing.  `events` is a host array of `capacity` cudaEvent_t handles
+ * (created by the caller with timing enabled; the caller keeps the array and the events alive
+ * while installed).  While installed, right after its n-th kernel launch (n counting from 0 at
+ * installation) the library records events[n % capacity] on the stream of that launch, so the
+ * time between consecutive records is one kernel's duration in stream order.  NULL uninstalls.
+ * Process-wide; install and use it from one host thread at a time. */
+int moe_profile_events(void* const* events, int capacity);
+
+/* Launches recorded since the current moe_profile_events installation. */
+uint64_t moe_profile_count(void);
+
 /*
  * Gate -- X-MoE review §3 "Training pipeline" step 2 (padding-free gating, no dispatch_mask)
  * and the FlashDMoE blog §1.1 "DMoE operator definition" (each token picks a few experts).

@@ -29,6 +29,8 @@ _P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
 SIGNATURES = {
     "moe_abi_version": (_I, []),
     "moe_kernel_launches": (ctypes.c_uint64, []),
+    "moe_profile_events": (_I, [ctypes.POINTER(ctypes.c_void_p), _I]),
+    "moe_profile_count": (ctypes.c_uint64, []),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_status_reset": (_I, [_P, _P]),
@@ -107,6 +109,35 @@ def workspace_size(op: int, T: int, h: int, E: int, k: int, f: int, dtype: torch
 def new_workspace(op: int, T: int, h: int, E: int, k: int, f: int, dtype: torch.dtype, device="cuda"):
     """A zeroed uint8 workspace of moe_workspace_size bytes (status word cleared)."""
     return torch.zeros(workspace_size(op, T, h, E, k, f, dtype), dtype=torch.uint8, device=device)
+
+
+class KernelTimer:
+    """Per-kernel CUDA-event timing through moe_profile_events: the library records one event
+    after each of its launches, on the launching stream."""
+
+    def __init__(self, capacity: int):
+        stream = torch.cuda.current_stream()
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(capacity)]
+        for e in self.events:  # materialise the underlying cudaEvent_t
+            e.record(stream)
+        self._handles = (ctypes.c_void_p * capacity)(*[e.cuda_event for e in self.events])
+        self.capacity = capacity
+
+    def __enter__(self):
+        rc = lib().moe_profile_events(self._handles, self.capacity)
+        if rc != MOE_OK:
+            raise MoEError("moe_profile_events", rc, (lib().moe_last_error() or b"").decode())
+        return self
+
+    def count(self) -> int:
+        return int(lib().moe_profile_count())
+
+    def event(self, n: int):
+        return self.events[n % self.capacity]
+
+    def __exit__(self, *exc):
+        lib().moe_profile_events(None, 0)
+        return False
 
 
 def moe_status_reset(ws):

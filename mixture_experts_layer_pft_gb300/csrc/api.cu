@@ -63,7 +63,18 @@ bool use_tensor_cores(int dtype, int h, int f) {
 
 static std::atomic<unsigned long long> g_launches{0};
 
-void count_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+// Timing ring installed by moe_profile_events (diagnostic; one host thread at a time).
+static cudaEvent_t* g_prof_events = nullptr;
+static int g_prof_capacity = 0;
+static std::atomic<unsigned long long> g_prof_count{0};
+
+void count_launch(cudaStream_t st) {
+  g_launches.fetch_add(1ull, std::memory_order_relaxed);
+  if (g_prof_events != nullptr && g_prof_capacity > 0) {
+    const unsigned long long n = g_prof_count.fetch_add(1ull, std::memory_order_relaxed);
+    cudaEventRecord(g_prof_events[n % (unsigned long long)g_prof_capacity], st);
+  }
+}
 
 void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
 
@@ -90,12 +101,33 @@ int moe_abi_version(void) { return MOE_PFT_ABI_VERSION; }
 
 uint64_t moe_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int moe_profile_events(void* const* events, int capacity) {
+  if (events != nullptr && capacity <= 0) {
+    set_last_error("moe_profile_events: capacity must be positive");
+    return MOE_ERR_INVALID_ARG;
+  }
+  g_prof_events = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(events));
+  g_prof_capacity = events ? capacity : 0;
+  g_prof_count.store(0ull, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+uint64_t moe_profile_count(void) { return g_prof_count.load(std::memory_order_relaxed); }
+
 const char* moe_last_error(void) { return g_err; }
 
 size_t moe_workspace_size(int op, int T, int h, int E, int k, int f, int dtype) {
   const size_t hdr = sizeof(WsHeader);
   const long long Tk = (long long)std::max(T, 0) * std::max(k, 0);
   switch (op) {
+    case MOE_OP_ROUTE: {
+      const int sp = (T > 0 && h > 0 && E > 0) ? router_splits(T, E, h) : 1;
+      return hdr + (sp > 1 ? round256((size_t)sp * T * E * sizeof(float)) : 0);
+    }
+    case MOE_OP_ROUTE_BWD: {
+      const int sp = (T > 0 && h > 0 && E > 0) ? router_splits(h, E, T) : 1;
+      return hdr + (sp > 1 ? round256((size_t)sp * h * E * sizeof(float)) : 0);
+    }
     case MOE_OP_PFT_BUILD:
       return hdr + round256(pft_scratch_bytes(std::max(Tk, 1LL), std::max(E, 1)));
     case MOE_OP_EXPERT_FFN_BWD:
@@ -146,7 +178,8 @@ int moe_route(const void* x, const float* Wg, const float* bias, int T, int h, i
     REQUIRE(h >= 8 && h % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_route: h must be a multiple of 8");
     REQUIRE(E % 4 == 0, MOE_ERR_UNSUPPORTED, "moe_route: E must be a multiple of 4");
     REQUIRE(bias == nullptr || aligned16(bias), MOE_ERR_INVALID_ARG, "moe_route: bias not aligned");
-    simt_router_logits(dtype, x, Wg, bias, T, h, E, logits, st);
+    float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + sizeof(WsHeader));
+    simt_router_logits(dtype, x, Wg, bias, T, h, E, logits, partial, st);
   }
   launch_softmax_topk(logits, T, E, k, probs, topk_idx, topk_w, st);
   return check_launch("moe_route");
@@ -172,7 +205,8 @@ int moe_route_bwd(const void* x, const float* Wg, const float* probs, const int3
   REQUIRE(dx_router == nullptr || aligned16(dx_router), MOE_ERR_INVALID_ARG,
           "moe_route_bwd: dx_router not aligned");
   launch_route_dlogits(probs, topk_idx, d_topk_w, T, E, k, d_logits, status_of(ws), st);
-  simt_router_dwg(dtype, x, d_logits, T, h, E, dWg, st);
+  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + sizeof(WsHeader));
+  simt_router_dwg(dtype, x, d_logits, T, h, E, dWg, partial, st);
   if (dx_router) simt_router_dx(d_logits, Wg, T, h, E, dx_router, st);
   return check_launch("moe_route_bwd");
 }

@@ -256,7 +256,7 @@ void launch_dispatch_t(const void* x, const int* token_ids, int T_, int rows, in
   const int grid = (rows + g.rows_per_block - 1) / g.rows_per_block;
   dispatch_kernel<T><<<grid, kBlock, 0, st>>>(static_cast<const T*>(x), token_ids, T_, rows,
                                               nvec, g.tpr, static_cast<T*>(xbuf), status);
-  count_launch();
+  count_launch(st);
 }
 
 template <typename T>
@@ -267,7 +267,7 @@ void launch_combine_t(const void* ybuf, const int* slot_of, const float* w, int 
   const int grid = (T_ + g.rows_per_block - 1) / g.rows_per_block;
   combine_kernel<T><<<grid, kBlock, 0, st>>>(static_cast<const T*>(ybuf), slot_of, w, T_, k,
                                              nvec, g.tpr, T_ * k, static_cast<T*>(y), status);
-  count_launch();
+  count_launch(st);
 }
 
 template <typename T>
@@ -279,7 +279,7 @@ void launch_dispatch_bwd_t(const void* dxbuf, const int* slot_of, const float* d
   dispatch_bwd_kernel<T><<<grid, kBlock, 0, st>>>(static_cast<const T*>(dxbuf), slot_of, dx_add,
                                                   T_, k, nvec, g.tpr, T_ * k,
                                                   static_cast<T*>(dx), status);
-  count_launch();
+  count_launch(st);
 }
 
 template <typename T, int KMAX>
@@ -292,7 +292,7 @@ void launch_combine_bwd_k(const void* dy, const void* ybuf, const int* slot_of, 
   combine_bwd_kernel<T, KMAX><<<grid, kBlock, 0, st>>>(
       static_cast<const T*>(dy), static_cast<const T*>(ybuf), slot_of, w, T_, k, nvec, g.tpr,
       T_ * k, static_cast<T*>(dybuf), d_w, status);
-  count_launch();
+  count_launch(st);
 }
 
 template <typename T>

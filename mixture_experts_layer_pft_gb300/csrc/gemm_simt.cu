@@ -13,7 +13,12 @@
 //   KSEG: C_g[M,N] = A_seg^T * B_seg, K = the segment's rows -- the weight gradients
 //         (A, B stored [rows, M] / [rows, N]).  An empty segment writes zeros.
 // DUAL computes two products that share A (C = A*B0, C2 = A*B1) for the SwiGLU pair.
+// SPLIT-K (router GEMMs, whose N = E is small): gridDim.z CTAs share one output tile, each
+// over a contiguous slice of K, and write fp32 partials; splitk_reduce_kernel then adds the
+// slices in a fixed order (and the bias), so the result does not depend on scheduling.
 #include <string.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 #include "internal.h"
@@ -46,6 +51,8 @@ struct Args {
   const void* X1;     // DSWIGLU: stored h1
   const void* X2;     // DSWIGLU: stored h3
   const float* bias;  // EPI_BIAS: [N]
+  int splits;         // > 1: write fp32 partials [splits][rows][N] to `partial`
+  float* partial;
 };
 
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
@@ -121,6 +128,13 @@ __global__ void __launch_bounds__(NT, 1) simt_gemm_kernel(const Args args) {
     rows_valid = min(BM, seg_end - (int)row0);
     Ktot = args.K0 + args.K1;
   }
+  // this CTA's slice of K (all of it without split-K); slices are multiples of BK
+  int kbeg = 0, kend = Ktot;
+  if (args.splits > 1) {
+    const int per = (((Ktot + args.splits - 1) / args.splits) + BK - 1) / BK * BK;
+    kbeg = min(Ktot, (int)blockIdx.z * per);
+    kend = min(Ktot, kbeg + per);
+  }
   const TA* A0 = static_cast<const TA*>(args.A0);
   const TA* A1 = static_cast<const TA*>(args.A1);
   const TB* B0 = static_cast<const TB*>(args.B0);
@@ -137,7 +151,7 @@ __global__ void __launch_bounds__(NT, 1) simt_gemm_kernel(const Args args) {
       // A stored [rows, lda]: 8 token rows x 128 m; B stored [rows, ldb]: 8 x 128 n
       const int kr = tid >> 5, c4 = (tid & 31) * 4;
       const int tok = kb + k0 + kr;
-      const bool kv = tok < ke;
+      const bool kv = tok < ke && k0 + kr < kend;
       ra = (kv && m0 + c4 < args.M) ? load4(A0 + (size_t)tok * args.lda + m0 + c4) : zero4();
       const bool nv = kv && n0 + c4 < N;
       rb = nv ? load4(B0 + (size_t)tok * args.ldb + n0 + c4) : zero4();
@@ -149,17 +163,17 @@ __global__ void __launch_bounds__(NT, 1) simt_gemm_kernel(const Args args) {
       const int kl = seg1 ? k0 - args.K0 : k0;
       {
         const int r = tid >> 1, kc = (tid & 1) * 4;
-        const bool v = r < rows_valid && k0 + kc < Ktot;
+        const bool v = r < rows_valid && k0 + kc < kend;
         ra = v ? load4(Ab + (row0 + r) * (size_t)args.lda + kl + kc) : zero4();
       }
       if (TRANS_B) {  // B stored [N, ldb]
         const int n = tid >> 1, kc = (tid & 1) * 4;
-        const bool v = n0 + n < N && k0 + kc < Ktot;
+        const bool v = n0 + n < N && k0 + kc < kend;
         rb = v ? load4(Bb + (size_t)(n0 + n) * args.ldb + kl + kc) : zero4();
         if (DUAL) rb2 = v ? load4(B1 + (size_t)(n0 + n) * args.ldb + kl + kc) : zero4();
       } else {  // B stored [K, ldb]
         const int kr = tid >> 5, c4 = (tid & 31) * 4;
-        const bool v = k0 + kr < Ktot && n0 + c4 < N;
+        const bool v = k0 + kr < kend && n0 + c4 < N;
         rb = v ? load4(Bb + (size_t)(kl + kr) * args.ldb + n0 + c4) : zero4();
         if (DUAL) rb2 = v ? load4(B1 + (size_t)(kl + kr) * args.ldb + n0 + c4) : zero4();
       }
@@ -207,14 +221,14 @@ __global__ void __launch_bounds__(NT, 1) simt_gemm_kernel(const Args args) {
       for (int j = 0; j < (DUAL ? 8 : 1); ++j) acc2[i][j] = 0.f;
   }
 
-  const int ntiles = (Ktot + BK - 1) / BK;
+  const int ntiles = (kend - kbeg + BK - 1) / BK;
   if (ntiles > 0) {
-    load_tiles(0);
+    load_tiles(kbeg);
     store_tiles(0);
     __syncthreads();
     for (int kt = 0; kt < ntiles; ++kt) {
       const int buf = kt & 1;
-      if (kt + 1 < ntiles) load_tiles((kt + 1) * BK);
+      if (kt + 1 < ntiles) load_tiles(kbeg + (kt + 1) * BK);
 #pragma unroll
       for (int kk = 0; kk < BK; ++kk) {
         float a[8], b[8];
@@ -272,7 +286,9 @@ __global__ void __launch_bounds__(NT, 1) simt_gemm_kernel(const Args args) {
       if (n >= N) continue;
       const size_t off = crow * (size_t)args.ldc + n;
       float4 v = make_float4(acc[i][hh * 4 + 0], acc[i][hh * 4 + 1], acc[i][hh * 4 + 2], acc[i][hh * 4 + 3]);
-      if (EPI == EPI_STORE) {
+      if (args.splits > 1) {
+        *reinterpret_cast<float4*>(args.partial + ((size_t)blockIdx.z * args.M + crow) * args.N + n) = v;
+      } else if (EPI == EPI_STORE) {
         store4(C + off, v);
       } else if (EPI == EPI_BIAS) {
         const float4 b = *reinterpret_cast<const float4*>(args.bias + n);
@@ -309,6 +325,20 @@ __global__ void __launch_bounds__(NT, 1) simt_gemm_kernel(const Args args) {
   }
 }
 
+// out[r][n] = sum_{z ascending} partial[z][r][n] (+ bias[n]), fp32.
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ partial, int splits,
+                                                            long long count, int N,
+                                                            const float* __restrict__ bias,
+                                                            float* __restrict__ out) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < count;
+       i += (long long)gridDim.x * blockDim.x) {
+    float s = 0.f;
+    for (int z = 0; z < splits; ++z) s += __ldg(partial + (size_t)z * count + i);
+    if (bias) s += __ldg(bias + (int)(i % N));
+    out[i] = s;
+  }
+}
+
 template <typename TA, typename TB, typename TC, bool KSEG, bool TRANS_B, bool DUAL, int EPI>
 void run(const Args& a, cudaStream_t st) {
   dim3 grid;
@@ -322,10 +352,18 @@ void run(const Args& a, cudaStream_t st) {
     grid.x = (unsigned)rows;
   }
   grid.y = (unsigned)((a.N + BN - 1) / BN);
-  grid.z = 1;
+  grid.z = (unsigned)(a.splits > 1 ? a.splits : 1);
   if (grid.x == 0 || grid.y == 0) return;
   simt_gemm_kernel<TA, TB, TC, KSEG, TRANS_B, DUAL, EPI><<<grid, NT, 0, st>>>(a);
-  count_launch();
+  count_launch(st);
+  if (a.splits > 1) {
+    const long long count = (long long)a.M * a.N;
+    const int blocks = (int)std::min<long long>((count + 255) / 256, 4096);
+    splitk_reduce_kernel<<<blocks, 256, 0, st>>>(a.partial, a.splits, count, a.N,
+                                                 EPI == EPI_BIAS ? a.bias : nullptr,
+                                                 static_cast<float*>(a.C));
+    count_launch(st);
+  }
 }
 
 Args blank() {
@@ -389,13 +427,24 @@ void expert_ffn_bwd_t(const void* dybuf, const void* xbuf, const void* h1, const
 
 }  // namespace
 
+// K slices for a router GEMM with an M x N output and K-long sums: enough CTAs for about two
+// waves on 152 SMs, at least 128 of K per slice.  The same count sizes the workspace.
+int router_splits(int M, int N, int K) {
+  const long long base = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  long long s = (304 + base - 1) / base;
+  s = std::min<long long>(s, std::max(1, K / 128));
+  return (int)std::max<long long>(1, std::min<long long>(s, 64));
+}
+
 void simt_router_logits(int dtype, const void* x, const float* Wg, const float* bias, int T, int h,
-                        int E, float* logits, cudaStream_t st) {
+                        int E, float* logits, float* partial, cudaStream_t st) {
   Args a = blank();
   a.A0 = x; a.lda = h; a.K0 = h;
   a.B0 = Wg; a.ldb = E;
   a.M = T; a.N = E; a.G = 1;
   a.C = logits; a.ldc = E; a.bias = bias;
+  a.splits = router_splits(T, E, h);
+  a.partial = partial;
   if (dtype == MOE_BF16) {
     if (bias) run<__nv_bfloat16, float, float, false, false, false, EPI_BIAS>(a, st);
     else run<__nv_bfloat16, float, float, false, false, false, EPI_STORE>(a, st);
@@ -406,12 +455,14 @@ void simt_router_logits(int dtype, const void* x, const float* Wg, const float* 
 }
 
 void simt_router_dwg(int dtype, const void* x, const float* d_logits, int T, int h, int E,
-                     float* dWg, cudaStream_t st) {
+                     float* dWg, float* partial, cudaStream_t st) {
   Args a = blank();
   a.A0 = x; a.lda = h; a.M = h;
   a.B0 = d_logits; a.ldb = E; a.N = E;
   a.K0 = T; a.G = 1;
   a.C = dWg; a.ldc = E;
+  a.splits = router_splits(h, E, T);
+  a.partial = partial;
   if (dtype == MOE_BF16) run<__nv_bfloat16, float, float, true, false, false, EPI_STORE>(a, st);
   else run<float, float, float, true, false, false, EPI_STORE>(a, st);
 }

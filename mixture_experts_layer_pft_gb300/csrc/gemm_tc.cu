@@ -18,7 +18,8 @@
 // Warp roles (192 threads, one CTA per SM): warp 0 issues TMA loads into a ring of shared-
 // memory stages; warp 1 owns the TMEM allocation and one lane issues tcgen05.mma into fp32
 // accumulators in TMEM; warps 2-5 drain TMEM (tcgen05.ld), apply the epilogue (SwiGLU, its
-// derivative, or a plain store) and write bf16 results with 64-byte coalesced stores.  Stages
+// derivative, or a plain store), transpose each 32 x 16 block through shared memory and write
+// bf16 results with 16-byte stores, four lanes per 64-byte column segment.  Stages
 // and accumulators hand over through mbarriers.  Every wait is bounded (about two seconds of
 // %globaltimer): on expiry the kernel sets MOE_STATUS_TIMEOUT, every role unwinds, and the
 // TMEM is released before the CTA exits.  No cluster, no multicast.
@@ -261,6 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_pref[kMaxE + 1];
   __shared__ Sched s_sched;
+  // epilogue transpose buffers: 4 warps x 4 slots x 16 columns x 32 rows of bf16 (16 KB)
+  __shared__ __align__(16) __nv_bfloat16 s_stage[4][4][16][32];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // stage ring aligned to 1024 bytes (the swizzle atom)
@@ -452,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   } else {
     // ================================================================ epilogue (warps 2..5)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    const int m_local = q * 32 + lane;
+    __nv_bfloat16 (*stg)[16][32] = s_stage[warp - 2];  // this warp's transpose buffers
     int it = 0;
     for (int u = blockIdx.x; u < sc.total; u += gridDim.x, ++it) {
       const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
@@ -460,10 +463,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const uint32_t aph = (uint32_t)(it / C::ACC_BUFS) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[b], aph, &s_abort, p.status))) break;
       tc_fence_after();
-      const int m = w.m0 + m_local;
       const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::NUM_A * C::BN);
       const bool zero = (w.nk == 0);
+      // output element (m, c) lives at [colbase + c][mbase + lane] (+ the expert's base for wgrad)
+      const size_t colbase = C::TOKEN_N ? (size_t)w.row0 : (size_t)w.n0;
+      const size_t ebase = C::TOKEN_N ? 0 : (size_t)w.e * (size_t)p.out_expert_stride;
+      const int mbase = w.m0 + q * 32;
       for (int c0 = 0; c0 < w.ncols; c0 += 16) {
+        // (1) DA: start the coalesced 16-byte loads of h1, h3 for these 16 columns
+        uint4 in_a[2], in_b[2];
+        if (MODE == DA) {
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            const int v = lane + 32 * r, ci = v >> 2, part = v & 3;
+            in_a[r] = make_uint4(0, 0, 0, 0);
+            in_b[r] = in_a[r];
+            if (c0 + ci < w.ncols) {
+              const size_t o = ebase + (colbase + c0 + ci) * (size_t)p.ld_out + mbase + part * 8;
+              in_a[r] = __ldg(reinterpret_cast<const uint4*>(p.in0 + o));
+              in_b[r] = __ldg(reinterpret_cast<const uint4*>(p.in1 + o));
+            }
+          }
+        }
+        // (2) the accumulator columns
         float v0[16], v1[16];
         if (!zero) {
           tmem_ld16(t0 + c0, v0);
@@ -473,32 +495,62 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 #pragma unroll
           for (int i = 0; i < 16; ++i) { v0[i] = 0.f; v1[i] = 0.f; }
         }
+        // (3) DA: transpose h1, h3 through shared memory to this lane's row
+        float z1[16], z3[16];
+        if (MODE == DA) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int c = c0 + i;
-          if (c >= w.ncols) break;
-          if (MODE == GATEUP) {
-            const size_t o = (size_t)(w.row0 + c) * p.ld_out + m;
-            const float h1 = v0[i], h3 = v1[i];
-            p.out0[o] = __float2bfloat16_rn(h1);
-            p.out1[o] = __float2bfloat16_rn(h3);
-            p.out2[o] = __float2bfloat16_rn(h1 * sigmoidf_(h1) * h3);
-          } else if (MODE == DOWN || MODE == DX) {
-            p.out0[(size_t)(w.row0 + c) * p.ld_out + m] = __float2bfloat16_rn(v0[i]);
-          } else if (MODE == DA) {
-            const size_t o = (size_t)(w.row0 + c) * p.ld_out + m;
-            const float z1 = __bfloat162float(p.in0[o]);
-            const float z3 = __bfloat162float(p.in1[o]);
-            const float sg = sigmoidf_(z1);
-            const float da = v0[i];
-            p.out0[o] = __float2bfloat16_rn(da * z3 * sg * (1.f + z1 * (1.f - sg)));
-            p.out1[o] = __float2bfloat16_rn(da * z1 * sg);
-          } else {  // wgrad: D[m][c] is dW^T, stored at [n0 + c][m] of expert e
-            const size_t o = (size_t)w.e * p.out_expert_stride + (size_t)(w.n0 + c) * p.ld_out + m;
-            p.out0[o] = __float2bfloat16_rn(v0[i]);
-            if (MODE == WGRAD13) p.out1[o] = __float2bfloat16_rn(v1[i]);
+          for (int r = 0; r < 2; ++r) {
+            const int v = lane + 32 * r, ci = v >> 2, part = v & 3;
+            *reinterpret_cast<uint4*>(&stg[0][ci][part * 8]) = in_a[r];
+            *reinterpret_cast<uint4*>(&stg[1][ci][part * 8]) = in_b[r];
+          }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            z1[i] = __bfloat162float(stg[0][i][lane]);
+            z3[i] = __bfloat162float(stg[1][i][lane]);
           }
         }
+        // (4) the epilogue math, written to shared memory as [column][m]
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          if (MODE == GATEUP) {
+            const float h1 = v0[i], h3 = v1[i];
+            stg[0][i][lane] = __float2bfloat16_rn(h1);
+            stg[1][i][lane] = __float2bfloat16_rn(h3);
+            stg[2][i][lane] = __float2bfloat16_rn(h1 * sigmoidf_(h1) * h3);
+          } else if (MODE == DA) {
+            const float sg = sigmoidf_(z1[i]);
+            const float da = v0[i];
+            stg[2][i][lane] = __float2bfloat16_rn(da * z3[i] * sg * (1.f + z1[i] * (1.f - sg)));
+            stg[3][i][lane] = __float2bfloat16_rn(da * z1[i] * sg);
+          } else {
+            stg[0][i][lane] = __float2bfloat16_rn(v0[i]);
+            if (MODE == WGRAD13) stg[1][i][lane] = __float2bfloat16_rn(v1[i]);
+          }
+        }
+        __syncwarp();
+        // (5) 16-byte stores: four lanes cover one column's 32 rows (64 contiguous bytes)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+          const int v = lane + 32 * r, ci = v >> 2, part = v & 3;
+          if (c0 + ci < w.ncols) {
+            const size_t o = ebase + (colbase + c0 + ci) * (size_t)p.ld_out + mbase + part * 8;
+            if (MODE == GATEUP) {
+              *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[0][ci][part * 8]);
+              *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
+              *reinterpret_cast<uint4*>(p.out2 + o) = *reinterpret_cast<const uint4*>(&stg[2][ci][part * 8]);
+            } else if (MODE == DA) {
+              *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[2][ci][part * 8]);
+              *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[3][ci][part * 8]);
+            } else {
+              *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[0][ci][part * 8]);
+              if (MODE == WGRAD13)
+                *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
+            }
+          }
+        }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
@@ -554,7 +606,7 @@ int launch(const TcParams& p, cudaStream_t st) {
       cudaSuccess)
     return -1;
   tc_gemm_kernel<MODE><<<num_sms(), kThreads, smem, st>>>(p);
-  count_launch();
+  count_launch(st);
   return 0;
 }
 

@@ -7,7 +7,9 @@
 namespace moe {
 
 int num_sms();  // SM count of the current device (cached per device)
-void count_launch(int n = 1);  // adds to the moe_kernel_launches counter
+// After each kernel launch on `st`: bump the moe_kernel_launches counter and, while a timing
+// ring is installed (moe_profile_events), record its next event on `st`.
+void count_launch(cudaStream_t st);
 void set_last_error(const char* msg);  // the text moe_last_error() returns on this thread
 
 // gather.cu
@@ -35,10 +37,11 @@ void launch_pft_build(const int* topk_idx, int T, int E, int k, int* num_ids, in
                       int* token_ids, int* expert_ids, int* slot_of, void* ws, cudaStream_t st);
 
 // gemm_simt.cu -- fp32-accumulating SIMT GEMMs (all shapes, both dtypes)
+int router_splits(int M, int N, int K);  // split-K factor of a router GEMM (>= 1)
 void simt_router_logits(int dtype, const void* x, const float* Wg, const float* bias, int T, int h,
-                        int E, float* logits, cudaStream_t st);
+                        int E, float* logits, float* partial, cudaStream_t st);
 void simt_router_dwg(int dtype, const void* x, const float* d_logits, int T, int h, int E,
-                     float* dWg, cudaStream_t st);
+                     float* dWg, float* partial, cudaStream_t st);
 void simt_router_dx(const float* d_logits, const float* Wg, int T, int h, int E, float* dx,
                     cudaStream_t st);
 void simt_expert_ffn(int dtype, const void* xbuf, const int* offsets, const void* W1,

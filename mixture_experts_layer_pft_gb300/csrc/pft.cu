@@ -168,13 +168,13 @@ void launch_pft_build(const int* topk_idx, int T, int E, int k, int* num_ids, in
   int* hist = reinterpret_cast<int*>(static_cast<char*>(ws) + sizeof(WsHeader));
   pft_hist_kernel<<<nchunks, kHistBlock, 0, st>>>(topk_idx, Tk, E, chunk, nchunks, hist, num_ids,
                                                   offsets, hdr);
-  count_launch();
+  count_launch(st);
   const size_t smem = (size_t)(1 + kScatWarps) * E * sizeof(int);
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(pft_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   pft_scatter_kernel<<<nchunks, kScatBlock, smem, st>>>(topk_idx, Tk, k, E, chunk, hist, token_ids,
                                                         expert_ids, slot_of);
-  count_launch();
+  count_launch(st);
 }
 
 }  // namespace moe

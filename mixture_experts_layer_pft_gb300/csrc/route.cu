@@ -117,7 +117,7 @@ void launch_softmax_topk(const float* logits, int T, int E, int k, float* probs,
   else if (E <= 256) softmax_topk_kernel<8><<<grid, block, 0, st>>>(logits, T, E, k, probs, topk_idx, topk_w);
   else if (E <= 512) softmax_topk_kernel<16><<<grid, block, 0, st>>>(logits, T, E, k, probs, topk_idx, topk_w);
   else softmax_topk_kernel<32><<<grid, block, 0, st>>>(logits, T, E, k, probs, topk_idx, topk_w);
-  count_launch();
+  count_launch(st);
 }
 
 void launch_route_dlogits(const float* probs, const int* topk_idx, const float* d_topk_w, int T,
@@ -125,7 +125,7 @@ void launch_route_dlogits(const float* probs, const int* topk_idx, const float* 
   const int grid = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   route_dlogits_kernel<<<grid, kWarpsPerBlock * kWarp, 0, st>>>(probs, topk_idx, d_topk_w, T, E,
                                                                  k, d_logits, status);
-  count_launch();
+  count_launch(st);
 }
 
 }  // namespace moe
