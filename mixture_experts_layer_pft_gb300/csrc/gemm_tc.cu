@@ -5,7 +5,8 @@
 // (or weight-gradient) dimension is the MMA's M = 128 and the expert's tokens are either the
 // MMA's N (forward, dgrad) or its K (wgrad).  With tokens on N, an expert segment of n rows
 // costs round_up(n, 16) columns: the in-place tile padding is at most 15 columns per segment
-// and each 128-row weight tile streams from HBM once per 256 tokens of its expert.
+// and each 128-row weight tile streams from HBM once per chunk of its expert's tokens (128 for
+// the gate/up GEMM, 256 for the others; the chunks of one tile run side by side and share L2).
 //
 //   mode      D (fp32 in TMEM)            A operand (M x K)          B operand (N x K)
 //   GATEUP    H1^T, H3^T [f x n]          W1[e], W3[e] ([h,f]: MN)   xbuf rows   (K-major)
@@ -15,9 +16,10 @@
 //   WGRAD13   dW1^T, dW3^T [f x h-tile]   dh1, dh3 rows ([n,f]: MN)  xbuf rows ([n,h]: MN), K = n
 //   WGRAD2    dW2^T [h x f-tile]          dybuf rows ([n,h]: MN)     a rows ([n,f]: MN), K = n
 //
-// Warp roles (192 threads, one CTA per SM): warp 0 issues TMA loads into a ring of shared-
-// memory stages; warp 1 owns the TMEM allocation and one lane issues tcgen05.mma into fp32
-// accumulators in TMEM; warps 2-5 drain TMEM (tcgen05.ld), apply the epilogue (SwiGLU, its
+// Warp roles (one CTA per SM): warp 0 issues TMA loads into a ring of shared-memory stages;
+// warp 1 owns the TMEM allocation and one lane issues tcgen05.mma into fp32 accumulators in
+// TMEM; the epilogue warps (4, or 8 = two per TMEM lane quarter splitting the columns) drain
+// TMEM (tcgen05.ld), apply the epilogue (SwiGLU, its
 // derivative, or a plain store), transpose each 32 x 16 block through shared memory and write
 // bf16 results with 16-byte stores, four lanes per 64-byte column segment.  Stages
 // and accumulators hand over through mbarriers.  Every wait is bounded (about two seconds of
@@ -37,7 +39,6 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 192;
 constexpr int BM = 128;           // MMA M: rows of the weight dimension per tile
 constexpr int BK = 64;            // K per stage: one 128-byte swizzle row of bf16
 constexpr uint32_t kBox = 8192;   // bytes of one 64 x 64 bf16 box
@@ -54,11 +55,17 @@ template <int MODE> struct Cfg {
   static constexpr bool A_MN = (MODE == GATEUP || MODE == DOWN || MODE == WGRAD13 || MODE == WGRAD2);
   static constexpr bool B_MN = (MODE == WGRAD13 || MODE == WGRAD2);
   static constexpr bool TOKEN_N = (MODE <= DX);
-  static constexpr int BN = (MODE == WGRAD13) ? 128 : 256;
+  // gate/up keeps two accumulators per unit; 128-token chunks leave room to double-buffer them
+  static constexpr int BN = (MODE == WGRAD13 || MODE == GATEUP) ? 128 : 256;
   static constexpr uint32_t A_BYTES = NUM_A * kATile;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + (BN / 64) * kBox;
   static constexpr int STAGES = kStageRegion / STAGE_BYTES;
   static constexpr int ACC_BUFS = kTmemCols / (NUM_A * BN);
+  // epilogue: two warps per TMEM lane quarter (splitting the columns), except for the gate/up
+  // GEMM, whose three outputs per element need more transpose buffer than shared memory has left
+  static constexpr int EPI_WARPS = (MODE == GATEUP) ? 4 : 8;
+  static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+  static constexpr int NSLOT = (MODE == GATEUP) ? 3 : (MODE == DA || MODE == WGRAD13) ? 2 : 1;
   static_assert(ACC_BUFS >= 1 && STAGES >= 2, "tile configuration");
 };
 
@@ -184,6 +191,10 @@ __device__ __forceinline__ void tmem_ld16(uint32_t addr, float* v) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// Logistic function for the bf16 epilogues: the fast exponential and division are accurate to a
+// few fp32 ulps, far below the bf16 rounding of every value they feed.
+__device__ __forceinline__ float sigmoid_bf16_epilogue(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
+
 // ---------------------------------------------------------------------------- work units
 
 struct Unit {
@@ -197,7 +208,7 @@ struct Unit {
   int nk;       // K steps of BK
 };
 
-// Token-N modes: expert e has nc_e = ceil(n_e / 256) chunks of about equal size (a multiple of
+// Token-N modes: expert e has nc_e = ceil(n_e / BN) chunks of about equal size (a multiple of
 // 16 rows, the last one shorter); its units are (m-tile, chunk) pairs, chunks innermost, so
 // the CTAs that stream one weight tile for different chunks run side by side.
 struct Sched {
@@ -219,7 +230,7 @@ __device__ __forceinline__ Unit decode(int u, const Sched& sc, const int* s_pref
     }
     const int e = lo;
     const int n = s_off[e + 1] - s_off[e];
-    const int nc = (n + 255) / 256;
+    const int nc = (n + C::BN - 1) / C::BN;
     const int cs = ((n + nc - 1) / nc + 15) & ~15;
     const int local = u - s_pref[e];
     const int mtile = local / nc, c = local % nc;
@@ -249,7 +260,7 @@ __device__ __forceinline__ Unit decode(int u, const Sched& sc, const int* s_pref
 // ---------------------------------------------------------------------------- the kernel
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<MODE>;
   extern __shared__ __align__(1024) uint8_t dsmem[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
@@ -262,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   __shared__ int s_off[kMaxE + 1];
   __shared__ int s_pref[kMaxE + 1];
   __shared__ Sched s_sched;
-  // epilogue transpose buffers: 4 warps x 4 slots x 16 columns x 32 rows of bf16 (16 KB)
-  __shared__ __align__(16) __nv_bfloat16 s_stage[4][4][16][32];
+  // epilogue transpose buffers: one 16-column x 32-row bf16 block per warp and output slot
+  __shared__ __align__(16) __nv_bfloat16 s_stage[C::EPI_WARPS][C::NSLOT][16][32];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // stage ring aligned to 1024 bytes (the swizzle atom)
@@ -281,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     int local = 0;
     for (int e = b0; e < b1; ++e) {
       int ue;
-      if (C::TOKEN_N) ue = ((s_off[e + 1] - s_off[e] + 255) / 256) * mt;
+      if (C::TOKEN_N) ue = ((s_off[e + 1] - s_off[e] + C::BN - 1) / C::BN) * mt;
       else ue = mt * ((p.Nw + C::BN - 1) / C::BN);
       s_pref[e + 1] = ue;
       local += ue;
@@ -312,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   // ------------------------------------------------------------------ barriers + TMEM
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
-    for (int b = 0; b < C::ACC_BUFS; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
+    for (int b = 0; b < C::ACC_BUFS; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], C::EPI_WARPS); }
     mbar_init(&drain_bar, 1);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -405,20 +416,25 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], ph, &s_abort, p.status))) { ok = false; break; }
         const uint32_t a_sm = ring + s * C::STAGE_BYTES;
         const uint32_t b_sm = a_sm + C::A_BYTES;
+        int nsl = BK / 16;  // K slices of 16 to multiply in this stage
         if (!C::TOKEN_N && ks == w.nk - 1 && (w.rows & (BK - 1)) != 0) {
-          // the last K step straddles the next expert's rows: zero token rows >= rows
+          // the last K step ends inside the stage: multiply only the slices that hold valid
+          // token rows, and zero the rows of the last slice that belong to the next expert
           const int valid = w.rows & (BK - 1);
-          const int nbox = C::NUM_A * 2 + C::BN / 64;
-          const int zrows = BK - valid;
-          for (int q = lane; q < nbox * zrows * 8; q += 32) {
-            const int box = q / (zrows * 8);
-            const int r = valid + (q / 8) % zrows;
-            const int c16 = q % 8;
-            uint4* dst = reinterpret_cast<uint4*>(ring_ptr + (a_sm - ring) + box * kBox + r * 128 + c16 * 16);
-            *dst = make_uint4(0, 0, 0, 0);
+          nsl = (valid + 15) / 16;
+          const int zrows = nsl * 16 - valid;
+          if (zrows > 0) {
+            const int nbox = C::NUM_A * 2 + C::BN / 64;
+            for (int q = lane; q < nbox * zrows * 8; q += 32) {
+              const int box = q / (zrows * 8);
+              const int r = valid + (q / 8) % zrows;
+              const int c16 = q % 8;
+              uint4* dst = reinterpret_cast<uint4*>(ring_ptr + (a_sm - ring) + box * kBox + r * 128 + c16 * 16);
+              *dst = make_uint4(0, 0, 0, 0);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
           }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
         }
         tc_fence_after();
         if (lane == 0) {
@@ -427,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const uint32_t a_base = a_sm + a * kATile;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
+              if (kk >= nsl) break;
               uint64_t ad, bd;
               if (C::A_MN) ad = sdesc(a_base + kk * 2048, kBox, 1024);
               else ad = sdesc(a_base + kk * 32, 16, 1024);
@@ -453,8 +470,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
     __syncwarp();
   } else {
-    // ================================================================ epilogue (warps 2..5)
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // ================================================================ epilogue (warps 2..)
+    const int q = warp & 3;              // TMEM lane quarter this warp may access
+    const int cg = (warp - 2) >> 2;      // column group: chunks cg, cg + G, cg + 2G, ...
+    constexpr int G = C::EPI_WARPS / 4;  // warps per lane quarter
     __nv_bfloat16 (*stg)[16][32] = s_stage[warp - 2];  // this warp's transpose buffers
     int it = 0;
     for (int u = blockIdx.x; u < sc.total; u += gridDim.x, ++it) {
@@ -469,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const size_t colbase = C::TOKEN_N ? (size_t)w.row0 : (size_t)w.n0;
       const size_t ebase = C::TOKEN_N ? 0 : (size_t)w.e * (size_t)p.out_expert_stride;
       const int mbase = w.m0 + q * 32;
-      for (int c0 = 0; c0 < w.ncols; c0 += 16) {
+      for (int c0 = 16 * cg; c0 < w.ncols; c0 += 16 * G) {
         // (1) DA: start the coalesced 16-byte loads of h1, h3 for these 16 columns
         uint4 in_a[2], in_b[2];
         if (MODE == DA) {
@@ -510,6 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             z1[i] = __bfloat162float(stg[0][i][lane]);
             z3[i] = __bfloat162float(stg[1][i][lane]);
           }
+          __syncwarp();  // the outputs below reuse these two slots
         }
         // (4) the epilogue math, written to shared memory as [column][m]
 #pragma unroll
@@ -518,12 +538,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const float h1 = v0[i], h3 = v1[i];
             stg[0][i][lane] = __float2bfloat16_rn(h1);
             stg[1][i][lane] = __float2bfloat16_rn(h3);
-            stg[2][i][lane] = __float2bfloat16_rn(h1 * sigmoidf_(h1) * h3);
+            stg[2][i][lane] = __float2bfloat16_rn(h1 * sigmoid_bf16_epilogue(h1) * h3);
           } else if (MODE == DA) {
-            const float sg = sigmoidf_(z1[i]);
+            const float sg = sigmoid_bf16_epilogue(z1[i]);
             const float da = v0[i];
-            stg[2][i][lane] = __float2bfloat16_rn(da * z3[i] * sg * (1.f + z1[i] * (1.f - sg)));
-            stg[3][i][lane] = __float2bfloat16_rn(da * z1[i] * sg);
+            stg[0][i][lane] = __float2bfloat16_rn(da * z3[i] * sg * (1.f + z1[i] * (1.f - sg)));
+            stg[1][i][lane] = __float2bfloat16_rn(da * z1[i] * sg);
           } else {
             stg[0][i][lane] = __float2bfloat16_rn(v0[i]);
             if (MODE == WGRAD13) stg[1][i][lane] = __float2bfloat16_rn(v1[i]);
@@ -541,8 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
               *reinterpret_cast<uint4*>(p.out2 + o) = *reinterpret_cast<const uint4*>(&stg[2][ci][part * 8]);
             } else if (MODE == DA) {
-              *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[2][ci][part * 8]);
-              *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[3][ci][part * 8]);
+              *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[0][ci][part * 8]);
+              *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
             } else {
               *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[0][ci][part * 8]);
               if (MODE == WGRAD13)
@@ -605,7 +625,7 @@ int launch(const TcParams& p, cudaStream_t st) {
   if (cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)
     return -1;
-  tc_gemm_kernel<MODE><<<num_sms(), kThreads, smem, st>>>(p);
+  tc_gemm_kernel<MODE><<<num_sms(), C::THREADS, smem, st>>>(p);
   count_launch(st);
   return 0;
 }
