@@ -74,6 +74,8 @@ struct TcParams {
   CUtensorMap mapA1;  // GATEUP W3 | DX W3 | WGRAD13 dh3
   CUtensorMap mapB0;  // GATEUP xbuf | DOWN a | DA dybuf | DX dh1 | WGRAD13 xbuf | WGRAD2 a
   CUtensorMap mapB1;  // DX dh3
+  CUtensorMap mapO0;  // wgrad: dW1 | dW2 viewed [E * rows, cols], 32 x 16 boxes (TMA stores)
+  CUtensorMap mapO1;  // WGRAD13: dW3
   const int* offsets;
   int E;
   int M;           // total rows of the M (weight) dimension per expert
@@ -146,6 +148,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+
+// Shared -> global tensor store (bulk-async group); x is the innermost coordinate.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until at most N committed bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
 __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -274,7 +291,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
   __shared__ int s_pref[kMaxE + 1];
   __shared__ Sched s_sched;
   // epilogue transpose buffers: one 16-column x 32-row bf16 block per warp and output slot
-  __shared__ __align__(16) __nv_bfloat16 s_stage[C::EPI_WARPS][C::NSLOT][16][32];
+  __shared__ __align__(128) __nv_bfloat16 s_stage[C::EPI_WARPS][C::NSLOT][16][32];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // stage ring aligned to 1024 bytes (the swizzle atom)
@@ -532,6 +549,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           __syncwarp();  // the outputs below reuse these two slots
         }
         // (4) the epilogue math, written to shared memory as [column][m]
+        if (!C::TOKEN_N) {  // wgrad: the previous chunk's TMA store must have read the slots
+          if (lane == 0) bulk_wait_read<0>();
+          __syncwarp();
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if (MODE == GATEUP) {
@@ -550,6 +571,18 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           }
         }
         __syncwarp();
+        if (!C::TOKEN_N) {
+          // wgrad: full 16-column chunks go out as one asynchronous 32 x 16 tensor store per output
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            const int y = w.e * p.a_rows + w.n0 + c0;  // row of the [E * rows, cols] view
+            tma_store_2d(&p.mapO0, smem_u32(&stg[0][0][0]), mbase, y);
+            if (MODE == WGRAD13) tma_store_2d(&p.mapO1, smem_u32(&stg[1][0][0]), mbase, y);
+            bulk_commit();
+          }
+          continue;
+        }
         // (5) 16-byte stores: four lanes cover one column's 32 rows (64 contiguous bytes)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -579,6 +612,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
   }
 
   // ------------------------------------------------------------------ teardown
+  if (!C::TOKEN_N && warp >= 2 && lane == 0) bulk_wait_all();  // this warp's tensor stores
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -605,7 +639,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 2D bf16 map over a row-major [rows, cols] matrix, box = box_cols x box_rows, 128B swizzle.
-bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_cols, int box_rows) {
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_cols, int box_rows,
+              bool swizzle = true) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -613,7 +648,8 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
   const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -689,7 +725,10 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
   ok = make_map(&w13.mapA0, dh1, Tk, f, 64, 64) && make_map(&w13.mapA1, dh3, Tk, f, 64, 64) &&
        make_map(&w13.mapB0, xbuf, Tk, h, 64, 64);
   if (!ok) return -1;
-  w13.offsets = offsets; w13.E = E; w13.M = f; w13.Nw = h;
+  ok = make_map(&w13.mapO0, dW1, (long long)E * h, f, 32, 16, false) &&
+       make_map(&w13.mapO1, dW3, (long long)E * h, f, 32, 16, false);
+  if (!ok) return -1;
+  w13.offsets = offsets; w13.E = E; w13.M = f; w13.Nw = h; w13.a_rows = h;
   w13.out0 = static_cast<__nv_bfloat16*>(dW1); w13.out1 = static_cast<__nv_bfloat16*>(dW3);
   w13.ld_out = f; w13.out_expert_stride = (long long)h * f; w13.status = status;
   if (launch<WGRAD13>(w13, st)) return -1;
@@ -698,7 +737,9 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
   TcParams w2 = blank_params();
   ok = make_map(&w2.mapA0, dybuf, Tk, h, 64, 64) && make_map(&w2.mapB0, a, Tk, f, 64, 64);
   if (!ok) return -1;
-  w2.offsets = offsets; w2.E = E; w2.M = h; w2.Nw = f;
+  ok = make_map(&w2.mapO0, dW2, (long long)E * f, h, 32, 16, false);
+  if (!ok) return -1;
+  w2.offsets = offsets; w2.E = E; w2.M = h; w2.Nw = f; w2.a_rows = f;
   w2.out0 = static_cast<__nv_bfloat16*>(dW2); w2.ld_out = h; w2.out_expert_stride = (long long)f * h;
   w2.status = status;
   return launch<WGRAD2>(w2, st);
