@@ -12,7 +12,9 @@ What it computes, stage by stage, and where each stage comes from:
   token).  The pages fix no gate formula.  Reading adopted: router logits l = x·W_g
   (+ an optional fixed per-expert bias), softmax over all E experts, the k largest
   logits, descending, ties to the lower expert index; each selected expert's weight is
-  its softmax probability, not renormalised.
+  its softmax probability, not renormalised.  Variants (FSMoE report, part 6: the system
+  supports several routers, sigmoid among them): sigmoid scores instead of the softmax, and
+  renormalising the k selected weights to sum to one.
 * PFT build -- X-MoE review, §3 "Training pipeline" step 1 (flatten and sort the
   top_experts array into token_ids / expert_ids) and §3 "Model components" (the PFT
   holds token_ids, expert_ids, num_ids and only valid tokens).  Reading adopted: the
@@ -136,17 +138,29 @@ def topk(logits, k):
     return idx
 
 
-def route(x, Wg, k, bias=None, dtype="f32"):
+def route(x, Wg, k, bias=None, dtype="f32", gate="softmax", renorm=False):
     """Gating stage: logits, probabilities, top-k expert ids and gate weights."""
     logits = router_logits(x, Wg, bias, dtype)
-    return route_from_logits(logits, k, dtype)
+    return route_from_logits(logits, k, dtype, gate, renorm)
 
 
-def route_from_logits(logits, k, dtype="f32"):
-    probs = gate_store(softmax(logits), dtype)
+def route_from_logits(logits, k, dtype="f32", gate="softmax", renorm=False):
+    """Scores, top-k selection and gate weights from the router logits.
+
+    gate="softmax" (the layer's default): p = softmax over the E experts.  gate="sigmoid": each
+    expert's score is p_e = sigmoid(l_e) on its own -- the FSMoE report (part 6, "highlights")
+    lists a sigmoid router beside the GShard and X-MoE ones.  Both maps are monotone, so the
+    selection is the k largest logits either way.  renorm=True divides the k selected scores
+    by their sum (taken from the stored scores), so a token's gate weights add up to one.
+    """
+    l = np.asarray(logits, np.float64)
+    p = softmax(l) if gate == "softmax" else sigmoid(l)
+    probs = gate_store(p, dtype)
     idx = topk(logits, k)
     w = np.take_along_axis(probs, idx.astype(np.int64), axis=1)
-    return {"logits": np.asarray(logits, np.float64), "probs": probs, "topk_idx": idx, "topk_w": w}
+    if renorm:
+        w = gate_store(w / w.sum(axis=1, keepdims=True), dtype)
+    return {"logits": l, "probs": probs, "topk_idx": idx, "topk_w": w}
 
 
 # ----------------------------------------------------------------------------- PFT build
@@ -309,20 +323,30 @@ def combine_bwd(dy, ybuf, slot_of, topk_w, dtype="f32"):
 # ----------------------------------------------------------------------------- gating bwd
 
 
-def route_bwd(x, Wg, probs, topk_idx, d_topk_w, dtype="f32"):
-    """Backward of softmax + top-k gate weights.
+def route_bwd(x, Wg, probs, topk_idx, d_topk_w, dtype="f32", gate="softmax", renorm=False):
+    """Backward of the gate scores + top-k gate weights.
 
-    The weights are w[t,j] = p[t, idx[t,j]], so g[t,e] = d_w[t,j] where e = idx[t,j]
-    (zero elsewhere) and, through the softmax Jacobian, d_l = p*(g - sum_e p*g).
-    Then dW_g = x^T·d_l and the router's share of dx is d_l·W_g^T.  The selection is
-    piecewise constant and contributes no gradient.
+    Without renormalisation w[t,j] = p[t, idx[t,j]], so the gradient g with respect to the
+    scores is d_w[t,j] at e = idx[t,j] and zero elsewhere.  With renormalisation
+    w_j = p_j / S, S = sum of the selected scores, so g at the selected entries is
+    (d_w_j - sum_i d_w_i w_i) / S.  Through the softmax Jacobian d_l = p*(g - sum_e p*g);
+    through the sigmoid d_l = p*(1-p)*g.  Then dW_g = x^T·d_l and the router's share of dx is
+    d_l·W_g^T.  The selection is piecewise constant and contributes no gradient.
     """
     p = np.asarray(probs, np.float64)
     T, E = p.shape
     idx = np.asarray(topk_idx, np.int64)
+    dw = np.asarray(d_topk_w, np.float64)
+    if renorm:
+        sel = np.take_along_axis(p, idx, axis=1)
+        S = sel.sum(axis=1, keepdims=True)
+        dw = (dw - (dw * (sel / S)).sum(axis=1, keepdims=True)) / S
     g = np.zeros((T, E))
-    np.put_along_axis(g, idx, np.asarray(d_topk_w, np.float64), axis=1)
-    d_logits = p * (g - (p * g).sum(axis=1, keepdims=True))
+    np.put_along_axis(g, idx, dw, axis=1)
+    if gate == "softmax":
+        d_logits = p * (g - (p * g).sum(axis=1, keepdims=True))
+    else:
+        d_logits = p * (1.0 - p) * g
     d_logits = gate_store(d_logits, dtype)
     dWg = gate_store(np.asarray(x, np.float64).T @ d_logits, dtype)
     dx_router = gate_store(d_logits @ np.asarray(Wg, np.float64).T, dtype)
@@ -332,10 +356,10 @@ def route_bwd(x, Wg, probs, topk_idx, d_topk_w, dtype="f32"):
 # ----------------------------------------------------------------------------- layer
 
 
-def layer_forward(x, Wg, W1, W3, W2, k, bias=None, dtype="f32"):
+def layer_forward(x, Wg, W1, W3, W2, k, bias=None, dtype="f32", gate="softmax", renorm=False):
     """The whole forward pass: gate -> PFT build -> dispatch -> experts -> combine."""
     E = W1.shape[0]
-    r = route(x, Wg, k, bias, dtype)
+    r = route(x, Wg, k, bias, dtype, gate, renorm)
     pft = pft_build(r["topk_idx"], E)
     xbuf = dispatch(x, pft["token_ids"])
     ffn = expert_ffn(xbuf, pft["offsets"], W1, W3, W2, dtype)
@@ -345,6 +369,7 @@ def layer_forward(x, Wg, W1, W3, W2, k, bias=None, dtype="f32"):
     out.update(ffn)
     out["xbuf"] = xbuf
     out["y"] = y
+    out["gate"], out["renorm"] = gate, renorm
     return out
 
 
@@ -354,7 +379,8 @@ def layer_backward(fwd, x, Wg, W1, W3, W2, dy, dtype="f32"):
     dybuf, d_w = combine_bwd(dy, fwd["ybuf"], fwd["slot_of"], fwd["topk_w"], dtype)
     eb = expert_ffn_bwd(dybuf, fwd["xbuf"], fwd["h1"], fwd["h3"], fwd["a"], fwd["offsets"],
                         W1, W3, W2, dtype)
-    rb = route_bwd(x, Wg, fwd["probs"], fwd["topk_idx"], d_w, dtype)
+    rb = route_bwd(x, Wg, fwd["probs"], fwd["topk_idx"], d_w, dtype, fwd.get("gate", "softmax"),
+                   fwd.get("renorm", False))
     dx = dispatch_bwd(eb["dxbuf"], fwd["slot_of"], k, rb["dx_router"], dtype)
     out = {"dybuf": dybuf, "d_topk_w": d_w, "dx": dx}
     out.update(eb)

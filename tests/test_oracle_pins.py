@@ -298,7 +298,9 @@ def test_empty_expert_gets_exact_zero_weight_gradient():
 # ----------------------------------------------------------------------------- gradients
 
 
-def test_every_gradient_matches_central_finite_differences():
+@pytest.mark.parametrize("gate,renorm", [("softmax", False), ("softmax", True), ("sigmoid", False),
+                                         ("sigmoid", True)])
+def test_every_gradient_matches_central_finite_differences(gate, renorm):
     T, h, E, k, f = 5, 4, 4, 2, 3
     g = rng(2024)
     x = g.standard_normal((T, h)); Wg = g.standard_normal((h, E))
@@ -307,9 +309,9 @@ def test_every_gradient_matches_central_finite_differences():
     bias = np.array([0.3, -0.2, 0.0, 0.1])
 
     def loss(x_, Wg_, W1_, W3_, W2_):
-        return np.sum(O.layer_forward(x_, Wg_, W1_, W3_, W2_, k, bias, "f64")["y"] * dy)
+        return np.sum(O.layer_forward(x_, Wg_, W1_, W3_, W2_, k, bias, "f64", gate, renorm)["y"] * dy)
 
-    fw = O.layer_forward(x, Wg, W1, W3, W2, k, bias, "f64")
+    fw = O.layer_forward(x, Wg, W1, W3, W2, k, bias, "f64", gate, renorm)
     bw = O.layer_backward(fw, x, Wg, W1, W3, W2, dy, "f64")
     params = {"x": x, "Wg": Wg, "W1": W1, "W3": W3, "W2": W2}
     grads = {"x": bw["dx"], "Wg": bw["dWg"], "W1": bw["dW1"], "W3": bw["dW3"], "W2": bw["dW2"]}
@@ -325,6 +327,27 @@ def test_every_gradient_matches_central_finite_differences():
             P[i] = keep
             fd[i] = (lp - lm) / (2 * eps)
         np.testing.assert_allclose(grads[name], fd, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+def test_sigmoid_gate_closed_form_and_selection():
+    l = rng(9).standard_normal((25, 6)) * 3
+    r = O.route_from_logits(l, 3, "f64", gate="sigmoid")
+    for t in range(25):
+        for e in range(6):
+            assert abs(r["probs"][t, e] - 1.0 / (1.0 + math.exp(-l[t, e]))) < 1e-15
+    # the selection is the k largest scores (brute force on the scores themselves)
+    np.testing.assert_array_equal(r["topk_idx"], brute_topk(r["probs"], 3))
+
+
+@pytest.mark.parametrize("gate", ["softmax", "sigmoid"])
+def test_renormalised_weights_sum_to_one_in_proportion(gate):
+    l = rng(10).standard_normal((30, 8)).astype(np.float32)
+    r = O.route_from_logits(l, 3, "f64", gate=gate, renorm=True)
+    plain = O.route_from_logits(l, 3, "f64", gate=gate)
+    np.testing.assert_array_equal(r["topk_idx"], plain["topk_idx"])
+    np.testing.assert_allclose(r["topk_w"].sum(axis=1), 1.0, rtol=1e-14)
+    ratio = r["topk_w"] / plain["topk_w"]
+    np.testing.assert_allclose(ratio, ratio[:, :1] * np.ones_like(ratio), rtol=1e-13)
 
 
 # ----------------------------------------------------------------------------- workloads
