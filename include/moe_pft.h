@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define MOE_PFT_ABI_VERSION 1
+#define MOE_PFT_ABI_VERSION 2
 
 enum moe_status_code {
   MOE_OK = 0,
@@ -61,7 +61,9 @@ enum moe_device_status {
 
 /* moe_route flags */
 enum moe_route_flags {
-  MOE_ROUTE_FROM_LOGITS = 1 /* `logits` is an input: skip the router GEMM and the bias */
+  MOE_ROUTE_FROM_LOGITS = 1, /* `logits` is an input: skip the router GEMM and the bias */
+  MOE_ROUTE_SIGMOID = 2,     /* scores p_e = sigmoid(l_e) per expert instead of the softmax */
+  MOE_ROUTE_RENORM = 4       /* divide the k selected scores by their sum (weights sum to 1) */
 };
 
 /* Operation ids for moe_workspace_size. */
@@ -114,7 +116,10 @@ uint64_t moe_profile_count(void);
  *   logits[t,e] = sum_c x[t,c] * Wg[c,e] (+ bias[e]);  probs = softmax over the E experts;
  *   topk_idx[t,0..k-1] = the k largest logits, descending, ties to the lower expert index
  *   (selection compares the fp32 logits); topk_w[t,j] = probs[t, topk_idx[t,j]], not
- *   renormalised.
+ *   renormalised.  Router variants (the FSMoE report, part 6, lists several routers, sigmoid
+ *   among them): MOE_ROUTE_SIGMOID makes probs[t,e] = sigmoid(logits[t,e]) (the selection is
+ *   unchanged: both maps are monotone); MOE_ROUTE_RENORM divides the k selected scores by their
+ *   sum.  The same gate flags must be passed to moe_route_bwd.
  * x: [T,h] dtype.  Wg: [h,E] fp32.  bias: [E] fp32 or NULL.  logits, probs: [T,E] fp32
  * (logits is an input when flags has MOE_ROUTE_FROM_LOGITS; x, Wg, bias may then be NULL).
  * topk_idx: [T,k] int32.  topk_w: [T,k] fp32.  Requires 1 <= k <= E <= 1024, h % 8 == 0.
@@ -125,15 +130,19 @@ int moe_route(const void* x, const float* Wg, const float* bias, int T, int h, i
 
 /*
  * Gate backward (the adjoint of moe_route; the selection itself has no gradient):
- *   g[t,e] = d_topk_w[t,j] where e = topk_idx[t,j], else 0;
- *   d_logits = probs * (g - sum_e probs*g);  dWg = x^T d_logits;  dx_router = d_logits Wg^T.
+ *   g[t,e] = d_topk_w[t,j] where e = topk_idx[t,j], else 0 (with MOE_ROUTE_RENORM,
+ *   g = (d_topk_w[t,j] - sum_i d_topk_w[t,i] topk_w[t,i]) / S, S = sum of the selected probs);
+ *   d_logits = probs * (g - sum_e probs*g) (MOE_ROUTE_SIGMOID: probs * (1 - probs) * g);
+ *   dWg = x^T d_logits;  dx_router = d_logits Wg^T.  `flags`: the gate flags given to moe_route
+ *   (MOE_ROUTE_FROM_LOGITS is ignored here).
  * d_logits: [T,E] fp32 (written).  dWg: [h,E] fp32 (overwritten).  dx_router: [T,h] fp32
  * (overwritten; NULL skips it).  Feed dx_router to moe_dispatch_bwd as `dx_add` so that dx is
  * rounded once.  Same limits as moe_route.
  */
 int moe_route_bwd(const void* x, const float* Wg, const float* probs, const int32_t* topk_idx,
-                  const float* d_topk_w, int T, int h, int E, int k, int dtype, float* d_logits,
-                  float* dWg, float* dx_router, void* ws, size_t ws_bytes, void* stream);
+                  const float* d_topk_w, int T, int h, int E, int k, int dtype, int flags,
+                  float* d_logits, float* dWg, float* dx_router, void* ws, size_t ws_bytes,
+                  void* stream);
 
 /*
  * PFT build (Order) -- X-MoE review §3 "Training pipeline" step 1 (flatten and sort

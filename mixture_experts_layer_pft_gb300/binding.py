@@ -20,7 +20,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE, MOE_ERR_CUD
     0, -1, -2, -3, -4, -5)
 MOE_F32, MOE_BF16 = 0, 1
 MOE_STATUS_BAD_INDEX, MOE_STATUS_TIMEOUT = 1, 2
-MOE_ROUTE_FROM_LOGITS = 1
+MOE_ROUTE_FROM_LOGITS, MOE_ROUTE_SIGMOID, MOE_ROUTE_RENORM = 1, 2, 4
 (MOE_OP_ROUTE, MOE_OP_ROUTE_BWD, MOE_OP_PFT_BUILD, MOE_OP_DISPATCH, MOE_OP_DISPATCH_BWD,
  MOE_OP_EXPERT_FFN, MOE_OP_EXPERT_FFN_BWD, MOE_OP_COMBINE, MOE_OP_COMBINE_BWD, MOE_OP_ALL) = range(10)
 
@@ -36,7 +36,7 @@ SIGNATURES = {
     "moe_status_reset": (_I, [_P, _P]),
     "moe_check_status": (_I, [_P, _P, ctypes.POINTER(ctypes.c_int)]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
-    "moe_route_bwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "moe_route_bwd": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_pft_build": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_pft_build_noalloc": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
@@ -153,21 +153,30 @@ def moe_check_status(ws) -> int:
     return code.value
 
 
-def moe_route(x, Wg, bias, k, logits, probs, topk_idx, topk_w, ws, from_logits=False, dtype=None):
+def gate_flags(gate: str = "softmax", renorm: bool = False) -> int:
+    if gate not in ("softmax", "sigmoid"):
+        raise ValueError(f"unknown gate {gate!r}")
+    return (MOE_ROUTE_SIGMOID if gate == "sigmoid" else 0) | (MOE_ROUTE_RENORM if renorm else 0)
+
+
+def moe_route(x, Wg, bias, k, logits, probs, topk_idx, topk_w, ws, from_logits=False, dtype=None,
+              gate="softmax", renorm=False):
     T, E = logits.shape
     h = x.shape[1] if x is not None else 0
     dt = _dtype_code(x) if x is not None else (MOE_BF16 if dtype == torch.bfloat16 else MOE_F32)
-    _call("moe_route", _p(x), _p(Wg), _p(bias), T, h, E, k, dt,
-          MOE_ROUTE_FROM_LOGITS if from_logits else 0, _p(logits), _p(probs), _p(topk_idx),
-          _p(topk_w), _p(ws), ws.numel(), _stream())
+    flags = gate_flags(gate, renorm) | (MOE_ROUTE_FROM_LOGITS if from_logits else 0)
+    _call("moe_route", _p(x), _p(Wg), _p(bias), T, h, E, k, dt, flags, _p(logits), _p(probs),
+          _p(topk_idx), _p(topk_w), _p(ws), ws.numel(), _stream())
 
 
-def moe_route_bwd(x, Wg, probs, topk_idx, d_topk_w, d_logits, dWg, dx_router, ws):
+def moe_route_bwd(x, Wg, probs, topk_idx, d_topk_w, d_logits, dWg, dx_router, ws, gate="softmax",
+                  renorm=False):
     T, h = x.shape
     E = Wg.shape[1]
     k = topk_idx.shape[1]
     _call("moe_route_bwd", _p(x), _p(Wg), _p(probs), _p(topk_idx), _p(d_topk_w), T, h, E, k,
-          _dtype_code(x), _p(d_logits), _p(dWg), _p(dx_router), _p(ws), ws.numel(), _stream())
+          _dtype_code(x), gate_flags(gate, renorm), _p(d_logits), _p(dWg), _p(dx_router), _p(ws),
+          ws.numel(), _stream())
 
 
 def moe_pft_build(topk_idx, E, num_ids, offsets, token_ids, expert_ids, slot_of, ws):

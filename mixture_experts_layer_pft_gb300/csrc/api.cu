@@ -181,13 +181,15 @@ int moe_route(const void* x, const float* Wg, const float* bias, int T, int h, i
     float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + sizeof(WsHeader));
     simt_router_logits(dtype, x, Wg, bias, T, h, E, logits, partial, st);
   }
-  launch_softmax_topk(logits, T, E, k, probs, topk_idx, topk_w, st);
+  launch_softmax_topk(logits, T, E, k, (flags & MOE_ROUTE_SIGMOID) != 0, (flags & MOE_ROUTE_RENORM) != 0, probs,
+                      topk_idx, topk_w, st);
   return check_launch("moe_route");
 }
 
 int moe_route_bwd(const void* x, const float* Wg, const float* probs, const int32_t* topk_idx,
-                  const float* d_topk_w, int T, int h, int E, int k, int dtype, float* d_logits,
-                  float* dWg, float* dx_router, void* ws, size_t ws_bytes, void* stream) {
+                  const float* d_topk_w, int T, int h, int E, int k, int dtype, int flags,
+                  float* d_logits, float* dWg, float* dx_router, void* ws, size_t ws_bytes,
+                  void* stream) {
   const cudaStream_t st = (cudaStream_t)stream;
   REQUIRE(T >= 0 && E >= 1 && E <= 1024 && k >= 1 && k <= E && h >= 8, MOE_ERR_INVALID_ARG,
           "moe_route_bwd: need T >= 0, 1 <= k <= E <= 1024, h >= 8");
@@ -204,7 +206,8 @@ int moe_route_bwd(const void* x, const float* Wg, const float* probs, const int3
   REQUIRE_PTR(probs); REQUIRE_PTR(topk_idx); REQUIRE_PTR(d_topk_w); REQUIRE_PTR(d_logits);
   REQUIRE(dx_router == nullptr || aligned16(dx_router), MOE_ERR_INVALID_ARG,
           "moe_route_bwd: dx_router not aligned");
-  launch_route_dlogits(probs, topk_idx, d_topk_w, T, E, k, d_logits, status_of(ws), st);
+  launch_route_dlogits(probs, topk_idx, d_topk_w, T, E, k, (flags & MOE_ROUTE_SIGMOID) != 0,
+                       (flags & MOE_ROUTE_RENORM) != 0, d_logits, status_of(ws), st);
   float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + sizeof(WsHeader));
   simt_router_dwg(dtype, x, d_logits, T, h, E, dWg, partial, st);
   if (dx_router) simt_router_dx(d_logits, Wg, T, h, E, dx_router, st);

@@ -24,10 +24,11 @@ void launch_combine_bwd(int dtype, const void* dy, const void* ybuf, const int* 
                         int* status, cudaStream_t st);
 
 // route.cu
-void launch_softmax_topk(const float* logits, int T, int E, int k, float* probs, int* topk_idx,
-                         float* topk_w, cudaStream_t st);
+void launch_softmax_topk(const float* logits, int T, int E, int k, bool sigmoid, bool renorm, float* probs,
+                         int* topk_idx, float* topk_w, cudaStream_t st);
 void launch_route_dlogits(const float* probs, const int* topk_idx, const float* d_topk_w, int T,
-                          int E, int k, float* d_logits, int* status, cudaStream_t st);
+                          int E, int k, bool sigmoid, bool renorm, float* d_logits, int* status,
+                          cudaStream_t st);
 
 // pft.cu
 int pft_num_chunks(long long Tk);

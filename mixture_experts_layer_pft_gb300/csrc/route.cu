@@ -16,10 +16,13 @@ constexpr int kWarpsPerBlock = 8;
 // PL logits per lane (expert e = lane + 32*i), E <= 32*PL.  The k winners are found by k
 // rounds of a warp arg-max under the order (logit descending, expert index ascending), so
 // ties go to the lower index and the result equals a full stable sort's first k entries.
+// Scores: softmax over the E experts, or (sigmoid) each expert's logistic score on its own;
+// both are monotone in the logit, so the selection is the same.  With renorm the k selected
+// scores are divided by their sum.
 template <int PL>
 __global__ void __launch_bounds__(kWarpsPerBlock * kWarp) softmax_topk_kernel(
-    const float* __restrict__ logits, int T, int E, int k, float* __restrict__ probs,
-    int* __restrict__ topk_idx, float* __restrict__ topk_w) {
+    const float* __restrict__ logits, int T, int E, int k, bool sigmoid, bool renorm,
+    float* __restrict__ probs, int* __restrict__ topk_idx, float* __restrict__ topk_w) {
   const int lane = threadIdx.x % kWarp;
   const int t = blockIdx.x * kWarpsPerBlock + threadIdx.x / kWarp;
   if (t >= T) return;  // warp-uniform
@@ -32,22 +35,32 @@ __global__ void __launch_bounds__(kWarpsPerBlock * kWarp) softmax_topk_kernel(
     v[i] = e < E ? __ldg(lt + e) : -INFINITY;
     m = fmaxf(m, v[i]);
   }
-  m = warp_max(m);
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < PL; ++i) {
-    const int e = lane + kWarp * i;
-    p[i] = e < E ? expf(v[i] - m) : 0.f;
-    s += p[i];
-  }
-  s = warp_sum(s);
   float* pt = probs + (size_t)t * E;
+  if (sigmoid) {
 #pragma unroll
-  for (int i = 0; i < PL; ++i) {
-    const int e = lane + kWarp * i;
-    p[i] = p[i] / s;
-    if (e < E) pt[e] = p[i];
+    for (int i = 0; i < PL; ++i) {
+      const int e = lane + kWarp * i;
+      p[i] = e < E ? 1.0f / (1.0f + expf(-v[i])) : 0.f;
+      if (e < E) pt[e] = p[i];
+    }
+  } else {
+    m = warp_max(m);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const int e = lane + kWarp * i;
+      p[i] = e < E ? expf(v[i] - m) : 0.f;
+      s += p[i];
+    }
+    s = warp_sum(s);
+#pragma unroll
+    for (int i = 0; i < PL; ++i) {
+      const int e = lane + kWarp * i;
+      p[i] = p[i] / s;
+      if (e < E) pt[e] = p[i];
+    }
   }
+  float sel_sum = 0.f;  // sum of the selected scores, in selection order (same in every lane)
   unsigned taken = 0;
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY, bp = 0.f;
@@ -68,63 +81,97 @@ __global__ void __launch_bounds__(kWarpsPerBlock * kWarp) softmax_topk_kernel(
       if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; bp = op; }
     }
     if (bi != INT_MAX && lane == (bi % kWarp)) taken |= 1u << (bi / kWarp);
+    sel_sum += bp;
     if (lane == 0) {
       topk_idx[(size_t)t * k + j] = bi == INT_MAX ? -1 : bi;
       topk_w[(size_t)t * k + j] = bp;
     }
   }
+  if (renorm) {
+    __syncwarp();  // lane 0's weights above are visible to the whole warp
+    float* wt = topk_w + (size_t)t * k;
+    for (int j = lane; j < k; j += kWarp) wt[j] = wt[j] / sel_sum;
+  }
 }
 
-// d_logits[t,e] = p[t,e] * (g[t,e] - s_t),  s_t = sum_j p[t,idx[t,j]] * d_w[t,j],
-// g[t,e] = d_w[t,j] at e = idx[t,j] (0 elsewhere).  Pass 1 writes p*(0 - s) everywhere;
-// pass 2 overwrites the k selected entries.
+// Gradient of the scores: g[t,e] = d_w[t,j] at e = idx[t,j] (0 elsewhere); with renorm
+// (w_j = p_j / S, S = sum of the selected scores) g_j = (d_w[t,j] - sum_i d_w[t,i] w_i) / S.
+// Softmax: d_logits = p * (g - s_t), s_t = sum_j p[idx_j] g_j -- pass 1 writes p*(0 - s)
+// everywhere and pass 2 overwrites the k selected entries.  Sigmoid: d_logits = p(1-p) g, zero
+// off the selection.
 __global__ void __launch_bounds__(kWarpsPerBlock * kWarp) route_dlogits_kernel(
     const float* __restrict__ probs, const int* __restrict__ topk_idx,
-    const float* __restrict__ d_w, int T, int E, int k, float* __restrict__ d_logits,
-    int* status) {
+    const float* __restrict__ d_w, int T, int E, int k, bool sigmoid, bool renorm,
+    float* __restrict__ d_logits, int* status) {
   const int lane = threadIdx.x % kWarp;
   const int t = blockIdx.x * kWarpsPerBlock + threadIdx.x / kWarp;
   if (t >= T) return;
   const float* pt = probs + (size_t)t * E;
-  float s = 0.f;
-  for (int j = lane; j < k; j += kWarp) {
-    const int e = __ldg(topk_idx + (size_t)t * k + j);
-    if ((unsigned)e < (unsigned)E) s = fmaf(__ldg(pt + e), __ldg(d_w + (size_t)t * k + j), s);
+  const int* it = topk_idx + (size_t)t * k;
+  const float* dwt = d_w + (size_t)t * k;
+  float S = 1.f, dwm = 0.f;
+  if (renorm) {
+    float a = 0.f, b = 0.f;
+    for (int j = lane; j < k; j += kWarp) {
+      const int e = __ldg(it + j);
+      if ((unsigned)e < (unsigned)E) {
+        const float pe = __ldg(pt + e);
+        a += pe;
+        b = fmaf(__ldg(dwt + j), pe, b);
+      }
+    }
+    S = warp_sum(a);
+    dwm = warp_sum(b) / S;  // sum_i d_w_i w_i
   }
-  s = warp_sum(s);
+  float s = 0.f;
+  if (!sigmoid) {
+    for (int j = lane; j < k; j += kWarp) {
+      const int e = __ldg(it + j);
+      if ((unsigned)e < (unsigned)E) {
+        const float g = renorm ? (__ldg(dwt + j) - dwm) / S : __ldg(dwt + j);
+        s = fmaf(__ldg(pt + e), g, s);
+      }
+    }
+    s = warp_sum(s);
+  }
   float* dl = d_logits + (size_t)t * E;
-  for (int e = lane; e < E; e += kWarp) dl[e] = __ldg(pt + e) * (0.f - s);
+  for (int e = lane; e < E; e += kWarp) dl[e] = sigmoid ? 0.f : __ldg(pt + e) * (0.f - s);
   __syncwarp();
   for (int j = lane; j < k; j += kWarp) {
-    const int e = __ldg(topk_idx + (size_t)t * k + j);
+    const int e = __ldg(it + j);
     if ((unsigned)e >= (unsigned)E) {
       flag_status(status, MOE_STATUS_BAD_INDEX);
       continue;
     }
-    dl[e] = __ldg(pt + e) * (__ldg(d_w + (size_t)t * k + j) - s);
+    const float g = renorm ? (__ldg(dwt + j) - dwm) / S : __ldg(dwt + j);
+    const float pe = __ldg(pt + e);
+    dl[e] = sigmoid ? pe * (1.f - pe) * g : pe * (g - s);
   }
 }
 
 }  // namespace
 
-void launch_softmax_topk(const float* logits, int T, int E, int k, float* probs, int* topk_idx,
-                         float* topk_w, cudaStream_t st) {
+void launch_softmax_topk(const float* logits, int T, int E, int k, bool sigmoid, bool renorm, float* probs,
+                         int* topk_idx, float* topk_w, cudaStream_t st) {
   const int grid = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int block = kWarpsPerBlock * kWarp;
-  if (E <= 32) softmax_topk_kernel<1><<<grid, block, 0, st>>>(logits, T, E, k, probs, topk_idx, topk_w);
-  else if (E <= 64) softmax_topk_kernel<2><<<grid, block, 0, st>>>(logits, T, E, k, probs, topk_idx, topk_w);
-  else if (E <= 128) softmax_topk_kernel<4><<<grid, block, 0, st>>>(logits, T, E, k, probs, topk_idx, topk_w);
-  else if (E <= 256) softmax_topk_kernel<8><<<grid, block, 0, st>>>(logits, T, E, k, probs, topk_idx, topk_w);
-  else if (E <= 512) softmax_topk_kernel<16><<<grid, block, 0, st>>>(logits, T, E, k, probs, topk_idx, topk_w);
-  else softmax_topk_kernel<32><<<grid, block, 0, st>>>(logits, T, E, k, probs, topk_idx, topk_w);
+#define MOE_TOPK(PLV) softmax_topk_kernel<PLV><<<grid, block, 0, st>>>(logits, T, E, k, sigmoid, renorm, probs, topk_idx, topk_w)
+  if (E <= 32) MOE_TOPK(1);
+  else if (E <= 64) MOE_TOPK(2);
+  else if (E <= 128) MOE_TOPK(4);
+  else if (E <= 256) MOE_TOPK(8);
+  else if (E <= 512) MOE_TOPK(16);
+  else MOE_TOPK(32);
+#undef MOE_TOPK
   count_launch(st);
 }
 
 void launch_route_dlogits(const float* probs, const int* topk_idx, const float* d_topk_w, int T,
-                          int E, int k, float* d_logits, int* status, cudaStream_t st) {
+                          int E, int k, bool sigmoid, bool renorm, float* d_logits, int* status,
+                          cudaStream_t st) {
   const int grid = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   route_dlogits_kernel<<<grid, kWarpsPerBlock * kWarp, 0, st>>>(probs, topk_idx, d_topk_w, T, E,
-                                                                 k, d_logits, status);
+                                                                 k, sigmoid, renorm, d_logits, status);
   count_launch(st);
 }
 

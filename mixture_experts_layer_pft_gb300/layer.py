@@ -14,8 +14,9 @@ from . import binding as B
 
 class LayerBuffers:
     def __init__(self, T: int, h: int, E: int, k: int, f: int, dtype: torch.dtype, device="cuda",
-                 backward: bool = True):
+                 backward: bool = True, gate: str = "softmax", renorm: bool = False):
         self.T, self.h, self.E, self.k, self.f, self.dtype = T, h, E, k, f, dtype
+        self.gate, self.renorm = gate, renorm
         Tk = T * k
         f32, i32 = torch.float32, torch.int32
         d = dict(device=device)
@@ -51,7 +52,8 @@ class LayerBuffers:
 
 def forward(inp: dict, b: LayerBuffers):
     """Gate -> PFT build -> dispatch -> experts -> combine.  Returns b.y."""
-    B.moe_route(inp["x"], inp["Wg"], inp.get("bias"), b.k, b.logits, b.probs, b.topk_idx, b.topk_w, b.ws)
+    B.moe_route(inp["x"], inp["Wg"], inp.get("bias"), b.k, b.logits, b.probs, b.topk_idx, b.topk_w, b.ws,
+                gate=b.gate, renorm=b.renorm)
     B.moe_pft_build(b.topk_idx, b.E, b.num_ids, b.offsets, b.token_ids, b.expert_ids, b.slot_of, b.ws)
     B.moe_dispatch(inp["x"], b.token_ids, b.k, b.xbuf, b.ws)
     B.moe_expert_ffn(b.xbuf, b.offsets, inp["W1"], inp["W3"], inp["W2"], b.ybuf, b.h1, b.h3, b.a, b.ws)
@@ -65,7 +67,7 @@ def backward(inp: dict, dy: torch.Tensor, b: LayerBuffers):
     B.moe_expert_ffn_bwd(b.dybuf, b.xbuf, b.h1, b.h3, b.a, b.offsets, inp["W1"], inp["W3"], inp["W2"],
                          b.dxbuf, b.dW1, b.dW3, b.dW2, b.ws)
     B.moe_route_bwd(inp["x"], inp["Wg"], b.probs, b.topk_idx, b.d_topk_w, b.d_logits, b.dWg,
-                    b.dx_router, b.ws)
+                    b.dx_router, b.ws, gate=b.gate, renorm=b.renorm)
     B.moe_dispatch_bwd(b.dxbuf, b.slot_of, b.dx_router, b.k, b.dx, b.ws)
     return b.dx
 

@@ -3,7 +3,8 @@
 This module only draws inputs; it holds none of the layer's arithmetic, so both the CUDA
 path and the CPU oracle may consume what it makes.  Shapes follow the model table of the
 X-MoE review (§5 "Benchmarks": Small h=2048 f=1408 E=64 k=6 s=2048; Medium h=5120 f=1536
-E=128 k=6 s=4096; Large h=7168 f=2048 E=256 k=8 s=4096) and the FlashDMoE blog §6
+E=128 k=6 s=4096; Large h=7168 f=2048 E=256 k=8 s=4096; Super h=7168 f=2560 E=256 k=8
+s=4096) and the FlashDMoE blog §6
 (synthetic inputs, up to 16k tokens, k=2, up to 128 experts, FP32).
 
 Recipe (every workload): one ``torch.Generator`` on the target device seeded with the
@@ -52,6 +53,8 @@ WORKLOADS = [
     Workload("xmoe-medium-bf16-zipf", 4096, 5120, 128, 6, 1536, "bf16", True, True, 2),
     Workload("xmoe-large-bf16", 4096, 7168, 256, 8, 2048, "bf16", False, True, 3),
     Workload("longseq-fp32-fwd-zipf", 16384, 2048, 128, 2, 2048, "f32", True, False, 4),
+    # the X-MoE Super layer (same table): the Large layer with a wider expert FFN
+    Workload("xmoe-super-bf16", 4096, 7168, 256, 8, 2560, "bf16", False, True, 5),
 ]
 
 

@@ -54,7 +54,7 @@ def test_host_only_entry_points(lib):
     from mixture_experts_layer_pft_gb300 import binding as B
 
     lib.moe_abi_version.restype = ctypes.c_int
-    assert lib.moe_abi_version() == 1
+    assert lib.moe_abi_version() == 2
     f = lib.moe_workspace_size
     f.restype = ctypes.c_size_t
     f.argtypes = [ctypes.c_int] * 7

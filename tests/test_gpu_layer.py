@@ -100,7 +100,7 @@ def _sample(n, hi, seed):
     return np.array(sorted(s))
 
 
-@pytest.mark.parametrize("cfg,ntok,nexp", [(2, 6, 2), (3, 4, 2), (4, 16, 0)])
+@pytest.mark.parametrize("cfg,ntok,nexp", [(2, 6, 2), (3, 4, 2), (4, 16, 0), (5, 3, 1)])
 def test_full_size_layer_sampled(M, cfg, ntok, nexp):
     _, workloads = M
     w = workloads.WORKLOADS[cfg]
@@ -178,6 +178,30 @@ def test_edge_case_layers(M, T, h, E, k, f, dt):
     for n in ("dx", "dW1", "dW3", "dW2"):
         assert rel_l2(np64(getattr(b, n)), bw[n]) <= TOL[dn], n
     assert rel_l2(np64(b.dWg), bw["dWg"]) <= TOL[dn]
+
+
+@pytest.mark.parametrize("gate,renorm,dt", [("sigmoid", True, torch.float32), ("softmax", True, torch.bfloat16),
+                                           ("sigmoid", False, torch.bfloat16)])
+def test_layer_with_router_variants(M, gate, renorm, dt):
+    layer, workloads = M
+    w = workloads.Workload("variant", 192, 256, 16, 4, 128, dtype_name(dt), True, True, 11)
+    inp = workloads.make_inputs(w, "cuda")
+    b = layer.LayerBuffers(w.T, w.h, w.E, w.k, w.f, dt, gate=gate, renorm=renorm)
+    layer.step(inp, b)
+    torch.cuda.synchronize()
+    dn = dtype_name(dt)
+    x, Wg, bias = np64(inp["x"]), np64(inp["Wg"]), np64(inp["bias"])
+    W1, W3, W2, dy = np64(inp["W1"]), np64(inp["W3"]), np64(inp["W2"]), np64(inp["dy"])
+    exact = O.router_logits(x, Wg, bias, "f64")
+    una = routing_checks(b, exact, w.k)
+    if not una.all():
+        pytest.skip("near-tied logits")
+    fw = O.layer_forward(x, Wg, W1, W3, W2, w.k, bias, dn, gate, renorm)
+    bw = O.layer_backward(fw, x, Wg, W1, W3, W2, dy, dn)
+    assert rel_l2(np64(b.topk_w), fw["topk_w"]) <= TOL["f32"]
+    assert rel_l2(np64(b.y), fw["y"]) <= TOL[dn]
+    for n in ("dx", "dW1", "dW2", "dWg", "d_logits"):
+        assert rel_l2(np64(getattr(b, n)), bw[n]) <= TOL[dn], n
 
 
 def test_layer_step_is_bitwise_deterministic(M):

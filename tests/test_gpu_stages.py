@@ -111,6 +111,49 @@ def test_route_bwd(B, dt, T, h, E, k):
     assert B.moe_check_status(ws) == 0
 
 
+@pytest.mark.parametrize("gate,renorm", [("softmax", True), ("sigmoid", False), ("sigmoid", True)])
+@pytest.mark.parametrize("T,E,k", [(37, 8, 2), (300, 64, 6), (129, 256, 8), (40, 1000, 5)])
+def test_gate_variants_given_the_same_logits(B, gate, renorm, T, E, k):
+    logits = gen_logits(T, E, 7 * T + E)
+    probs = torch.empty(T, E, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_ROUTE, T, 8, E, k, 8, torch.float32)
+    B.moe_route(None, None, None, k, logits, probs, idx, w, ws, from_logits=True, gate=gate, renorm=renorm)
+    r = O.route_from_logits(logits.cpu().numpy(), k, "f32", gate, renorm)
+    np.testing.assert_array_equal(npi(idx), r["topk_idx"])
+    assert rel_l2(np64(probs), r["probs"]) <= TOL["f32"]
+    assert rel_l2(np64(w), r["topk_w"]) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("gate,renorm", [("softmax", True), ("sigmoid", False), ("sigmoid", True)])
+@pytest.mark.parametrize("T,h,E,k", [(200, 128, 8, 2), (129, 256, 64, 6), (64, 512, 256, 8)])
+def test_route_bwd_gate_variants(B, gate, renorm, T, h, E, k):
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    x = random_tensor((T, h), 21, torch.float32, "cuda")
+    Wg = random_tensor((h, E), 22, torch.float32, "cuda", std=h ** -0.5)
+    logits = gen_logits(T, E, 23)
+    probs = torch.empty(T, E, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, 8, torch.float32)
+    B.moe_route(None, None, None, k, logits, probs, idx, w, ws, from_logits=True, gate=gate, renorm=renorm)
+    # both sides of the backward take the oracle gate's scores and selection
+    r = O.route_from_logits(logits.cpu().numpy(), k, "f32", gate, renorm)
+    probs = torch.from_numpy(r["probs"].astype(np.float32)).cuda()
+    idx = torch.from_numpy(r["topk_idx"].astype(np.int32)).cuda()
+    d_w = random_tensor((T, k), 24, torch.float32, "cuda")
+    d_logits = torch.empty(T, E, device="cuda")
+    dWg = torch.empty(h, E, device="cuda")
+    dxr = torch.empty(T, h, device="cuda")
+    B.moe_route_bwd(x, Wg, probs, idx, d_w, d_logits, dWg, dxr, ws, gate=gate, renorm=renorm)
+    want = O.route_bwd(np64(x), np64(Wg), r["probs"], r["topk_idx"], np64(d_w), "f32", gate, renorm)
+    for n, got in (("d_logits", d_logits), ("dWg", dWg), ("dx_router", dxr)):
+        assert rel_l2(np64(got), want[n]) <= TOL["f32"], n
+    assert B.moe_check_status(ws) == 0
+
+
 # ----------------------------------------------------------------------------- PFT
 
 

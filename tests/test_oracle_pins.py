@@ -357,7 +357,7 @@ def test_workload_shapes_match_the_pages_model_table():
     from mixture_experts_layer_pft_gb300.workloads import WORKLOADS
 
     g = json.load(open(os.path.join(GOLDEN, "xmoe_model_table.json")))
-    for w, name in zip(WORKLOADS[1:4], ["Small", "Medium", "Large"]):
+    for w, name in zip(WORKLOADS[1:4] + WORKLOADS[5:6], ["Small", "Medium", "Large", "Super"]):
         s, hm, hf, E, k, _ = g["models"][name]
         assert (w.T, w.h, w.f, w.E, w.k) == (s, hm, hf, E, k)
     fl = g["flashdmoe"]
