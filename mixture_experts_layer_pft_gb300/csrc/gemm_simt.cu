@@ -27,7 +27,18 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BN = 128, BK = 8, NT = 256;
+constexpr int BM = 128, BN = 128, NT = 256;
+// K depth of one shared-memory tile: BK for the single-product kernels (the two-product DUAL
+// ones stay at 8, which keeps their three double-buffered tiles under 48 KB of static shared
+// memory).  Each thread loads KT/2 consecutive elements of each operand per tile.
+#ifndef MOE_SIMT_BK
+#define MOE_SIMT_BK 16
+#endif
+// Single-product kernels fit two CTAs per SM (at most 128 registers); the DUAL ones need more.
+#ifndef MOE_SIMT_MINB
+#define MOE_SIMT_MINB 2
+#endif
+constexpr int BK = MOE_SIMT_BK;
 
 enum Epi { EPI_STORE = 0, EPI_BIAS = 1, EPI_SWIGLU = 2, EPI_DSWIGLU = 3, EPI_STORE2 = 4 };
 
@@ -58,10 +69,14 @@ struct Args {
 __device__ __forceinline__ float4 zero4() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
 template <typename TA, typename TB, typename TC, bool KSEG, bool TRANS_B, bool DUAL, int EPI>
-__global__ void __launch_bounds__(NT, 1) simt_gemm_kernel(const Args args) {
-  __shared__ __align__(16) float As[2][BK][BM];
-  __shared__ __align__(16) float Bs[2][BK][BN];
-  __shared__ __align__(16) float Bs2[DUAL ? 2 : 1][BK][DUAL ? BN : 4];
+__global__ void __launch_bounds__(NT, DUAL ? 1 : MOE_SIMT_MINB) simt_gemm_kernel(const Args args) {
+  constexpr int KT = DUAL ? 8 : BK;  // K depth of a tile
+  constexpr int VPT = KT / 2;        // elements of each operand a thread loads per tile
+  constexpr int NL = VPT / 4;        // 4-element loads per operand
+  constexpr int TPR = NT / KT;       // threads per k-row of a [KT x 128] tile
+  __shared__ __align__(16) float As[2][KT][BM];
+  __shared__ __align__(16) float Bs[2][KT][BN];
+  __shared__ __align__(16) float Bs2[DUAL ? 2 : 1][KT][DUAL ? BN : 4];
   __shared__ int s_g, s_mt;
 
   const int tid = threadIdx.x;
@@ -131,7 +146,7 @@ __global__ void __launch_bounds__(NT, 1) simt_gemm_kernel(const Args args) {
   // this CTA's slice of K (all of it without split-K); slices are multiples of BK
   int kbeg = 0, kend = Ktot;
   if (args.splits > 1) {
-    const int per = (((Ktot + args.splits - 1) / args.splits) + BK - 1) / BK * BK;
+    const int per = (((Ktot + args.splits - 1) / args.splits) + KT - 1) / KT * KT;
     kbeg = min(Ktot, (int)blockIdx.z * per);
     kend = min(Ktot, kbeg + per);
   }
@@ -145,64 +160,99 @@ __global__ void __launch_bounds__(NT, 1) simt_gemm_kernel(const Args args) {
   }
 
   // ------------------------------------------------------------------ tile loaders
-  float4 ra, rb, rb2;
+  // Tiles stored along K in memory ([rows, K]: the A rows, or B with TRANS_B) are read by two
+  // threads per row, VPT consecutive k each, and transposed into shared memory as [k][row].
+  // Tiles stored along M / N ([K, cols]: KSEG operands, B without TRANS_B) are read by TPR
+  // threads per k-row, VPT consecutive columns each.
+  float4 ra[NL], rb[NL], rb2[DUAL ? NL : 1];
   auto load_tiles = [&](int k0) {
     if (KSEG) {
-      // A stored [rows, lda]: 8 token rows x 128 m; B stored [rows, ldb]: 8 x 128 n
-      const int kr = tid >> 5, c4 = (tid & 31) * 4;
+      const int kr = tid / TPR, c = (tid % TPR) * VPT;
       const int tok = kb + k0 + kr;
       const bool kv = tok < ke && k0 + kr < kend;
-      ra = (kv && m0 + c4 < args.M) ? load4(A0 + (size_t)tok * args.lda + m0 + c4) : zero4();
-      const bool nv = kv && n0 + c4 < N;
-      rb = nv ? load4(B0 + (size_t)tok * args.ldb + n0 + c4) : zero4();
-      if (DUAL) rb2 = nv ? load4(B1 + (size_t)tok * args.ldb + n0 + c4) : zero4();
+#pragma unroll
+      for (int q = 0; q < NL; ++q) {
+        const int cc = c + 4 * q;
+        ra[q] = (kv && m0 + cc < args.M) ? load4(A0 + (size_t)tok * args.lda + m0 + cc) : zero4();
+        const bool nv = kv && n0 + cc < N;
+        rb[q] = nv ? load4(B0 + (size_t)tok * args.ldb + n0 + cc) : zero4();
+        if (DUAL) rb2[q] = nv ? load4(B1 + (size_t)tok * args.ldb + n0 + cc) : zero4();
+      }
     } else {
-      const bool seg1 = k0 >= args.K0;  // KCAT: whole tile in one segment (K0 % BK == 0)
-      const TA* Ab = seg1 ? A1 : A0;
-      const TB* Bb = seg1 ? B1 : B0;
-      const int kl = seg1 ? k0 - args.K0 : k0;
+      // KCAT: k < K0 reads (A0, B0) at k, k >= K0 reads (A1, B1) at k - K0.  K0 is a multiple
+      // of 4, so each 4-element load lies in one segment (a tile may straddle the two).
+      const bool kcat = A1 != nullptr;
       {
-        const int r = tid >> 1, kc = (tid & 1) * 4;
-        const bool v = r < rows_valid && k0 + kc < kend;
-        ra = v ? load4(Ab + (row0 + r) * (size_t)args.lda + kl + kc) : zero4();
+        const int r = tid >> 1, kc = (tid & 1) * VPT;
+#pragma unroll
+        for (int q = 0; q < NL; ++q) {
+          const int ka = k0 + kc + 4 * q;
+          const bool s1 = kcat && ka >= args.K0;
+          const bool v = r < rows_valid && ka < kend;
+          ra[q] = v ? load4((s1 ? A1 : A0) + (row0 + r) * (size_t)args.lda + (s1 ? ka - args.K0 : ka)) : zero4();
+        }
       }
       if (TRANS_B) {  // B stored [N, ldb]
-        const int n = tid >> 1, kc = (tid & 1) * 4;
-        const bool v = n0 + n < N && k0 + kc < kend;
-        rb = v ? load4(Bb + (size_t)(n0 + n) * args.ldb + kl + kc) : zero4();
-        if (DUAL) rb2 = v ? load4(B1 + (size_t)(n0 + n) * args.ldb + kl + kc) : zero4();
+        const int n = tid >> 1, kc = (tid & 1) * VPT;
+#pragma unroll
+        for (int q = 0; q < NL; ++q) {
+          const int ka = k0 + kc + 4 * q;
+          const bool s1 = kcat && ka >= args.K0;
+          const int kl = s1 ? ka - args.K0 : ka;
+          const bool v = n0 + n < N && ka < kend;
+          rb[q] = v ? load4((s1 ? B1 : B0) + (size_t)(n0 + n) * args.ldb + kl) : zero4();
+          if (DUAL) rb2[q] = v ? load4(B1 + (size_t)(n0 + n) * args.ldb + kl) : zero4();
+        }
       } else {  // B stored [K, ldb]
-        const int kr = tid >> 5, c4 = (tid & 31) * 4;
-        const bool v = k0 + kr < kend && n0 + c4 < N;
-        rb = v ? load4(Bb + (size_t)(kl + kr) * args.ldb + n0 + c4) : zero4();
-        if (DUAL) rb2 = v ? load4(B1 + (size_t)(kl + kr) * args.ldb + n0 + c4) : zero4();
+        const int kr = tid / TPR, c = (tid % TPR) * VPT;
+        const int ka = k0 + kr;
+        const bool s1 = kcat && ka >= args.K0;
+        const int kl = s1 ? ka - args.K0 : ka;
+#pragma unroll
+        for (int q = 0; q < NL; ++q) {
+          const bool v = ka < kend && n0 + c + 4 * q < N;
+          rb[q] = v ? load4((s1 ? B1 : B0) + (size_t)kl * args.ldb + n0 + c + 4 * q) : zero4();
+          if (DUAL) rb2[q] = v ? load4(B1 + (size_t)kl * args.ldb + n0 + c + 4 * q) : zero4();
+        }
       }
     }
   };
   auto store_tiles = [&](int buf) {
     if (KSEG) {
-      const int kr = tid >> 5, c4 = (tid & 31) * 4;
-      *reinterpret_cast<float4*>(&As[buf][kr][c4]) = ra;
-      *reinterpret_cast<float4*>(&Bs[buf][kr][c4]) = rb;
-      if (DUAL) *reinterpret_cast<float4*>(&Bs2[buf][kr][c4]) = rb2;
+      const int kr = tid / TPR, c = (tid % TPR) * VPT;
+#pragma unroll
+      for (int q = 0; q < NL; ++q) {
+        *reinterpret_cast<float4*>(&As[buf][kr][c + 4 * q]) = ra[q];
+        *reinterpret_cast<float4*>(&Bs[buf][kr][c + 4 * q]) = rb[q];
+        if (DUAL) *reinterpret_cast<float4*>(&Bs2[buf][kr][c + 4 * q]) = rb2[q];
+      }
     } else {
       {
-        const int r = tid >> 1, kc = (tid & 1) * 4;
-        As[buf][kc + 0][r] = ra.x; As[buf][kc + 1][r] = ra.y;
-        As[buf][kc + 2][r] = ra.z; As[buf][kc + 3][r] = ra.w;
+        const int r = tid >> 1, kc = (tid & 1) * VPT;
+#pragma unroll
+        for (int q = 0; q < NL; ++q) {
+          As[buf][kc + 4 * q + 0][r] = ra[q].x; As[buf][kc + 4 * q + 1][r] = ra[q].y;
+          As[buf][kc + 4 * q + 2][r] = ra[q].z; As[buf][kc + 4 * q + 3][r] = ra[q].w;
+        }
       }
       if (TRANS_B) {
-        const int n = tid >> 1, kc = (tid & 1) * 4;
-        Bs[buf][kc + 0][n] = rb.x; Bs[buf][kc + 1][n] = rb.y;
-        Bs[buf][kc + 2][n] = rb.z; Bs[buf][kc + 3][n] = rb.w;
-        if (DUAL) {
-          Bs2[buf][kc + 0][n] = rb2.x; Bs2[buf][kc + 1][n] = rb2.y;
-          Bs2[buf][kc + 2][n] = rb2.z; Bs2[buf][kc + 3][n] = rb2.w;
+        const int n = tid >> 1, kc = (tid & 1) * VPT;
+#pragma unroll
+        for (int q = 0; q < NL; ++q) {
+          Bs[buf][kc + 4 * q + 0][n] = rb[q].x; Bs[buf][kc + 4 * q + 1][n] = rb[q].y;
+          Bs[buf][kc + 4 * q + 2][n] = rb[q].z; Bs[buf][kc + 4 * q + 3][n] = rb[q].w;
+          if (DUAL) {
+            Bs2[buf][kc + 4 * q + 0][n] = rb2[q].x; Bs2[buf][kc + 4 * q + 1][n] = rb2[q].y;
+            Bs2[buf][kc + 4 * q + 2][n] = rb2[q].z; Bs2[buf][kc + 4 * q + 3][n] = rb2[q].w;
+          }
         }
       } else {
-        const int kr = tid >> 5, c4 = (tid & 31) * 4;
-        *reinterpret_cast<float4*>(&Bs[buf][kr][c4]) = rb;
-        if (DUAL) *reinterpret_cast<float4*>(&Bs2[buf][kr][c4]) = rb2;
+        const int kr = tid / TPR, c = (tid % TPR) * VPT;
+#pragma unroll
+        for (int q = 0; q < NL; ++q) {
+          *reinterpret_cast<float4*>(&Bs[buf][kr][c + 4 * q]) = rb[q];
+          if (DUAL) *reinterpret_cast<float4*>(&Bs2[buf][kr][c + 4 * q]) = rb2[q];
+        }
       }
     }
   };
@@ -221,16 +271,16 @@ __global__ void __launch_bounds__(NT, 1) simt_gemm_kernel(const Args args) {
       for (int j = 0; j < (DUAL ? 8 : 1); ++j) acc2[i][j] = 0.f;
   }
 
-  const int ntiles = (kend - kbeg + BK - 1) / BK;
+  const int ntiles = (kend - kbeg + KT - 1) / KT;
   if (ntiles > 0) {
     load_tiles(kbeg);
     store_tiles(0);
     __syncthreads();
     for (int kt = 0; kt < ntiles; ++kt) {
       const int buf = kt & 1;
-      if (kt + 1 < ntiles) load_tiles(kbeg + (kt + 1) * BK);
+      if (kt + 1 < ntiles) load_tiles(kbeg + (kt + 1) * KT);
 #pragma unroll
-      for (int kk = 0; kk < BK; ++kk) {
+      for (int kk = 0; kk < KT; ++kk) {
         float a[8], b[8];
         const float4 a0 = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
         const float4 a1 = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
@@ -427,13 +477,23 @@ void expert_ffn_bwd_t(const void* dybuf, const void* xbuf, const void* h1, const
 
 }  // namespace
 
-// K slices for a router GEMM with an M x N output and K-long sums: enough CTAs for about two
-// waves on 152 SMs, at least 128 of K per slice.  The same count sizes the workspace.
+// K slices for a router GEMM with an M x N output and K-long sums (one CTA per SM; 152 SMs):
+// at least 128 of K per slice, and the count whose last wave of CTAs is fullest among those
+// giving two waves or more (fewer slices on ties).  The same count sizes the workspace.
 int router_splits(int M, int N, int K) {
+  constexpr int kSms = 152;
   const long long base = (long long)((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-  long long s = (304 + base - 1) / base;
-  s = std::min<long long>(s, std::max(1, K / 128));
-  return (int)std::max<long long>(1, std::min<long long>(s, 64));
+  const int smax = std::max(1, std::min(64, K / 128));
+  int best = 1;
+  double best_score = -1.0;
+  for (int sp = 1; sp <= smax; ++sp) {
+    const long long ctas = base * sp;
+    const long long waves = (ctas + kSms - 1) / kSms;
+    double score = (double)ctas / (double)(waves * kSms);  // fill of the waves
+    if (ctas < 2 * kSms) score *= (double)ctas / (2.0 * kSms);
+    if (score > best_score + 1e-9) { best_score = score; best = sp; }
+  }
+  return best;
 }
 
 void simt_router_logits(int dtype, const void* x, const float* Wg, const float* bias, int T, int h,
