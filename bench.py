@@ -261,10 +261,23 @@ CSRC = "mixture_experts_layer_pft_gb300/csrc/"
 
 def kernel_names(stage, n, w):
     """Names (and source file) of the n launches one stage call makes, in launch order."""
-    tc = w.dtype == "bf16" and w.h % 128 == 0 and w.f % 128 == 0 and os.environ.get("MOE_PFT_GEMM") != "simt"
+    simt_only = os.environ.get("MOE_PFT_GEMM") == "simt"
+    tc = w.dtype == "bf16" and w.h % 128 == 0 and w.f % 128 == 0 and not simt_only
+    tc_router = w.dtype == "bf16" and w.h % 64 == 0 and w.E % 16 == 0 and w.E >= 64 and not simt_only
+    if tc_router:
+        route = (["router_split_w", "tc_router_fwd", "softmax_topk"] if n == 3 else
+                 ["router_split_w", "tc_router_fwd", "router_splitk_reduce", "softmax_topk"], CSRC + "router_tc.cu")
+        route_bwd = ((["route_dlogits", "router_split_dl", "tc_router_dwg", "router_split_w", "tc_router_dx"] if n == 5
+                      else ["route_dlogits", "router_split_dl", "tc_router_dwg", "router_dwg_splitk_reduce",
+                            "router_split_w", "tc_router_dx"]), CSRC + "router_tc.cu")
+    else:
+        route = (["router_gemm", "softmax_topk"] if n == 2 else ["router_gemm", "router_splitk_reduce", "softmax_topk"],
+                 CSRC + "gemm_simt.cu")
+        route_bwd = ((["route_dlogits", "router_dwg", "router_dx"] if n == 3
+                      else ["route_dlogits", "router_dwg", "router_dwg_splitk_reduce", "router_dx"]),
+                     CSRC + "gemm_simt.cu")
     table = {
-        "route": (["router_gemm", "softmax_topk"] if n == 2 else ["router_gemm", "router_splitk_reduce", "softmax_topk"],
-                  CSRC + "gemm_simt.cu"),
+        "route": route,
         "pft_build": (["pft_hist", "pft_scatter"], CSRC + "pft.cu"),
         "dispatch": (["dispatch"], CSRC + "gather.cu"),
         "expert_ffn": ((["tc_GATEUP", "tc_DOWN"], CSRC + "gemm_tc.cu") if tc
@@ -273,9 +286,7 @@ def kernel_names(stage, n, w):
         "combine_bwd": (["combine_bwd"], CSRC + "gather.cu"),
         "expert_ffn_bwd": ((["tc_DA", "tc_DX", "tc_WGRAD13", "tc_WGRAD2"], CSRC + "gemm_tc.cu") if tc
                            else (["simt_dA", "simt_dX", "simt_dW13", "simt_dW2"], CSRC + "gemm_simt.cu")),
-        "route_bwd": ((["route_dlogits", "router_dwg", "router_dx"] if n == 3
-                       else ["route_dlogits", "router_dwg", "router_dwg_splitk_reduce", "router_dx"]),
-                      CSRC + "gemm_simt.cu"),
+        "route_bwd": route_bwd,
         "dispatch_bwd": (["dispatch_bwd"], CSRC + "gather.cu"),
     }
     names, src = table[stage]
@@ -305,6 +316,12 @@ def kernel_counts(w, T, e_active, binding=None):
         "tc_WGRAD13": {"flops": 4 * Tk * h * f, "bytes": Tk * h * s + 2 * Tk * f * s + 2 * E * Wb},
         "tc_WGRAD2": {"flops": 2 * Tk * h * f, "bytes": Tk * h * s + Tk * f * s + E * Wb},
         "route_dlogits": {"flops": 0, "bytes": 2 * T * E * 4 + 12 * Tk},
+        # tensor-core router: exact three-plane bf16 splits of the fp32 operands, then the GEMMs
+        "router_split_w": {"flops": 0, "bytes": h * E * 4 + 3 * h * E * 2},
+        "router_split_dl": {"flops": 0, "bytes": T * E * 4 + 3 * T * E * 2},
+        "tc_router_fwd": {"flops": 2 * T * h * E, "bytes": T * h * s + 3 * h * E * 2 + T * E * 4},
+        "tc_router_dwg": {"flops": 2 * T * h * E, "bytes": T * h * s + 3 * T * E * 2 + h * E * 4},
+        "tc_router_dx": {"flops": 2 * T * h * E, "bytes": 3 * T * E * 2 + 3 * h * E * 2 + T * h * 4},
         "router_dwg": {"flops": 2 * T * h * E, "bytes": T * h * s + T * E * 4 + h * E * 4},
         "router_dwg_splitk_reduce": {"flops": 0, "bytes": 2 * h * E * 4},
         "router_dx": {"flops": 2 * T * h * E, "bytes": T * E * 4 + h * E * 4 + T * h * 4},
@@ -443,7 +460,7 @@ def run_ours(args, w):
     c = kc[dom]
     region_ms = ms_per_step * args.steps
     fkey = "bf16_tflops_sustained" if region_ms > 2000 else "bf16_tflops"
-    if dom.startswith("simt") or (dom.startswith("router") and not dom.endswith("reduce")):
+    if dom.startswith("simt") or dom in ("router_gemm", "router_dwg", "router_dx"):
         roof = {"bound": "alu", "achieved": c["flops"] / (dom_ms * 1e-3) / 1e12,
                 "peak": FP32_ALU_TFLOPS_NOMINAL, "unit": "TFLOP/s"}
         which = "derived FP32 FMA peak: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (nominal)"

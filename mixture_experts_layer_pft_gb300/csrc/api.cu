@@ -45,6 +45,9 @@ int tc_failure(const char* what) {
   return MOE_ERR_CUDA;
 }
 
+// Shapes the tensor-core router takes (the workspace is sized for them whatever the engine).
+bool router_tc_shape(int dtype, int h, int E) { return dtype == MOE_BF16 && h % 64 == 0 && E % 16 == 0 && E >= 64; }
+
 bool use_tensor_cores(int dtype, int h, int f) {
   const char* env = getenv("MOE_PFT_GEMM");
   if (env && strcmp(env, "simt") == 0) return false;
@@ -122,11 +125,15 @@ size_t moe_workspace_size(int op, int T, int h, int E, int k, int f, int dtype) 
   switch (op) {
     case MOE_OP_ROUTE: {
       const int sp = (T > 0 && h > 0 && E > 0) ? router_splits(T, E, h) : 1;
-      return hdr + (sp > 1 ? round256((size_t)sp * T * E * sizeof(float)) : 0);
+      size_t b = sp > 1 ? round256((size_t)sp * T * E * sizeof(float)) : 0;
+      if (T > 0 && router_tc_shape(dtype, h, E)) b = std::max(b, tc_router_scratch(0, T, h, E));
+      return hdr + b;
     }
     case MOE_OP_ROUTE_BWD: {
       const int sp = (T > 0 && h > 0 && E > 0) ? router_splits(h, E, T) : 1;
-      return hdr + (sp > 1 ? round256((size_t)sp * h * E * sizeof(float)) : 0);
+      size_t b = sp > 1 ? round256((size_t)sp * h * E * sizeof(float)) : 0;
+      if (T > 0 && router_tc_shape(dtype, h, E)) b = std::max(b, tc_router_scratch(1, T, h, E));
+      return hdr + b;
     }
     case MOE_OP_PFT_BUILD:
       return hdr + round256(pft_scratch_bytes(std::max(Tk, 1LL), std::max(E, 1)));
@@ -178,8 +185,15 @@ int moe_route(const void* x, const float* Wg, const float* bias, int T, int h, i
     REQUIRE(h >= 8 && h % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_route: h must be a multiple of 8");
     REQUIRE(E % 4 == 0, MOE_ERR_UNSUPPORTED, "moe_route: E must be a multiple of 4");
     REQUIRE(bias == nullptr || aligned16(bias), MOE_ERR_INVALID_ARG, "moe_route: bias not aligned");
-    float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + sizeof(WsHeader));
-    simt_router_logits(dtype, x, Wg, bias, T, h, E, logits, partial, st);
+    REQUIRE(aligned16(ws), MOE_ERR_WORKSPACE, "moe_route: workspace not 16-byte aligned");
+    char* scratch = static_cast<char*>(ws) + sizeof(WsHeader);
+    if (tc_router_supported(dtype, h, E)) {
+      REQUIRE(aligned16(x) && aligned16(logits), MOE_ERR_INVALID_ARG, "moe_route: x or logits not aligned");
+      if (tc_router_logits(x, Wg, bias, T, h, E, logits, scratch, status_of(ws), st) != 0)
+        return tc_failure("moe_route");
+    } else {
+      simt_router_logits(dtype, x, Wg, bias, T, h, E, logits, reinterpret_cast<float*>(scratch), st);
+    }
   }
   launch_softmax_topk(logits, T, E, k, (flags & MOE_ROUTE_SIGMOID) != 0, (flags & MOE_ROUTE_RENORM) != 0, probs,
                       topk_idx, topk_w, st);
@@ -208,9 +222,17 @@ int moe_route_bwd(const void* x, const float* Wg, const float* probs, const int3
           "moe_route_bwd: dx_router not aligned");
   launch_route_dlogits(probs, topk_idx, d_topk_w, T, E, k, (flags & MOE_ROUTE_SIGMOID) != 0,
                        (flags & MOE_ROUTE_RENORM) != 0, d_logits, status_of(ws), st);
-  float* partial = reinterpret_cast<float*>(static_cast<char*>(ws) + sizeof(WsHeader));
-  simt_router_dwg(dtype, x, d_logits, T, h, E, dWg, partial, st);
-  if (dx_router) simt_router_dx(d_logits, Wg, T, h, E, dx_router, st);
+  REQUIRE(aligned16(ws), MOE_ERR_WORKSPACE, "moe_route_bwd: workspace not 16-byte aligned");
+  char* scratch = static_cast<char*>(ws) + sizeof(WsHeader);
+  if (tc_router_supported(dtype, h, E)) {
+    REQUIRE(aligned16(x) && aligned16(d_logits) && aligned16(dWg), MOE_ERR_INVALID_ARG,
+            "moe_route_bwd: x, d_logits or dWg not aligned");
+    if (tc_router_bwd(x, Wg, d_logits, T, h, E, dWg, dx_router, scratch, status_of(ws), st) != 0)
+      return tc_failure("moe_route_bwd");
+  } else {
+    simt_router_dwg(dtype, x, d_logits, T, h, E, dWg, reinterpret_cast<float*>(scratch), st);
+    if (dx_router) simt_router_dx(d_logits, Wg, T, h, E, dx_router, st);
+  }
   return check_launch("moe_route_bwd");
 }
 

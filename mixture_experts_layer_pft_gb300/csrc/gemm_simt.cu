@@ -406,14 +406,9 @@ void run(const Args& a, cudaStream_t st) {
   if (grid.x == 0 || grid.y == 0) return;
   simt_gemm_kernel<TA, TB, TC, KSEG, TRANS_B, DUAL, EPI><<<grid, NT, 0, st>>>(a);
   count_launch(st);
-  if (a.splits > 1) {
-    const long long count = (long long)a.M * a.N;
-    const int blocks = (int)std::min<long long>((count + 255) / 256, 4096);
-    splitk_reduce_kernel<<<blocks, 256, 0, st>>>(a.partial, a.splits, count, a.N,
-                                                 EPI == EPI_BIAS ? a.bias : nullptr,
-                                                 static_cast<float*>(a.C));
-    count_launch(st);
-  }
+  if (a.splits > 1)
+    launch_splitk_reduce(a.partial, a.splits, (long long)a.M * a.N, a.N, EPI == EPI_BIAS ? a.bias : nullptr,
+                         static_cast<float*>(a.C), st);
 }
 
 Args blank() {
@@ -476,6 +471,13 @@ void expert_ffn_bwd_t(const void* dybuf, const void* xbuf, const void* h1, const
 }
 
 }  // namespace
+
+void launch_splitk_reduce(const float* partial, int splits, long long count, int N, const float* bias,
+                          float* out, cudaStream_t st) {
+  const int blocks = (int)std::min<long long>((count + 255) / 256, 4096);
+  splitk_reduce_kernel<<<blocks, 256, 0, st>>>(partial, splits, count, N, bias, out);
+  count_launch(st);
+}
 
 // K slices for a router GEMM with an M x N output and K-long sums (one CTA per SM; 152 SMs):
 // at least 128 of K per slice, and the count whose last wave of CTAs is fullest among those

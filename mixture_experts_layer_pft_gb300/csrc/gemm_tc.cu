@@ -34,10 +34,13 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
 namespace {
+
+using namespace ptx;
 
 constexpr int BM = 128;           // MMA M: rows of the weight dimension per tile
 constexpr int BK = 64;            // K per stage: one 128-byte swizzle row of bf16
@@ -46,7 +49,6 @@ constexpr uint32_t kATile = 16384;  // bytes of one 128 x 64 A tile
 constexpr int kTmemCols = 512;
 constexpr int kMaxE = 1024;
 constexpr uint32_t kStageRegion = 196608;  // shared memory given to the stage ring
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 enum Mode { GATEUP = 0, DOWN = 1, DA = 2, DX = 3, WGRAD13 = 4, WGRAD2 = 5 };
 
@@ -91,122 +93,6 @@ struct TcParams {
   long long out_expert_stride;  // wgrad: elements between consecutive experts' outputs
   int* status;
 };
-
-// ---------------------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ unsigned long long globaltimer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Wait for the phase of `bar` with parity `parity`.  Gives up after kWaitLimitNs or when
-// another role has already given up; then returns false.
-__device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                       int* status) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        atomicOr(status, MOE_STATUS_TIMEOUT);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar,
-                                            int x, int y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
-
-// Shared -> global tensor store (bulk-async group); x is the innermost coordinate.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int x, int y) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y), "r"(src)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until at most N committed bulk groups of this thread still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// Shared-memory matrix descriptor, 128-byte swizzle.
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M = 128, N = n.
-__device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn, bool b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
-         ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
-}
-
-__device__ __forceinline__ void umma(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                     uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
-          tmem_d),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// 32 lanes x 16 consecutive 32-bit TMEM columns -> 16 registers per thread.
-__device__ __forceinline__ void tmem_ld16(uint32_t addr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(addr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Logistic function for the bf16 epilogues: the fast exponential and division are accurate to a
 // few fp32 ulps, far below the bf16 rounding of every value they feed.
@@ -638,9 +524,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D bf16 map over a row-major [rows, cols] matrix, box = box_cols x box_rows, 128B swizzle.
-bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_cols, int box_rows,
-              bool swizzle = true) {
+}  // namespace
+
+bool tc_encode_available() { return encode_fn() != nullptr; }
+
+bool tc_make_map(CUtensorMap* m, const void* base, long long rows, long long cols, int box_cols, int box_rows,
+                 bool swizzle) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
@@ -653,6 +542,9 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
+
+
+namespace {
 
 template <int MODE>
 int launch(const TcParams& p, cudaStream_t st) {
@@ -681,8 +573,8 @@ bool tc_supported(int dtype, int h, int f) {
 int tc_expert_ffn(const void* xbuf, const int* offsets, const void* W1, const void* W3, const void* W2, int Tk,
                   int E, int h, int f, void* ybuf, void* h1, void* h3, void* a, int* status, cudaStream_t st) {
   TcParams g = blank_params();
-  bool ok = make_map(&g.mapA0, W1, (long long)E * h, f, 64, 64) &&
-            make_map(&g.mapA1, W3, (long long)E * h, f, 64, 64) && make_map(&g.mapB0, xbuf, Tk, h, 64, 64);
+  bool ok = tc_make_map(&g.mapA0, W1, (long long)E * h, f, 64, 64) &&
+            tc_make_map(&g.mapA1, W3, (long long)E * h, f, 64, 64) && tc_make_map(&g.mapB0, xbuf, Tk, h, 64, 64);
   if (!ok) return -1;
   g.offsets = offsets; g.E = E; g.M = f; g.K = h; g.a_rows = h;
   g.out0 = static_cast<__nv_bfloat16*>(h1); g.out1 = static_cast<__nv_bfloat16*>(h3);
@@ -690,7 +582,7 @@ int tc_expert_ffn(const void* xbuf, const int* offsets, const void* W1, const vo
   if (launch<GATEUP>(g, st)) return -1;
 
   TcParams d = blank_params();
-  ok = make_map(&d.mapA0, W2, (long long)E * f, h, 64, 64) && make_map(&d.mapB0, a, Tk, f, 64, 64);
+  ok = tc_make_map(&d.mapA0, W2, (long long)E * f, h, 64, 64) && tc_make_map(&d.mapB0, a, Tk, f, 64, 64);
   if (!ok) return -1;
   d.offsets = offsets; d.E = E; d.M = h; d.K = f; d.a_rows = f;
   d.out0 = static_cast<__nv_bfloat16*>(ybuf); d.ld_out = h; d.status = status;
@@ -703,7 +595,7 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
                       cudaStream_t st) {
   // dA^T = W2[e] dY^T, fused with the SwiGLU backward -> dh1, dh3
   TcParams da = blank_params();
-  bool ok = make_map(&da.mapA0, W2, (long long)E * f, h, 64, 128) && make_map(&da.mapB0, dybuf, Tk, h, 64, 64);
+  bool ok = tc_make_map(&da.mapA0, W2, (long long)E * f, h, 64, 128) && tc_make_map(&da.mapB0, dybuf, Tk, h, 64, 64);
   if (!ok) return -1;
   da.offsets = offsets; da.E = E; da.M = f; da.K = h; da.a_rows = f;
   da.out0 = static_cast<__nv_bfloat16*>(dh1); da.out1 = static_cast<__nv_bfloat16*>(dh3);
@@ -713,8 +605,8 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
 
   // dX^T = W1[e] dh1^T + W3[e] dh3^T
   TcParams dx = blank_params();
-  ok = make_map(&dx.mapA0, W1, (long long)E * h, f, 64, 128) && make_map(&dx.mapA1, W3, (long long)E * h, f, 64, 128) &&
-       make_map(&dx.mapB0, dh1, Tk, f, 64, 64) && make_map(&dx.mapB1, dh3, Tk, f, 64, 64);
+  ok = tc_make_map(&dx.mapA0, W1, (long long)E * h, f, 64, 128) && tc_make_map(&dx.mapA1, W3, (long long)E * h, f, 64, 128) &&
+       tc_make_map(&dx.mapB0, dh1, Tk, f, 64, 64) && tc_make_map(&dx.mapB1, dh3, Tk, f, 64, 64);
   if (!ok) return -1;
   dx.offsets = offsets; dx.E = E; dx.M = h; dx.K = f; dx.a_rows = h;
   dx.out0 = static_cast<__nv_bfloat16*>(dxbuf); dx.ld_out = h; dx.status = status;
@@ -722,11 +614,11 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
 
   // dW1[e]^T = dh1^T X, dW3[e]^T = dh3^T X  (stored as dW1[e][h][f])
   TcParams w13 = blank_params();
-  ok = make_map(&w13.mapA0, dh1, Tk, f, 64, 64) && make_map(&w13.mapA1, dh3, Tk, f, 64, 64) &&
-       make_map(&w13.mapB0, xbuf, Tk, h, 64, 64);
+  ok = tc_make_map(&w13.mapA0, dh1, Tk, f, 64, 64) && tc_make_map(&w13.mapA1, dh3, Tk, f, 64, 64) &&
+       tc_make_map(&w13.mapB0, xbuf, Tk, h, 64, 64);
   if (!ok) return -1;
-  ok = make_map(&w13.mapO0, dW1, (long long)E * h, f, 32, 16, false) &&
-       make_map(&w13.mapO1, dW3, (long long)E * h, f, 32, 16, false);
+  ok = tc_make_map(&w13.mapO0, dW1, (long long)E * h, f, 32, 16, false) &&
+       tc_make_map(&w13.mapO1, dW3, (long long)E * h, f, 32, 16, false);
   if (!ok) return -1;
   w13.offsets = offsets; w13.E = E; w13.M = f; w13.Nw = h; w13.a_rows = h;
   w13.out0 = static_cast<__nv_bfloat16*>(dW1); w13.out1 = static_cast<__nv_bfloat16*>(dW3);
@@ -735,9 +627,9 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
 
   // dW2[e]^T = dY^T a  (stored as dW2[e][f][h])
   TcParams w2 = blank_params();
-  ok = make_map(&w2.mapA0, dybuf, Tk, h, 64, 64) && make_map(&w2.mapB0, a, Tk, f, 64, 64);
+  ok = tc_make_map(&w2.mapA0, dybuf, Tk, h, 64, 64) && tc_make_map(&w2.mapB0, a, Tk, f, 64, 64);
   if (!ok) return -1;
-  ok = make_map(&w2.mapO0, dW2, (long long)E * f, h, 32, 16, false);
+  ok = tc_make_map(&w2.mapO0, dW2, (long long)E * f, h, 32, 16, false);
   if (!ok) return -1;
   w2.offsets = offsets; w2.E = E; w2.M = h; w2.Nw = f; w2.a_rows = f;
   w2.out0 = static_cast<__nv_bfloat16*>(dW2); w2.ld_out = h; w2.out_expert_stride = (long long)f * h;

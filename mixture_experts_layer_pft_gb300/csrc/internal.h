@@ -39,6 +39,9 @@ void launch_pft_build(const int* topk_idx, int T, int E, int k, int* num_ids, in
 
 // gemm_simt.cu -- fp32-accumulating SIMT GEMMs (all shapes, both dtypes)
 int router_splits(int M, int N, int K);  // split-K factor of a router GEMM (>= 1)
+// out[i] = sum over z ascending of partial[z * count + i] (+ bias[i % N]), fp32
+void launch_splitk_reduce(const float* partial, int splits, long long count, int N, const float* bias,
+                          float* out, cudaStream_t st);
 void simt_router_logits(int dtype, const void* x, const float* Wg, const float* bias, int T, int h,
                         int E, float* logits, float* partial, cudaStream_t st);
 void simt_router_dwg(int dtype, const void* x, const float* d_logits, int T, int h, int E,
@@ -52,6 +55,15 @@ void simt_expert_ffn_bwd(int dtype, const void* dybuf, const void* xbuf, const v
                          const void* h3, const void* a, const int* offsets, const void* W1,
                          const void* W3, const void* W2, int Tk, int E, int h, int f, void* dxbuf,
                          void* dW1, void* dW3, void* dW2, void* dh1, void* dh3, cudaStream_t st);
+
+// router_tc.cu -- router GEMMs on tcgen05 over exact three-plane bf16 splits (bf16 activations,
+// h a multiple of 64, E of 16).  The scratch follows the workspace header, 256-byte aligned.
+bool tc_router_supported(int dtype, int h, int E);
+size_t tc_router_scratch(int op, int T, int h, int E);  // op 0: forward, 1: backward
+int tc_router_logits(const void* x, const float* Wg, const float* bias, int T, int h, int E, float* logits,
+                     void* scratch, int* status, cudaStream_t st);
+int tc_router_bwd(const void* x, const float* Wg, const float* d_logits, int T, int h, int E, float* dWg,
+                  float* dx_router, void* scratch, int* status, cudaStream_t st);
 
 // gemm_tc.cu -- tcgen05/TMEM/TMA grouped GEMMs (bf16; h and f multiples of 128)
 bool tc_supported(int dtype, int h, int f);

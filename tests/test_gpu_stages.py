@@ -111,6 +111,69 @@ def test_route_bwd(B, dt, T, h, E, k):
     assert B.moe_check_status(ws) == 0
 
 
+@pytest.mark.parametrize("T,h,E", [(300, 7168, 256), (4096, 2048, 64), (1000, 5120, 128), (257, 2048, 80)])
+def test_router_gemms_at_full_widths(B, T, h, E):
+    """bf16 activations with an fp32 router at the pages' widths (long sums over h = 7168 and
+    T = 4096): logits, dWg and dx stay within the fp32 tolerance of the exact sums."""
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    dt = torch.bfloat16
+    k = 2
+    x = random_tensor((T, h), 21, dt, "cuda")
+    Wg = random_tensor((h, E), 22, torch.float32, "cuda", std=h ** -0.5)
+    logits = torch.empty(T, E, device="cuda")
+    probs = torch.empty(T, E, device="cuda")
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    w = torch.empty(T, k, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, 8, dt)
+    B.moe_route(x, Wg, None, k, logits, probs, idx, w, ws)
+    want = O.router_logits(np64(x), np64(Wg), None, "f32")
+    assert rel_l2(np64(logits), want) <= TOL["f32"]
+    d_w = random_tensor((T, k), 23, torch.float32, "cuda")
+    d_logits = torch.empty(T, E, device="cuda")
+    dWg = torch.empty(h, E, device="cuda")
+    dxr = torch.empty(T, h, device="cuda")
+    B.moe_route_bwd(x, Wg, probs, idx, d_w, d_logits, dWg, dxr, ws)
+    r = O.route_bwd(np64(x), np64(Wg), np64(probs), npi(idx), np64(d_w), "f32")
+    assert rel_l2(np64(d_logits), r["d_logits"]) <= TOL["f32"]
+    assert rel_l2(np64(dWg), r["dWg"]) <= TOL["f32"]
+    assert rel_l2(np64(dxr), r["dx_router"]) <= TOL["f32"]
+    assert B.moe_check_status(ws) == 0
+
+
+@pytest.mark.parametrize("T,h,E", [(300, 2048, 64), (77, 512, 256)])
+def test_tensor_core_router_matches_fp32_fma_router(B, monkeypatch, T, h, E):
+    """The tensor-core router (exact bf16 planes, short truncated chains) and the fp32 FMA router
+    agree to fp32 accuracy on the same inputs."""
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    dt = torch.bfloat16
+    k = 4
+    x = random_tensor((T, h), 31, dt, "cuda")
+    Wg = random_tensor((h, E), 32, torch.float32, "cuda", std=h ** -0.5)
+    d_w = random_tensor((T, k), 33, torch.float32, "cuda")
+    probs0, idx0, _, _ = route_from_logits(B, gen_logits(T, E, 34), k)
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, 8, dt)
+    outs = {}
+    for engine in ("tc", "simt"):
+        if engine == "simt":
+            monkeypatch.setenv("MOE_PFT_GEMM", "simt")
+        else:
+            monkeypatch.delenv("MOE_PFT_GEMM", raising=False)
+        o = {"logits": torch.empty(T, E, device="cuda"), "d_logits": torch.empty(T, E, device="cuda"),
+             "dWg": torch.empty(h, E, device="cuda"), "dx": torch.empty(T, h, device="cuda")}
+        probs = torch.empty(T, E, device="cuda")
+        idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+        w = torch.empty(T, k, device="cuda")
+        B.moe_route(x, Wg, None, k, o["logits"], probs, idx, w, ws)
+        B.moe_route_bwd(x, Wg, probs0, idx0, d_w, o["d_logits"], o["dWg"], o["dx"], ws)
+        torch.cuda.synchronize()
+        outs[engine] = o
+    assert B.moe_check_status(ws) == 0
+    for n in outs["tc"]:
+        assert rel_l2(np64(outs["tc"][n]), np64(outs["simt"][n])) <= TOL["f32"], n
+
+
 @pytest.mark.parametrize("gate,renorm", [("softmax", True), ("sigmoid", False), ("sigmoid", True)])
 @pytest.mark.parametrize("T,E,k", [(37, 8, 2), (300, 64, 6), (129, 256, 8), (40, 1000, 5)])
 def test_gate_variants_given_the_same_logits(B, gate, renorm, T, E, k):
