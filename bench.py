@@ -79,6 +79,11 @@ def read_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+CSRC = "mixture_experts_layer_pft_gb300/csrc/"
+# headers every kernel source includes: a change there also invalidates recorded counters
+KERNEL_HEADERS = [CSRC + "common.cuh", CSRC + "tc_ptx.cuh"]
+
+
 def source_hash(files):
     h = hashlib.sha256()
     for f in files:
@@ -256,7 +261,6 @@ def workload_desc(w):
             f"{'fwd+bwd' if w.backward else 'fwd only'}{', Zipf router bias' if w.skew else ''}")
 
 
-CSRC = "mixture_experts_layer_pft_gb300/csrc/"
 
 
 def kernel_names(stage, n, w):
@@ -478,7 +482,7 @@ def run_ours(args, w):
         if c["flops"]:
             roof["tensor_frac"] = c["flops"] / (dom_ms * 1e-3) / (float(peaks[fkey]) * 1e12)
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = recorded_traffic(f"{dom}:{w.name}", source_hash([kern_src[dom]]))
+    roof["traffic"] = recorded_traffic(f"{dom}:{w.name}", source_hash([kern_src[dom]] + KERNEL_HEADERS))
     roof["kernel"] = dom
     roof["launch_us"] = round(1e3 * dom_ms, 2)
     roof["peak_source"] = which

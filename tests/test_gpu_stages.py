@@ -384,6 +384,50 @@ def test_tensor_core_engine_matches_simt_engine(B, monkeypatch, T, h, E, k, f, s
         assert rel_l2(np64(outs["tc"][n]), np64(outs["simt"][n])) <= TOL["bf16"], n
 
 
+def test_weight_gradients_at_segment_length_edges(B):
+    """Expert segments whose lengths straddle the 16-row MMA slice, the 64-row K step and the
+    256-row resident chunk of the weight-gradient GEMMs (0, 1, 15, 16, 17, 63, 64, 65, 255, 256,
+    257 and 513 rows), built directly as PFT offsets; dW1, dW3, dW2 and dX against the oracle."""
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    dt = torch.bfloat16
+    lens = np.array([0, 1, 15, 16, 17, 63, 64, 65, 255, 256, 257, 513], dtype=np.int64)
+    E, h, f = len(lens), 256, 384
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    Tk = int(offsets[-1])
+    d = {
+        "xbuf": random_tensor((Tk, h), 51, dt, "cuda"),
+        "dybuf": random_tensor((Tk, h), 52, dt, "cuda"),
+        "W1": random_tensor((E, h, f), 53, dt, "cuda", std=h ** -0.5),
+        "W3": random_tensor((E, h, f), 54, dt, "cuda", std=h ** -0.5),
+        "W2": random_tensor((E, f, h), 55, dt, "cuda", std=f ** -0.5),
+    }
+    off = torch.from_numpy(offsets).cuda()
+    want = O.expert_ffn(np64(d["xbuf"]), offsets, np64(d["W1"]), np64(d["W3"]), np64(d["W2"]), "bf16")
+    sv = {n: torch.from_numpy(want[n]).to(dt).cuda() for n in ("h1", "h3", "a")}
+    z = lambda *s: torch.full(s, float("nan"), dtype=dt, device="cuda")  # noqa: E731
+    dxbuf, dW1, dW3, dW2 = z(Tk, h), z(E, h, f), z(E, h, f), z(E, f, h)
+    ws = B.new_workspace(B.MOE_OP_ALL, Tk, h, E, 1, f, dt)
+    B.moe_expert_ffn_bwd(d["dybuf"], d["xbuf"], sv["h1"], sv["h3"], sv["a"], off, d["W1"], d["W3"], d["W2"],
+                         dxbuf, dW1, dW3, dW2, ws)
+    torch.cuda.synchronize()
+    wb = O.expert_ffn_bwd(np64(d["dybuf"]), np64(d["xbuf"]), want["h1"], want["h3"], want["a"], offsets,
+                          np64(d["W1"]), np64(d["W3"]), np64(d["W2"]), "bf16")
+    for n, got in (("dxbuf", dxbuf), ("dW1", dW1), ("dW3", dW3), ("dW2", dW2)):
+        g = np64(got)
+        assert np.isfinite(g).all(), n
+        for e in range(E):  # every expert on its own, so a wrong segment cannot hide in the norm
+            if n == "dxbuf":
+                sl = slice(offsets[e], offsets[e + 1])
+                if lens[e]:
+                    assert rel_l2(g[sl], wb[n][sl]) <= TOL["bf16"], (n, e)
+            elif lens[e] == 0:
+                assert (g[e] == 0).all(), (n, e)
+            else:
+                assert rel_l2(g[e], wb[n][e]) <= TOL["bf16"], (n, e, lens[e])
+    assert B.moe_check_status(ws) == 0
+
+
 @pytest.mark.parametrize("T,h,E,k,f,dt,skew", EXPERT_SHAPES)
 def test_expert_ffn_forward_and_backward(B, T, h, E, k, f, dt, skew):
     p, d = expert_inputs(T, h, E, k, f, dt, 40 + T, skew)
