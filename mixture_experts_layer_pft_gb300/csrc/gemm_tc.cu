@@ -50,13 +50,19 @@ constexpr int kTmemCols = 512;
 constexpr int kMaxE = 1024;
 constexpr uint32_t kStageRegion = 196608;  // shared memory given to the stage ring
 
-enum Mode { GATEUP = 0, DOWN = 1, DA = 2, DX = 3, WGRAD13 = 4, WGRAD2 = 5 };
+// GATEUP_WIDE is the gate/up GEMM with 256-token chunks: each weight tile streams once per
+// expert when experts hold up to 256 tokens, at the price of one accumulator set (its epilogue is
+// not overlapped with the next unit's MMAs) and three stages in place of four.  The host picks it
+// when experts average more than 96 tokens (every X-MoE shape measured: -5% to -22% against the
+// 128-token chunks).
+enum Mode { GATEUP = 0, DOWN = 1, DA = 2, DX = 3, WGRAD13 = 4, WGRAD2 = 5, GATEUP_WIDE = 6 };
 
 template <int MODE> struct Cfg {
-  static constexpr int NUM_A = (MODE == GATEUP || MODE == WGRAD13) ? 2 : 1;
-  static constexpr bool A_MN = (MODE == GATEUP || MODE == DOWN || MODE == WGRAD13 || MODE == WGRAD2);
+  static constexpr bool GU = (MODE == GATEUP || MODE == GATEUP_WIDE);
+  static constexpr int NUM_A = (GU || MODE == WGRAD13) ? 2 : 1;
+  static constexpr bool A_MN = (GU || MODE == DOWN || MODE == WGRAD13 || MODE == WGRAD2);
   static constexpr bool B_MN = (MODE == WGRAD13 || MODE == WGRAD2);
-  static constexpr bool TOKEN_N = (MODE <= DX);
+  static constexpr bool TOKEN_N = (MODE <= DX || MODE == GATEUP_WIDE);
   // gate/up keeps two accumulators per unit; 128-token chunks leave room to double-buffer them
   static constexpr int BN = (MODE == WGRAD13 || MODE == GATEUP) ? 128 : 256;
   static constexpr uint32_t A_BYTES = NUM_A * kATile;
@@ -65,9 +71,9 @@ template <int MODE> struct Cfg {
   static constexpr int ACC_BUFS = kTmemCols / (NUM_A * BN);
   // epilogue: two warps per TMEM lane quarter (splitting the columns), except for the gate/up
   // GEMM, whose three outputs per element need more transpose buffer than shared memory has left
-  static constexpr int EPI_WARPS = (MODE == GATEUP) ? 4 : 8;
+  static constexpr int EPI_WARPS = (MODE == GATEUP) ? 4 : 8;  // GATEUP_WIDE: 3 stages leave room for 8
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int NSLOT = (MODE == GATEUP) ? 3 : (MODE == DA || MODE == WGRAD13) ? 2 : 1;
+  static constexpr int NSLOT = GU ? 3 : (MODE == DA || MODE == WGRAD13) ? 2 : 1;
   static_assert(ACC_BUFS >= 1 && STAGES >= 2, "tile configuration");
 };
 
@@ -259,11 +265,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           const uint32_t a_sm = ring + s * C::STAGE_BYTES;
           const uint32_t b_sm = a_sm + C::A_BYTES;
           const int k0 = ks * BK;
-          if (MODE == GATEUP || MODE == DOWN) {
+          if (C::GU || MODE == DOWN) {
             const int y = w.e * p.a_rows + k0;
             tma_load_2d(a_sm, &p.mapA0, &full_bar[s], w.m0, y);
             tma_load_2d(a_sm + kBox, &p.mapA0, &full_bar[s], w.m0 + 64, y);
-            if (MODE == GATEUP) {
+            if (C::GU) {
               tma_load_2d(a_sm + kATile, &p.mapA1, &full_bar[s], w.m0, y);
               tma_load_2d(a_sm + kATile + kBox, &p.mapA1, &full_bar[s], w.m0 + 64, y);
             }
@@ -441,7 +447,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
         }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          if (MODE == GATEUP) {
+          if (C::GU) {
             const float h1 = v0[i], h3 = v1[i];
             stg[0][i][lane] = __float2bfloat16_rn(h1);
             stg[1][i][lane] = __float2bfloat16_rn(h3);
@@ -475,7 +481,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           const int v = lane + 32 * r, ci = v >> 2, part = v & 3;
           if (c0 + ci < w.ncols) {
             const size_t o = ebase + (colbase + c0 + ci) * (size_t)p.ld_out + mbase + part * 8;
-            if (MODE == GATEUP) {
+            if (C::GU) {
               *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[0][ci][part * 8]);
               *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
               *reinterpret_cast<uint4*>(p.out2 + o) = *reinterpret_cast<const uint4*>(&stg[2][ci][part * 8]);
@@ -579,7 +585,8 @@ int tc_expert_ffn(const void* xbuf, const int* offsets, const void* W1, const vo
   g.offsets = offsets; g.E = E; g.M = f; g.K = h; g.a_rows = h;
   g.out0 = static_cast<__nv_bfloat16*>(h1); g.out1 = static_cast<__nv_bfloat16*>(h3);
   g.out2 = static_cast<__nv_bfloat16*>(a); g.ld_out = f; g.status = status;
-  if (launch<GATEUP>(g, st)) return -1;
+  // experts averaging more than 96 tokens: one 256-token chunk per expert in most cases
+  if ((Tk > 96LL * E ? launch<GATEUP_WIDE>(g, st) : launch<GATEUP>(g, st)) != 0) return -1;
 
   TcParams d = blank_params();
   ok = tc_make_map(&d.mapA0, W2, (long long)E * f, h, 64, 64) && tc_make_map(&d.mapB0, a, Tk, f, 64, 64);

@@ -356,6 +356,8 @@ EXPERT_SHAPES = [
     (333, 384, 12, 3, 256, torch.bfloat16, False),  # ragged segments below one chunk
     (1000, 256, 4, 2, 128, torch.bfloat16, True),   # segments of several 256-row chunks, Zipf
     (96, 640, 64, 6, 384, torch.bfloat16, True),    # many empty and tiny segments
+    (600, 256, 4, 2, 256, torch.bfloat16, False),   # > 160 rows per expert: 256-row gate/up chunks
+    (520, 384, 4, 2, 128, torch.bfloat16, True),    # 256-row chunks over Zipf-sized segments
 ]
 
 
