@@ -55,14 +55,24 @@ constexpr uint32_t kStageRegion = 196608;  // shared memory given to the stage r
 // not overlapped with the next unit's MMAs) and three stages in place of four.  The host picks it
 // when experts average more than 96 tokens (every X-MoE shape measured: -5% to -22% against the
 // 128-token chunks).
-enum Mode { GATEUP = 0, DOWN = 1, DA = 2, DX = 3, WGRAD13 = 4, WGRAD2 = 5, GATEUP_WIDE = 6 };
+// DOWN_PAIR, DA_PAIR and DX_PAIR are DOWN, DA and DX with two 128-row M tiles per unit: the two
+// accumulators share each token-chunk stage, so the chunk streams into shared memory once per 256
+// rows of the weight dimension instead of once per 128 (one accumulator set, three stages).
+enum Mode {
+  GATEUP = 0, DOWN = 1, DA = 2, DX = 3, WGRAD13 = 4, WGRAD2 = 5, GATEUP_WIDE = 6,
+  DOWN_PAIR = 7, DA_PAIR = 8, DX_PAIR = 9
+};
 
 template <int MODE> struct Cfg {
-  static constexpr bool GU = (MODE == GATEUP || MODE == GATEUP_WIDE);
-  static constexpr int NUM_A = (GU || MODE == WGRAD13) ? 2 : 1;
-  static constexpr bool A_MN = (GU || MODE == DOWN || MODE == WGRAD13 || MODE == WGRAD2);
-  static constexpr bool B_MN = (MODE == WGRAD13 || MODE == WGRAD2);
-  static constexpr bool TOKEN_N = (MODE <= DX || MODE == GATEUP_WIDE);
+  static constexpr int BASE = MODE == GATEUP_WIDE ? GATEUP : MODE == DOWN_PAIR ? DOWN
+                              : MODE == DA_PAIR ? DA : MODE == DX_PAIR ? DX : MODE;
+  static constexpr bool PAIR = (MODE == DOWN_PAIR || MODE == DA_PAIR || MODE == DX_PAIR);
+  static constexpr bool GU = (BASE == GATEUP);
+  static constexpr int NUM_A = (GU || BASE == WGRAD13 || PAIR) ? 2 : 1;
+  static constexpr bool A_MN = (GU || BASE == DOWN || BASE == WGRAD13 || BASE == WGRAD2);
+  static constexpr bool B_MN = (BASE == WGRAD13 || BASE == WGRAD2);
+  static constexpr bool TOKEN_N = (BASE <= DX);
+  static constexpr int MT = PAIR ? 2 * BM : BM;  // rows of the weight (M) dimension per unit
   // gate/up keeps two accumulators per unit; 128-token chunks leave room to double-buffer them
   static constexpr int BN = (MODE == WGRAD13 || MODE == GATEUP) ? 128 : 256;
   static constexpr uint32_t A_BYTES = NUM_A * kATile;
@@ -73,7 +83,7 @@ template <int MODE> struct Cfg {
   // GEMM, whose three outputs per element need more transpose buffer than shared memory has left
   static constexpr int EPI_WARPS = (MODE == GATEUP) ? 4 : 8;  // GATEUP_WIDE: 3 stages leave room for 8
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int NSLOT = GU ? 3 : (MODE == DA || MODE == WGRAD13) ? 2 : 1;
+  static constexpr int NSLOT = GU ? 3 : (BASE == DA || BASE == WGRAD13) ? 2 : 1;
   static_assert(ACC_BUFS >= 1 && STAGES >= 2, "tile configuration");
 };
 
@@ -144,13 +154,13 @@ __device__ __forceinline__ Unit decode(int u, const Sched& sc, const int* s_pref
     const int local = u - s_pref[e];
     const int mtile = local / nc, c = local % nc;
     w.e = e;
-    w.m0 = mtile * BM;
+    w.m0 = mtile * C::MT;
     w.row0 = s_off[e] + c * cs;
     w.rows = min(cs, n - c * cs);
     w.n0 = 0;
     w.ncols = w.rows;
     w.nmma = (w.rows + 15) & ~15;
-    w.nk = (MODE == DX) ? 2 * p.K / BK : p.K / BK;
+    w.nk = (C::BASE == DX) ? 2 * p.K / BK : p.K / BK;
   } else {
     const int per = sc.mt * sc.nt;
     w.e = u / per;
@@ -197,7 +207,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
     // units per expert, then an inclusive scan into s_pref[1..E] (s_pref[0] = 0)
     const int per = (p.E + 31) / 32;
     const int b0 = min(lane * per, p.E), b1 = min(b0 + per, p.E);
-    const int mt = p.M / BM;
+    const int mt = p.M / C::MT;
     int local = 0;
     for (int e = b0; e < b1; ++e) {
       int ue;
@@ -265,22 +275,27 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           const uint32_t a_sm = ring + s * C::STAGE_BYTES;
           const uint32_t b_sm = a_sm + C::A_BYTES;
           const int k0 = ks * BK;
-          if (C::GU || MODE == DOWN) {
+          if (C::GU || C::BASE == DOWN) {
             const int y = w.e * p.a_rows + k0;
             tma_load_2d(a_sm, &p.mapA0, &full_bar[s], w.m0, y);
             tma_load_2d(a_sm + kBox, &p.mapA0, &full_bar[s], w.m0 + 64, y);
             if (C::GU) {
               tma_load_2d(a_sm + kATile, &p.mapA1, &full_bar[s], w.m0, y);
               tma_load_2d(a_sm + kATile + kBox, &p.mapA1, &full_bar[s], w.m0 + 64, y);
+            } else if (C::PAIR) {
+              tma_load_2d(a_sm + kATile, &p.mapA0, &full_bar[s], w.m0 + 128, y);
+              tma_load_2d(a_sm + kATile + kBox, &p.mapA0, &full_bar[s], w.m0 + 192, y);
             }
             for (int j = 0; j < nbB; ++j) tma_load_2d(b_sm + j * kBox, &p.mapB0, &full_bar[s], k0, w.row0 + 64 * j);
-          } else if (MODE == DA) {
-            tma_load_2d(a_sm, &p.mapA0, &full_bar[s], k0, w.e * p.a_rows + w.m0);
+          } else if (C::BASE == DA) {
+            for (int a = 0; a < C::NUM_A; ++a)
+              tma_load_2d(a_sm + a * kATile, &p.mapA0, &full_bar[s], k0, w.e * p.a_rows + w.m0 + a * BM);
             for (int j = 0; j < nbB; ++j) tma_load_2d(b_sm + j * kBox, &p.mapB0, &full_bar[s], k0, w.row0 + 64 * j);
-          } else if (MODE == DX) {
+          } else if (C::BASE == DX) {
             const bool second = k0 >= p.K;
             const int kk = second ? k0 - p.K : k0;
-            tma_load_2d(a_sm, second ? &p.mapA1 : &p.mapA0, &full_bar[s], kk, w.e * p.a_rows + w.m0);
+            for (int a = 0; a < C::NUM_A; ++a)
+              tma_load_2d(a_sm + a * kATile, second ? &p.mapA1 : &p.mapA0, &full_bar[s], kk, w.e * p.a_rows + w.m0 + a * BM);
             for (int j = 0; j < nbB; ++j)
               tma_load_2d(b_sm + j * kBox, second ? &p.mapB1 : &p.mapB0, &full_bar[s], kk, w.row0 + 64 * j);
           } else {  // wgrad: K runs over the expert's token rows
@@ -391,16 +406,19 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       const uint32_t aph = (uint32_t)(it / C::ACC_BUFS) & 1u;
       if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[b], aph, &s_abort, p.status))) break;
       tc_fence_after();
-      const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::NUM_A * C::BN);
+      const uint32_t t0u = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::NUM_A * C::BN);
       const bool zero = (w.nk == 0);
       // output element (m, c) lives at [colbase + c][mbase + lane] (+ the expert's base for wgrad)
       const size_t colbase = C::TOKEN_N ? (size_t)w.row0 : (size_t)w.n0;
       const size_t ebase = C::TOKEN_N ? 0 : (size_t)w.e * (size_t)p.out_expert_stride;
-      const int mbase = w.m0 + q * 32;
+      // a paired unit's two M tiles go out one after the other (accumulators at t0 and t0 + BN)
+      for (int mtl = 0; mtl < (C::PAIR ? 2 : 1); ++mtl) {
+      const uint32_t t0 = t0u + (uint32_t)(mtl * C::BN);
+      const int mbase = w.m0 + mtl * BM + q * 32;
       for (int c0 = 16 * cg; c0 < w.ncols; c0 += 16 * G) {
         // (1) DA: start the coalesced 16-byte loads of h1, h3 for these 16 columns
         uint4 in_a[2], in_b[2];
-        if (MODE == DA) {
+        if (C::BASE == DA) {
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const int v = lane + 32 * r, ci = v >> 2, part = v & 3;
@@ -417,7 +435,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
         float v0[16], v1[16];
         if (!zero) {
           tmem_ld16(t0 + c0, v0);
-          if (C::NUM_A == 2) tmem_ld16(t0 + C::BN + c0, v1);
+          if (C::GU || C::BASE == WGRAD13) tmem_ld16(t0 + C::BN + c0, v1);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -425,7 +443,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
         }
         // (3) DA: transpose h1, h3 through shared memory to this lane's row
         float z1[16], z3[16];
-        if (MODE == DA) {
+        if (C::BASE == DA) {
 #pragma unroll
           for (int r = 0; r < 2; ++r) {
             const int v = lane + 32 * r, ci = v >> 2, part = v & 3;
@@ -452,7 +470,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
             stg[0][i][lane] = __float2bfloat16_rn(h1);
             stg[1][i][lane] = __float2bfloat16_rn(h3);
             stg[2][i][lane] = __float2bfloat16_rn(h1 * sigmoid_bf16_epilogue(h1) * h3);
-          } else if (MODE == DA) {
+          } else if (C::BASE == DA) {
             const float sg = sigmoid_bf16_epilogue(z1[i]);
             const float da = v0[i];
             stg[0][i][lane] = __float2bfloat16_rn(da * z3[i] * sg * (1.f + z1[i] * (1.f - sg)));
@@ -485,7 +503,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
               *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[0][ci][part * 8]);
               *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
               *reinterpret_cast<uint4*>(p.out2 + o) = *reinterpret_cast<const uint4*>(&stg[2][ci][part * 8]);
-            } else if (MODE == DA) {
+            } else if (C::BASE == DA) {
               *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[0][ci][part * 8]);
               *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
             } else {
@@ -496,6 +514,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           }
         }
         __syncwarp();
+      }
       }
       tc_fence_before();
       __syncwarp();
@@ -593,7 +612,7 @@ int tc_expert_ffn(const void* xbuf, const int* offsets, const void* W1, const vo
   if (!ok) return -1;
   d.offsets = offsets; d.E = E; d.M = h; d.K = f; d.a_rows = f;
   d.out0 = static_cast<__nv_bfloat16*>(ybuf); d.ld_out = h; d.status = status;
-  return launch<DOWN>(d, st);
+  return h % 256 == 0 ? launch<DOWN_PAIR>(d, st) : launch<DOWN>(d, st);
 }
 
 int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const void* h3, const void* a,
@@ -608,7 +627,7 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
   da.out0 = static_cast<__nv_bfloat16*>(dh1); da.out1 = static_cast<__nv_bfloat16*>(dh3);
   da.in0 = static_cast<const __nv_bfloat16*>(h1); da.in1 = static_cast<const __nv_bfloat16*>(h3);
   da.ld_out = f; da.status = status;
-  if (launch<DA>(da, st)) return -1;
+  if ((f % 256 == 0 ? launch<DA_PAIR>(da, st) : launch<DA>(da, st)) != 0) return -1;
 
   // dX^T = W1[e] dh1^T + W3[e] dh3^T
   TcParams dx = blank_params();
@@ -617,7 +636,7 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
   if (!ok) return -1;
   dx.offsets = offsets; dx.E = E; dx.M = h; dx.K = f; dx.a_rows = h;
   dx.out0 = static_cast<__nv_bfloat16*>(dxbuf); dx.ld_out = h; dx.status = status;
-  if (launch<DX>(dx, st)) return -1;
+  if ((h % 256 == 0 ? launch<DX_PAIR>(dx, st) : launch<DX>(dx, st)) != 0) return -1;
 
   // dW1[e]^T = dh1^T X, dW3[e]^T = dh3^T X  (stored as dW1[e][h][f])
   TcParams w13 = blank_params();
