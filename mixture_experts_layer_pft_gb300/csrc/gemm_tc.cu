@@ -60,20 +60,22 @@ constexpr uint32_t kStageRegion = 196608;  // shared memory given to the stage r
 // rows of the weight dimension instead of once per 128 (one accumulator set, three stages).
 enum Mode {
   GATEUP = 0, DOWN = 1, DA = 2, DX = 3, WGRAD13 = 4, WGRAD2 = 5, GATEUP_WIDE = 6,
-  DOWN_PAIR = 7, DA_PAIR = 8, DX_PAIR = 9
+  DOWN_PAIR = 7, DA_PAIR = 8, DX_PAIR = 9, WGRAD13_WIDE = 10
 };
 
 template <int MODE> struct Cfg {
   static constexpr int BASE = MODE == GATEUP_WIDE ? GATEUP : MODE == DOWN_PAIR ? DOWN
-                              : MODE == DA_PAIR ? DA : MODE == DX_PAIR ? DX : MODE;
+                              : MODE == DA_PAIR ? DA : MODE == DX_PAIR ? DX
+                              : MODE == WGRAD13_WIDE ? WGRAD13 : MODE;
   static constexpr bool PAIR = (MODE == DOWN_PAIR || MODE == DA_PAIR || MODE == DX_PAIR);
   static constexpr bool GU = (BASE == GATEUP);
-  static constexpr int NUM_A = (GU || BASE == WGRAD13 || PAIR) ? 2 : 1;
+  static constexpr int NUM_A = (GU || BASE == WGRAD13 || PAIR) ? 2 : 1;  // accumulators per unit
   static constexpr bool A_MN = (GU || BASE == DOWN || BASE == WGRAD13 || BASE == WGRAD2);
   static constexpr bool B_MN = (BASE == WGRAD13 || BASE == WGRAD2);
   static constexpr bool TOKEN_N = (BASE <= DX);
   static constexpr int MT = PAIR ? 2 * BM : BM;  // rows of the weight (M) dimension per unit
-  // gate/up keeps two accumulators per unit; 128-token chunks leave room to double-buffer them
+  // gate/up and dW1/dW3 keep two accumulators per unit; 128-column tiles leave room to
+  // double-buffer them (the _WIDE variants take 256 columns and one accumulator set)
   static constexpr int BN = (MODE == WGRAD13 || MODE == GATEUP) ? 128 : 256;
   static constexpr uint32_t A_BYTES = NUM_A * kATile;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + (BN / 64) * kBox;
@@ -302,7 +304,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
             const int y = w.row0 + k0;
             tma_load_2d(a_sm, &p.mapA0, &full_bar[s], w.m0, y);
             tma_load_2d(a_sm + kBox, &p.mapA0, &full_bar[s], w.m0 + 64, y);
-            if (MODE == WGRAD13) {
+            if (C::BASE == WGRAD13) {
               tma_load_2d(a_sm + kATile, &p.mapA1, &full_bar[s], w.m0, y);
               tma_load_2d(a_sm + kATile + kBox, &p.mapA1, &full_bar[s], w.m0 + 64, y);
             }
@@ -477,7 +479,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
             stg[1][i][lane] = __float2bfloat16_rn(da * z1[i] * sg);
           } else {
             stg[0][i][lane] = __float2bfloat16_rn(v0[i]);
-            if (MODE == WGRAD13) stg[1][i][lane] = __float2bfloat16_rn(v1[i]);
+            if (C::BASE == WGRAD13) stg[1][i][lane] = __float2bfloat16_rn(v1[i]);
           }
         }
         __syncwarp();
@@ -488,7 +490,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           if (lane == 0) {
             const int y = w.e * p.a_rows + w.n0 + c0;  // row of the [E * rows, cols] view
             tma_store_2d(&p.mapO0, smem_u32(&stg[0][0][0]), mbase, y);
-            if (MODE == WGRAD13) tma_store_2d(&p.mapO1, smem_u32(&stg[1][0][0]), mbase, y);
+            if (C::BASE == WGRAD13) tma_store_2d(&p.mapO1, smem_u32(&stg[1][0][0]), mbase, y);
             bulk_commit();
           }
           continue;
@@ -508,7 +510,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
               *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
             } else {
               *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[0][ci][part * 8]);
-              if (MODE == WGRAD13)
+              if (C::BASE == WGRAD13)
                 *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
             }
           }
@@ -649,7 +651,7 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
   w13.offsets = offsets; w13.E = E; w13.M = f; w13.Nw = h; w13.a_rows = h;
   w13.out0 = static_cast<__nv_bfloat16*>(dW1); w13.out1 = static_cast<__nv_bfloat16*>(dW3);
   w13.ld_out = f; w13.out_expert_stride = (long long)h * f; w13.status = status;
-  if (launch<WGRAD13>(w13, st)) return -1;
+  if ((h % 256 == 0 ? launch<WGRAD13_WIDE>(w13, st) : launch<WGRAD13>(w13, st)) != 0) return -1;
 
   // dW2[e]^T = dY^T a  (stored as dW2[e][f][h])
   TcParams w2 = blank_params();
