@@ -3,9 +3,10 @@
 // All four are row gathers: every row of h elements moves as 16-byte vectors, a group of
 // `tpr` threads per row (tpr is a power of two, 32..256, chosen so each thread handles at
 // most four vectors per pass; rows wider than 256 x 4 vectors take several passes),
-// `256 / tpr` rows per 256-thread block.  Loads are issued before the
-// dependent stores so that each thread keeps several 16-byte requests in flight.  Sums run
-// in fp32 in a fixed order (j ascending), so results are bitwise reproducible; no atomics.
+// `256 / tpr` rows per 256-thread block.  Loads are issued before the dependent stores, and
+// the k-way gathers issue the loads of four source rows before summing any of them, so that
+// each thread keeps several 16-byte requests in flight.  Sums run in fp32 in a fixed order
+// (j ascending), so results are bitwise reproducible; no atomics.
 #include "common.cuh"
 #include "internal.h"
 
@@ -15,15 +16,20 @@ namespace {
 
 constexpr int kBlock = 256;
 constexpr int kMaxVecPerThread = 4;
+// The k-way gathers (combine, dispatch backward) issue the loads of kJB source rows before
+// consuming any, with at most kGatherVec vectors per thread per row, so each thread keeps
+// kJB * kGatherVec 16-byte loads in flight.
+constexpr int kJB = 4;
+constexpr int kGatherVec = 2;
 
 struct RowGeom {
   int tpr;       // threads per row
   int rows_per_block;
 };
 
-RowGeom row_geom(int nvec) {
+RowGeom row_geom(int nvec, int maxvec = kMaxVecPerThread) {
   int tpr = 32;
-  while (tpr < kBlock && tpr * kMaxVecPerThread < nvec) tpr *= 2;
+  while (tpr < kBlock && tpr * maxvec < nvec) tpr *= 2;
   return {tpr, kBlock / tpr};
 }
 
@@ -70,44 +76,59 @@ __global__ void __launch_bounds__(kBlock) combine_kernel(const T* __restrict__ y
                                                          int k, int nvec, int tpr, int Tk,
                                                          T* __restrict__ y, int* status) {
   constexpr int VN = Vec<T>::N;
+  constexpr int MV = kGatherVec;
   const int rpb = kBlock / tpr;
   const int t = blockIdx.x * rpb + threadIdx.x / tpr;
   const int lt = threadIdx.x % tpr;
   if (t >= T_) return;
   const uint4* yb = reinterpret_cast<const uint4*>(ybuf);
   uint4* dst = reinterpret_cast<uint4*>(y) + (size_t)t * nvec;
-  for (int vb = 0; vb < nvec; vb += tpr * kMaxVecPerThread) {
-    float acc[kMaxVecPerThread][VN];
+  for (int vb = 0; vb < nvec; vb += tpr * MV) {
+    float acc[MV][VN];
 #pragma unroll
-    for (int u = 0; u < kMaxVecPerThread; ++u)
+    for (int u = 0; u < MV; ++u)
 #pragma unroll
       for (int q = 0; q < VN; ++q) acc[u][q] = 0.f;
-    for (int j = 0; j < k; ++j) {
-      const int s = __ldg(slot_of + (size_t)t * k + j);
-      const float wj = __ldg(w + (size_t)t * k + j);
-      if ((unsigned)s >= (unsigned)Tk) {
-        if (lt == 0 && vb == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
-        continue;
+    for (int j0 = 0; j0 < k; j0 += kJB) {
+      // slots and weights of up to kJB rows, then all their loads, then the sums (j ascending)
+      int sj[kJB];
+      float wj[kJB];
+#pragma unroll
+      for (int jj = 0; jj < kJB; ++jj) {
+        sj[jj] = -1;
+        wj[jj] = 0.f;
+        if (j0 + jj < k) {
+          const int s = __ldg(slot_of + (size_t)t * k + j0 + jj);
+          wj[jj] = __ldg(w + (size_t)t * k + j0 + jj);
+          if ((unsigned)s < (unsigned)Tk) sj[jj] = s;
+          else if (lt == 0 && vb == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
+        }
       }
-      uint4 r[kMaxVecPerThread];
+      uint4 r[kJB][MV];
 #pragma unroll
-      for (int u = 0; u < kMaxVecPerThread; ++u) {
-        const int v = vb + lt + u * tpr;
-        if (v < nvec) r[u] = __ldg(yb + (size_t)s * nvec + v);
-      }
+      for (int jj = 0; jj < kJB; ++jj)
 #pragma unroll
-      for (int u = 0; u < kMaxVecPerThread; ++u) {
-        const int v = vb + lt + u * tpr;
-        if (v < nvec) {
-          float f[VN];
-          unpack(r[u], f, T());
+        for (int u = 0; u < MV; ++u) {
+          const int v = vb + lt + u * tpr;
+          if (sj[jj] >= 0 && v < nvec) r[jj][u] = __ldg(yb + (size_t)sj[jj] * nvec + v);
+        }
 #pragma unroll
-          for (int q = 0; q < VN; ++q) acc[u][q] = fmaf(wj, f[q], acc[u][q]);
+      for (int jj = 0; jj < kJB; ++jj) {
+        if (sj[jj] < 0) continue;
+#pragma unroll
+        for (int u = 0; u < MV; ++u) {
+          const int v = vb + lt + u * tpr;
+          if (v < nvec) {
+            float f[VN];
+            unpack(r[jj][u], f, T());
+#pragma unroll
+            for (int q = 0; q < VN; ++q) acc[u][q] = fmaf(wj[jj], f[q], acc[u][q]);
+          }
         }
       }
     }
 #pragma unroll
-    for (int u = 0; u < kMaxVecPerThread; ++u) {
+    for (int u = 0; u < MV; ++u) {
       const int v = vb + lt + u * tpr;
       if (v < nvec) dst[v] = pack(acc[u], T());
     }
@@ -121,16 +142,17 @@ __global__ void __launch_bounds__(kBlock) dispatch_bwd_kernel(
     const T* __restrict__ dxbuf, const int* __restrict__ slot_of, const float* __restrict__ dx_add,
     int T_, int k, int nvec, int tpr, int Tk, T* __restrict__ dx, int* status) {
   constexpr int VN = Vec<T>::N;
+  constexpr int MV = kGatherVec;
   const int rpb = kBlock / tpr;
   const int t = blockIdx.x * rpb + threadIdx.x / tpr;
   const int lt = threadIdx.x % tpr;
   if (t >= T_) return;
   const uint4* src = reinterpret_cast<const uint4*>(dxbuf);
   uint4* dst = reinterpret_cast<uint4*>(dx) + (size_t)t * nvec;
-  for (int vb = 0; vb < nvec; vb += tpr * kMaxVecPerThread) {
-    float acc[kMaxVecPerThread][VN];
+  for (int vb = 0; vb < nvec; vb += tpr * MV) {
+    float acc[MV][VN];
 #pragma unroll
-    for (int u = 0; u < kMaxVecPerThread; ++u) {
+    for (int u = 0; u < MV; ++u) {
       const int v = vb + lt + u * tpr;
 #pragma unroll
       for (int q = 0; q < VN; ++q) acc[u][q] = 0.f;
@@ -143,31 +165,42 @@ __global__ void __launch_bounds__(kBlock) dispatch_bwd_kernel(
         }
       }
     }
-    for (int j = 0; j < k; ++j) {
-      const int s = __ldg(slot_of + (size_t)t * k + j);
-      if ((unsigned)s >= (unsigned)Tk) {
-        if (lt == 0 && vb == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
-        continue;
+    for (int j0 = 0; j0 < k; j0 += kJB) {
+      int sj[kJB];
+#pragma unroll
+      for (int jj = 0; jj < kJB; ++jj) {
+        sj[jj] = -1;
+        if (j0 + jj < k) {
+          const int s = __ldg(slot_of + (size_t)t * k + j0 + jj);
+          if ((unsigned)s < (unsigned)Tk) sj[jj] = s;
+          else if (lt == 0 && vb == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
+        }
       }
-      uint4 r[kMaxVecPerThread];
+      uint4 r[kJB][MV];
 #pragma unroll
-      for (int u = 0; u < kMaxVecPerThread; ++u) {
-        const int v = vb + lt + u * tpr;
-        if (v < nvec) r[u] = __ldg(src + (size_t)s * nvec + v);
-      }
+      for (int jj = 0; jj < kJB; ++jj)
 #pragma unroll
-      for (int u = 0; u < kMaxVecPerThread; ++u) {
-        const int v = vb + lt + u * tpr;
-        if (v < nvec) {
-          float f[VN];
-          unpack(r[u], f, T());
+        for (int u = 0; u < MV; ++u) {
+          const int v = vb + lt + u * tpr;
+          if (sj[jj] >= 0 && v < nvec) r[jj][u] = __ldg(src + (size_t)sj[jj] * nvec + v);
+        }
 #pragma unroll
-          for (int q = 0; q < VN; ++q) acc[u][q] += f[q];
+      for (int jj = 0; jj < kJB; ++jj) {
+        if (sj[jj] < 0) continue;
+#pragma unroll
+        for (int u = 0; u < MV; ++u) {
+          const int v = vb + lt + u * tpr;
+          if (v < nvec) {
+            float f[VN];
+            unpack(r[jj][u], f, T());
+#pragma unroll
+            for (int q = 0; q < VN; ++q) acc[u][q] += f[q];
+          }
         }
       }
     }
 #pragma unroll
-    for (int u = 0; u < kMaxVecPerThread; ++u) {
+    for (int u = 0; u < MV; ++u) {
       const int v = vb + lt + u * tpr;
       if (v < nvec) dst[v] = pack(acc[u], T());
     }
@@ -175,7 +208,6 @@ __global__ void __launch_bounds__(kBlock) dispatch_bwd_kernel(
 }
 
 // ---------------------------------------------------------------------------- combine bwd
-// dybuf[slot_of[t*k+j],:] = w[t,j]*dy[t,:];  d_w[t,j] = <dy[t,:], ybuf[slot_of[t*k+j],:]>
 template <typename T, int KMAX>
 __global__ void __launch_bounds__(kBlock) combine_bwd_kernel(
     const T* __restrict__ dy, const T* __restrict__ ybuf, const int* __restrict__ slot_of,
@@ -263,7 +295,7 @@ template <typename T>
 void launch_combine_t(const void* ybuf, const int* slot_of, const float* w, int T_, int k, int h,
                       void* y, int* status, cudaStream_t st) {
   const int nvec = h / Vec<T>::N;
-  const RowGeom g = row_geom(nvec);
+  const RowGeom g = row_geom(nvec, kGatherVec);
   const int grid = (T_ + g.rows_per_block - 1) / g.rows_per_block;
   combine_kernel<T><<<grid, kBlock, 0, st>>>(static_cast<const T*>(ybuf), slot_of, w, T_, k,
                                              nvec, g.tpr, T_ * k, static_cast<T*>(y), status);
@@ -274,7 +306,7 @@ template <typename T>
 void launch_dispatch_bwd_t(const void* dxbuf, const int* slot_of, const float* dx_add, int T_,
                            int k, int h, void* dx, int* status, cudaStream_t st) {
   const int nvec = h / Vec<T>::N;
-  const RowGeom g = row_geom(nvec);
+  const RowGeom g = row_geom(nvec, kGatherVec);
   const int grid = (T_ + g.rows_per_block - 1) / g.rows_per_block;
   dispatch_bwd_kernel<T><<<grid, kBlock, 0, st>>>(static_cast<const T*>(dxbuf), slot_of, dx_add,
                                                   T_, k, nvec, g.tpr, T_ * k,
