@@ -269,11 +269,11 @@ def kernel_names(stage, n, w):
     tc = w.dtype == "bf16" and w.h % 128 == 0 and w.f % 128 == 0 and not simt_only
     tc_router = w.dtype == "bf16" and w.h % 64 == 0 and w.E % 16 == 0 and w.E >= 64 and not simt_only
     if tc_router:
-        route = (["router_split_w", "tc_router_fwd", "softmax_topk"] if n == 3 else
-                 ["router_split_w", "tc_router_fwd", "router_splitk_reduce", "softmax_topk"], CSRC + "router_tc.cu")
-        route_bwd = ((["route_dlogits", "router_split_dl", "tc_router_dwg", "router_split_w", "tc_router_dx"] if n == 5
-                      else ["route_dlogits", "router_split_dl", "tc_router_dwg", "router_dwg_splitk_reduce",
-                            "router_split_w", "tc_router_dx"]), CSRC + "router_tc.cu")
+        route = (["router_split_w", "tc_router_fwd", "softmax_topk"], CSRC + "router_tc.cu")
+        # route_dlogits also writes d_logits' bf16 planes; the top-k kernel finishes a K-split logits GEMM
+        route_bwd = ((["route_dlogits", "tc_router_dwg", "router_split_w", "tc_router_dx"] if n == 4
+                      else ["route_dlogits", "tc_router_dwg", "router_dwg_splitk_reduce", "router_split_w",
+                            "tc_router_dx"]), CSRC + "router_tc.cu")
     else:
         route = (["router_gemm", "softmax_topk"] if n == 2 else ["router_gemm", "router_splitk_reduce", "softmax_topk"],
                  CSRC + "gemm_simt.cu")
@@ -319,7 +319,7 @@ def kernel_counts(w, T, e_active, binding=None):
         "tc_DX": {"flops": 4 * Tk * h * f, "bytes": 2 * e_active * Wb + 2 * Tk * f * s + Tk * h * s},
         "tc_WGRAD13": {"flops": 4 * Tk * h * f, "bytes": Tk * h * s + 2 * Tk * f * s + 2 * E * Wb},
         "tc_WGRAD2": {"flops": 2 * Tk * h * f, "bytes": Tk * h * s + Tk * f * s + E * Wb},
-        "route_dlogits": {"flops": 0, "bytes": 2 * T * E * 4 + 12 * Tk},
+        "route_dlogits": {"flops": 0, "bytes": 2 * T * E * 4 + 12 * Tk},  # (+ 6 * T * E with the planes)
         # tensor-core router: exact three-plane bf16 splits of the fp32 operands, then the GEMMs
         "router_split_w": {"flops": 0, "bytes": h * E * 4 + 3 * h * E * 2},
         "router_split_dl": {"flops": 0, "bytes": T * E * 4 + 3 * T * E * 2},

@@ -180,6 +180,8 @@ int moe_route(const void* x, const float* Wg, const float* bias, int T, int h, i
           MOE_ERR_WORKSPACE, "moe_route: workspace too small");
   if (T == 0) return MOE_OK;
   REQUIRE_PTR(logits); REQUIRE_PTR(probs); REQUIRE_PTR(topk_idx); REQUIRE_PTR(topk_w);
+  const float* partial = nullptr;  // K-split partials the top-k kernel finishes (tensor-core router)
+  int slices = 1;
   if (!from_logits) {
     REQUIRE_PTR(x); REQUIRE_PTR(Wg);
     REQUIRE(h >= 8 && h % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_route: h must be a multiple of 8");
@@ -189,14 +191,15 @@ int moe_route(const void* x, const float* Wg, const float* bias, int T, int h, i
     char* scratch = static_cast<char*>(ws) + sizeof(WsHeader);
     if (tc_router_supported(dtype, h, E)) {
       REQUIRE(aligned16(x) && aligned16(logits), MOE_ERR_INVALID_ARG, "moe_route: x or logits not aligned");
-      if (tc_router_logits(x, Wg, bias, T, h, E, logits, scratch, status_of(ws), st) != 0)
+      if (tc_router_logits(x, Wg, bias, T, h, E, logits, scratch, &partial, &slices, status_of(ws), st) != 0)
         return tc_failure("moe_route");
     } else {
       simt_router_logits(dtype, x, Wg, bias, T, h, E, logits, reinterpret_cast<float*>(scratch), st);
     }
   }
-  launch_softmax_topk(logits, T, E, k, (flags & MOE_ROUTE_SIGMOID) != 0, (flags & MOE_ROUTE_RENORM) != 0, probs,
-                      topk_idx, topk_w, st);
+  launch_softmax_topk(logits, partial, slices, partial != nullptr ? bias : nullptr, T, E, k,
+                      (flags & MOE_ROUTE_SIGMOID) != 0, (flags & MOE_ROUTE_RENORM) != 0, probs, topk_idx, topk_w,
+                      st);
   return check_launch("moe_route");
 }
 
@@ -220,14 +223,17 @@ int moe_route_bwd(const void* x, const float* Wg, const float* probs, const int3
   REQUIRE_PTR(probs); REQUIRE_PTR(topk_idx); REQUIRE_PTR(d_topk_w); REQUIRE_PTR(d_logits);
   REQUIRE(dx_router == nullptr || aligned16(dx_router), MOE_ERR_INVALID_ARG,
           "moe_route_bwd: dx_router not aligned");
-  launch_route_dlogits(probs, topk_idx, d_topk_w, T, E, k, (flags & MOE_ROUTE_SIGMOID) != 0,
-                       (flags & MOE_ROUTE_RENORM) != 0, d_logits, status_of(ws), st);
   REQUIRE(aligned16(ws), MOE_ERR_WORKSPACE, "moe_route_bwd: workspace not 16-byte aligned");
   char* scratch = static_cast<char*>(ws) + sizeof(WsHeader);
-  if (tc_router_supported(dtype, h, E)) {
-    REQUIRE(aligned16(x) && aligned16(d_logits) && aligned16(dWg), MOE_ERR_INVALID_ARG,
-            "moe_route_bwd: x, d_logits or dWg not aligned");
-    if (tc_router_bwd(x, Wg, d_logits, T, h, E, dWg, dx_router, scratch, status_of(ws), st) != 0)
+  const bool tc = tc_router_supported(dtype, h, E);
+  REQUIRE(!tc || (aligned16(x) && aligned16(d_logits) && aligned16(dWg)), MOE_ERR_INVALID_ARG,
+          "moe_route_bwd: x, d_logits or dWg not aligned");
+  // the tensor-core router reads d_logits as three bf16 planes at the start of the scratch:
+  // the gate's backward writes them beside d_logits
+  launch_route_dlogits(probs, topk_idx, d_topk_w, T, E, k, (flags & MOE_ROUTE_SIGMOID) != 0,
+                       (flags & MOE_ROUTE_RENORM) != 0, d_logits, tc ? scratch : nullptr, status_of(ws), st);
+  if (tc) {
+    if (tc_router_bwd(x, Wg, d_logits, T, h, E, dWg, dx_router, scratch, true, status_of(ws), st) != 0)
       return tc_failure("moe_route_bwd");
   } else {
     simt_router_dwg(dtype, x, d_logits, T, h, E, dWg, reinterpret_cast<float*>(scratch), st);

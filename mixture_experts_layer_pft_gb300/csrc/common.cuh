@@ -23,6 +23,16 @@ __device__ __forceinline__ void flag_status(int* status, int bit) {
   if (status) atomicOr(status, bit);
 }
 
+// Exact split of an fp32 value into three bf16 planes, v = p0 + p1 + p2: p0 = bf16(v),
+// p1 = bf16(v - p0), p2 = bf16(v - p0 - p1).  Each difference is exact in fp32 and the last
+// plane holds the remaining at most 8 significant bits (normal values above 2^-100).
+__device__ __forceinline__ void split3_value(float v, __nv_bfloat16* p0, __nv_bfloat16* p1, __nv_bfloat16* p2) {
+  *p0 = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(*p0);
+  *p1 = __float2bfloat16_rn(r1);
+  *p2 = __float2bfloat16_rn(r1 - __bfloat162float(*p1));
+}
+
 // ---------------------------------------------------------------------------- element types
 
 template <typename T> struct Vec;  // 16-byte vector of T

@@ -24,11 +24,15 @@ void launch_combine_bwd(int dtype, const void* dy, const void* ybuf, const int* 
                         int* status, cudaStream_t st);
 
 // route.cu
-void launch_softmax_topk(const float* logits, int T, int E, int k, bool sigmoid, bool renorm, float* probs,
-                         int* topk_idx, float* topk_w, cudaStream_t st);
+// With `partial` (K-split router partials [slices][T][E]) the logits are summed there in slice
+// order, plus `bias`, and written to `logits`; otherwise `logits` is read.
+void launch_softmax_topk(float* logits, const float* partial, int slices, const float* bias, int T, int E,
+                         int k, bool sigmoid, bool renorm, float* probs, int* topk_idx, float* topk_w,
+                         cudaStream_t st);
+// With `dl_planes` ([3][T][E] bf16) the kernel also writes the exact three-plane split of d_logits.
 void launch_route_dlogits(const float* probs, const int* topk_idx, const float* d_topk_w, int T,
-                          int E, int k, bool sigmoid, bool renorm, float* d_logits, int* status,
-                          cudaStream_t st);
+                          int E, int k, bool sigmoid, bool renorm, float* d_logits, void* dl_planes,
+                          int* status, cudaStream_t st);
 
 // pft.cu
 int pft_num_chunks(long long Tk);
@@ -60,10 +64,13 @@ void simt_expert_ffn_bwd(int dtype, const void* dybuf, const void* xbuf, const v
 // h a multiple of 64, E of 16).  The scratch follows the workspace header, 256-byte aligned.
 bool tc_router_supported(int dtype, int h, int E);
 size_t tc_router_scratch(int op, int T, int h, int E);  // op 0: forward, 1: backward
+// The forward leaves several K slices' partials for launch_softmax_topk to add (*partial_out,
+// *slices_out; nullptr and 1 when the logits were written directly).  The backward splits
+// d_logits itself unless route_dlogits already wrote its planes at the start of `scratch`.
 int tc_router_logits(const void* x, const float* Wg, const float* bias, int T, int h, int E, float* logits,
-                     void* scratch, int* status, cudaStream_t st);
+                     void* scratch, const float** partial_out, int* slices_out, int* status, cudaStream_t st);
 int tc_router_bwd(const void* x, const float* Wg, const float* d_logits, int T, int h, int E, float* dWg,
-                  float* dx_router, void* scratch, int* status, cudaStream_t st);
+                  float* dx_router, void* scratch, bool dl_planes_ready, int* status, cudaStream_t st);
 
 // gemm_tc.cu -- tcgen05/TMEM/TMA grouped GEMMs (bf16; h and f multiples of 128)
 bool tc_supported(int dtype, int h, int f);

@@ -1,6 +1,8 @@
 // Gating: softmax over E experts and top-k selection, one warp per token; and the gate's
 // backward through the softmax Jacobian.  The router GEMMs (x·W_g, x^T·d_logits,
-// d_logits·W_g^T) run on the SIMT GEMM engine in fp32.
+// d_logits·W_g^T) run elsewhere (tensor-core or FP32 FMA engines); the top-k kernel can finish a
+// K-split logits GEMM (adding its partials in slice order), and the backward can emit the bf16
+// planes the tensor-core engine consumes.
 #include <float.h>
 #include <limits.h>
 
@@ -21,18 +23,28 @@ constexpr int kWarpsPerBlock = 8;
 // scores are divided by their sum.
 template <int PL>
 __global__ void __launch_bounds__(kWarpsPerBlock * kWarp) softmax_topk_kernel(
-    const float* __restrict__ logits, int T, int E, int k, bool sigmoid, bool renorm,
-    float* __restrict__ probs, int* __restrict__ topk_idx, float* __restrict__ topk_w) {
+    float* __restrict__ logits, const float* __restrict__ partial, int slices, const float* __restrict__ bias,
+    int T, int E, int k, bool sigmoid, bool renorm, float* __restrict__ probs, int* __restrict__ topk_idx,
+    float* __restrict__ topk_w) {
   const int lane = threadIdx.x % kWarp;
   const int t = blockIdx.x * kWarpsPerBlock + threadIdx.x / kWarp;
   if (t >= T) return;  // warp-uniform
-  const float* lt = logits + (size_t)t * E;
+  float* lt = logits + (size_t)t * E;
   float v[PL], p[PL];
   float m = -FLT_MAX;
 #pragma unroll
   for (int i = 0; i < PL; ++i) {
     const int e = lane + kWarp * i;
-    v[i] = e < E ? __ldg(lt + e) : -INFINITY;
+    if (e < E && partial != nullptr) {
+      // the logits GEMM left K slices: add them in slice order, then the bias
+      float s = 0.f;
+      for (int z = 0; z < slices; ++z) s += __ldg(partial + ((size_t)z * T + t) * E + e);
+      if (bias != nullptr) s += __ldg(bias + e);
+      lt[e] = s;
+      v[i] = s;
+    } else {
+      v[i] = e < E ? lt[e] : -INFINITY;
+    }
     m = fmaxf(m, v[i]);
   }
   float* pt = probs + (size_t)t * E;
@@ -102,7 +114,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * kWarp) softmax_topk_kernel(
 __global__ void __launch_bounds__(kWarpsPerBlock * kWarp) route_dlogits_kernel(
     const float* __restrict__ probs, const int* __restrict__ topk_idx,
     const float* __restrict__ d_w, int T, int E, int k, bool sigmoid, bool renorm,
-    float* __restrict__ d_logits, int* status) {
+    float* __restrict__ d_logits, __nv_bfloat16* __restrict__ dl_planes, int* status) {
   const int lane = threadIdx.x % kWarp;
   const int t = blockIdx.x * kWarpsPerBlock + threadIdx.x / kWarp;
   if (t >= T) return;
@@ -147,15 +159,26 @@ __global__ void __launch_bounds__(kWarpsPerBlock * kWarp) route_dlogits_kernel(
     const float pe = __ldg(pt + e);
     dl[e] = sigmoid ? pe * (1.f - pe) * g : pe * (g - s);
   }
+  if (dl_planes != nullptr) {  // the row is final: its three bf16 planes ([3][T][E])
+    __syncwarp();
+    const size_t n = (size_t)T * E;
+    for (int e = lane; e < E; e += kWarp) {
+      const size_t o = (size_t)t * E + e;
+      split3_value(dl[e], dl_planes + o, dl_planes + n + o, dl_planes + 2 * n + o);
+    }
+  }
 }
 
 }  // namespace
 
-void launch_softmax_topk(const float* logits, int T, int E, int k, bool sigmoid, bool renorm, float* probs,
-                         int* topk_idx, float* topk_w, cudaStream_t st) {
+void launch_softmax_topk(float* logits, const float* partial, int slices, const float* bias, int T, int E,
+                         int k, bool sigmoid, bool renorm, float* probs, int* topk_idx, float* topk_w,
+                         cudaStream_t st) {
   const int grid = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const int block = kWarpsPerBlock * kWarp;
-#define MOE_TOPK(PLV) softmax_topk_kernel<PLV><<<grid, block, 0, st>>>(logits, T, E, k, sigmoid, renorm, probs, topk_idx, topk_w)
+#define MOE_TOPK(PLV)                                                                                     \
+  softmax_topk_kernel<PLV><<<grid, block, 0, st>>>(logits, partial, slices, bias, T, E, k, sigmoid, renorm, \
+                                                   probs, topk_idx, topk_w)
   if (E <= 32) MOE_TOPK(1);
   else if (E <= 64) MOE_TOPK(2);
   else if (E <= 128) MOE_TOPK(4);
@@ -167,11 +190,11 @@ void launch_softmax_topk(const float* logits, int T, int E, int k, bool sigmoid,
 }
 
 void launch_route_dlogits(const float* probs, const int* topk_idx, const float* d_topk_w, int T,
-                          int E, int k, bool sigmoid, bool renorm, float* d_logits, int* status,
-                          cudaStream_t st) {
+                          int E, int k, bool sigmoid, bool renorm, float* d_logits, void* dl_planes,
+                          int* status, cudaStream_t st) {
   const int grid = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  route_dlogits_kernel<<<grid, kWarpsPerBlock * kWarp, 0, st>>>(probs, topk_idx, d_topk_w, T, E,
-                                                                 k, sigmoid, renorm, d_logits, status);
+  route_dlogits_kernel<<<grid, kWarpsPerBlock * kWarp, 0, st>>>(
+      probs, topk_idx, d_topk_w, T, E, k, sigmoid, renorm, d_logits, static_cast<__nv_bfloat16*>(dl_planes), status);
   count_launch(st);
 }
 

@@ -298,14 +298,7 @@ __global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ s
                                                      __nv_bfloat16* __restrict__ dst) {
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (long long)gridDim.x * blockDim.x) {
-    const float v = __ldg(src + i);
-    const __nv_bfloat16 p0 = __float2bfloat16_rn(v);
-    const float r1 = v - __bfloat162float(p0);
-    const __nv_bfloat16 p1 = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(p1);
-    dst[i] = p0;
-    dst[n + i] = p1;
-    dst[2 * n + i] = __float2bfloat16_rn(r2);
+    split3_value(__ldg(src + i), dst + i, dst + n + i, dst + 2 * n + i);
   }
 }
 
@@ -381,7 +374,7 @@ size_t tc_router_scratch(int op, int T, int h, int E) {
 }
 
 int tc_router_logits(const void* x, const float* Wg, const float* bias, int T, int h, int E, float* logits,
-                     void* scratch, int* status, cudaStream_t st) {
+                     void* scratch, const float** partial_out, int* slices_out, int* status, cudaStream_t st) {
   __nv_bfloat16* wp = static_cast<__nv_bfloat16*>(scratch);
   float* partial = reinterpret_cast<float*>(static_cast<char*>(scratch) + r256((size_t)3 * h * E * 2));
   launch_split3(Wg, (long long)h * E, wp, st);
@@ -395,16 +388,18 @@ int tc_router_logits(const void* x, const float* Wg, const float* bias, int T, i
   p.out = p.z > 1 ? partial : logits;
   p.bias = bias;
   if (rlaunch<FWD>(p, st)) return -1;
-  if (p.z > 1) launch_splitk_reduce(partial, p.z, (long long)T * E, E, bias, logits, st);
+  // several K slices: the caller adds the partials (with the bias) where it reads the logits
+  *partial_out = p.z > 1 ? partial : nullptr;
+  *slices_out = p.z;
   return 0;
 }
 
 int tc_router_bwd(const void* x, const float* Wg, const float* d_logits, int T, int h, int E, float* dWg,
-                  float* dx_router, void* scratch, int* status, cudaStream_t st) {
+                  float* dx_router, void* scratch, bool dl_planes_ready, int* status, cudaStream_t st) {
   __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(scratch);
   __nv_bfloat16* wp = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(scratch) + r256((size_t)3 * T * E * 2));
   float* partial = reinterpret_cast<float*>(reinterpret_cast<char*>(wp) + r256((size_t)3 * h * E * 2));
-  launch_split3(d_logits, (long long)T * E, dp, st);
+  if (!dl_planes_ready) launch_split3(d_logits, (long long)T * E, dp, st);
   // dWg = x^T dL: M = h, N = E, K = T
   RouterParams g = rblank(status);
   bool ok = tc_make_map(&g.mapA[0], x, T, h, 64, 64);
