@@ -19,9 +19,10 @@
 // Warp roles (one CTA per SM): warp 0 issues TMA loads into a ring of shared-memory stages;
 // warp 1 owns the TMEM allocation and one lane issues tcgen05.mma into fp32 accumulators in
 // TMEM; the epilogue warps (4, or 8 = two per TMEM lane quarter splitting the columns) drain
-// TMEM (tcgen05.ld), apply the epilogue (SwiGLU, its
-// derivative, or a plain store), transpose each 32 x 16 block through shared memory and write
-// bf16 results with 16-byte stores, four lanes per 64-byte column segment.  Stages
+// TMEM (tcgen05.ld), apply the epilogue (SwiGLU, its derivative, or a plain store) and
+// transpose each block through shared memory: token-N outputs go out in 32 x 16 blocks with
+// 16-byte stores, four lanes per 64-byte column segment; weight gradients in 32 x 32 blocks as
+// TMA tensor stores (wider blocks halve the per-block latency that bounds that epilogue).  Stages
 // and accumulators hand over through mbarriers.  Every wait is bounded (about two seconds of
 // %globaltimer): on expiry the kernel sets MOE_STATUS_TIMEOUT, every role unwinds, and the
 // TMEM is released before the CTA exits.  No cluster, no multicast.
@@ -85,7 +86,10 @@ template <int MODE> struct Cfg {
   // GEMM, whose three outputs per element need more transpose buffer than shared memory has left
   static constexpr int EPI_WARPS = (MODE == GATEUP) ? 4 : 8;  // GATEUP_WIDE: 3 stages leave room for 8
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-  static constexpr int NSLOT = GU ? 3 : (BASE == DA || BASE == WGRAD13) ? 2 : 1;
+  // epilogue chunk: columns per TMEM load and per tensor store.  Weight gradients drain 32 at a
+  // time, one output after the other through a single transpose slot per warp.
+  static constexpr int CW = TOKEN_N ? 16 : 32;
+  static constexpr int NSLOT = GU ? 3 : (BASE == DA) ? 2 : 1;
   static_assert(ACC_BUFS >= 1 && STAGES >= 2, "tile configuration");
 };
 
@@ -195,7 +199,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
   __shared__ int s_pref[kMaxE + 1];
   __shared__ Sched s_sched;
   // epilogue transpose buffers: one 16-column x 32-row bf16 block per warp and output slot
-  __shared__ __align__(128) __nv_bfloat16 s_stage[C::EPI_WARPS][C::NSLOT][16][32];
+  __shared__ __align__(128) __nv_bfloat16 s_stage[C::EPI_WARPS][C::NSLOT][C::CW][32];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // stage ring aligned to 1024 bytes (the swizzle atom)
@@ -400,7 +404,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
     const int q = warp & 3;              // TMEM lane quarter this warp may access
     const int cg = (warp - 2) >> 2;      // column group: chunks cg, cg + G, cg + 2G, ...
     constexpr int G = C::EPI_WARPS / 4;  // warps per lane quarter
-    __nv_bfloat16 (*stg)[16][32] = s_stage[warp - 2];  // this warp's transpose buffers
+    __nv_bfloat16 (*stg)[C::CW][32] = s_stage[warp - 2];  // this warp's transpose buffers
     int it = 0;
     for (int u = blockIdx.x; u < sc.total; u += gridDim.x, ++it) {
       const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
@@ -417,7 +421,33 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       for (int mtl = 0; mtl < (C::PAIR ? 2 : 1); ++mtl) {
       const uint32_t t0 = t0u + (uint32_t)(mtl * C::BN);
       const int mbase = w.m0 + mtl * BM + q * 32;
-      for (int c0 = 16 * cg; c0 < w.ncols; c0 += 16 * G) {
+      for (int c0 = C::CW * cg; c0 < w.ncols; c0 += C::CW * G) {
+        if constexpr (!C::TOKEN_N) {
+          // weight gradients: 32 columns per TMEM load and per 32 x 32 tensor store, one output
+          // (dW1 then dW3, or dW2) after the other
+#pragma unroll
+          for (int a = 0; a < (C::BASE == WGRAD13 ? 2 : 1); ++a) {
+            float vv[32];
+            if (!zero) {
+              tmem_ld32(t0 + a * C::BN + c0, vv);
+              tmem_wait_ld();
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) vv[i] = 0.f;
+            }
+            if (lane == 0) bulk_wait_read<0>();  // the previous store has read the slot
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) stg[0][i][lane] = __float2bfloat16_rn(vv[i]);
+            __syncwarp();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(a == 0 ? &p.mapO0 : &p.mapO1, smem_u32(&stg[0][0][0]), mbase, w.e * p.a_rows + w.n0 + c0);
+              bulk_commit();
+            }
+          }
+        } else {
         // (1) DA: start the coalesced 16-byte loads of h1, h3 for these 16 columns
         uint4 in_a[2], in_b[2];
         if (C::BASE == DA) {
@@ -437,7 +467,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
         float v0[16], v1[16];
         if (!zero) {
           tmem_ld16(t0 + c0, v0);
-          if (C::GU || C::BASE == WGRAD13) tmem_ld16(t0 + C::BN + c0, v1);
+          if (C::GU) tmem_ld16(t0 + C::BN + c0, v1);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -461,10 +491,6 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           __syncwarp();  // the outputs below reuse these two slots
         }
         // (4) the epilogue math, written to shared memory as [column][m]
-        if (!C::TOKEN_N) {  // wgrad: the previous chunk's TMA store must have read the slots
-          if (lane == 0) bulk_wait_read<0>();
-          __syncwarp();
-        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if (C::GU) {
@@ -479,22 +505,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
             stg[1][i][lane] = __float2bfloat16_rn(da * z1[i] * sg);
           } else {
             stg[0][i][lane] = __float2bfloat16_rn(v0[i]);
-            if (C::BASE == WGRAD13) stg[1][i][lane] = __float2bfloat16_rn(v1[i]);
           }
         }
         __syncwarp();
-        if (!C::TOKEN_N) {
-          // wgrad: full 16-column chunks go out as one asynchronous 32 x 16 tensor store per output
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) {
-            const int y = w.e * p.a_rows + w.n0 + c0;  // row of the [E * rows, cols] view
-            tma_store_2d(&p.mapO0, smem_u32(&stg[0][0][0]), mbase, y);
-            if (C::BASE == WGRAD13) tma_store_2d(&p.mapO1, smem_u32(&stg[1][0][0]), mbase, y);
-            bulk_commit();
-          }
-          continue;
-        }
         // (5) 16-byte stores: four lanes cover one column's 32 rows (64 contiguous bytes)
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
@@ -510,12 +523,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
               *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
             } else {
               *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(&stg[0][ci][part * 8]);
-              if (C::BASE == WGRAD13)
-                *reinterpret_cast<uint4*>(p.out1 + o) = *reinterpret_cast<const uint4*>(&stg[1][ci][part * 8]);
             }
           }
         }
         __syncwarp();
+        }  // token-N
       }
       }
       tc_fence_before();
@@ -645,8 +657,8 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
   ok = tc_make_map(&w13.mapA0, dh1, Tk, f, 64, 64) && tc_make_map(&w13.mapA1, dh3, Tk, f, 64, 64) &&
        tc_make_map(&w13.mapB0, xbuf, Tk, h, 64, 64);
   if (!ok) return -1;
-  ok = tc_make_map(&w13.mapO0, dW1, (long long)E * h, f, 32, 16, false) &&
-       tc_make_map(&w13.mapO1, dW3, (long long)E * h, f, 32, 16, false);
+  ok = tc_make_map(&w13.mapO0, dW1, (long long)E * h, f, 32, Cfg<WGRAD13>::CW, false) &&
+       tc_make_map(&w13.mapO1, dW3, (long long)E * h, f, 32, Cfg<WGRAD13>::CW, false);
   if (!ok) return -1;
   w13.offsets = offsets; w13.E = E; w13.M = f; w13.Nw = h; w13.a_rows = h;
   w13.out0 = static_cast<__nv_bfloat16*>(dW1); w13.out1 = static_cast<__nv_bfloat16*>(dW3);
@@ -657,7 +669,7 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
   TcParams w2 = blank_params();
   ok = tc_make_map(&w2.mapA0, dybuf, Tk, h, 64, 64) && tc_make_map(&w2.mapB0, a, Tk, f, 64, 64);
   if (!ok) return -1;
-  ok = tc_make_map(&w2.mapO0, dW2, (long long)E * f, h, 32, 16, false);
+  ok = tc_make_map(&w2.mapO0, dW2, (long long)E * f, h, 32, Cfg<WGRAD2>::CW, false);
   if (!ok) return -1;
   w2.offsets = offsets; w2.E = E; w2.M = h; w2.Nw = f; w2.a_rows = f;
   w2.out0 = static_cast<__nv_bfloat16*>(dW2); w2.ld_out = h; w2.out_expert_stride = (long long)f * h;
