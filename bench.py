@@ -285,7 +285,8 @@ def kernel_names(stage, n, w):
         "pft_build": (["pft_hist", "pft_scatter"], CSRC + "pft.cu"),
         "dispatch": (["dispatch"], CSRC + "gather.cu"),
         "expert_ffn": ((["tc_GATEUP", "tc_DOWN"], CSRC + "gemm_tc.cu") if tc
-                       else (["simt_gateup", "simt_down"], CSRC + "gemm_simt.cu")),
+                       else ((["simt_gateup", "simt_down"] if n == 2 else ["simt_h1", "simt_h3_swiglu", "simt_down"]),
+                             CSRC + "gemm_simt.cu")),
         "combine": (["combine"], CSRC + "gather.cu"),
         "combine_bwd": (["combine_bwd"], CSRC + "gather.cu"),
         "expert_ffn_bwd": ((["tc_DA", "tc_DX", "tc_WGRAD13", "tc_WGRAD2"], CSRC + "gemm_tc.cu") if tc
@@ -331,6 +332,8 @@ def kernel_counts(w, T, e_active, binding=None):
         "router_dx": {"flops": 2 * T * h * E, "bytes": T * E * 4 + h * E * 4 + T * h * 4},
         "dispatch_bwd": {"flops": 0, "bytes": Tk * h * s + T * h * s + T * h * 4 + 4 * Tk},
     }
+    d["simt_h1"] = {"flops": 2 * Tk * h * f, "bytes": e_active * Wb + Tk * h * s + Tk * f * s}
+    d["simt_h3_swiglu"] = {"flops": 2 * Tk * h * f, "bytes": e_active * Wb + Tk * h * s + 3 * Tk * f * s}
     for a, bname in (("simt_gateup", "tc_GATEUP"), ("simt_down", "tc_DOWN"), ("simt_dA", "tc_DA"),
                      ("simt_dX", "tc_DX"), ("simt_dW13", "tc_WGRAD13"), ("simt_dW2", "tc_WGRAD2")):
         d[a] = d[bname]
