@@ -386,6 +386,38 @@ def test_tensor_core_engine_matches_simt_engine(B, monkeypatch, T, h, E, k, f, s
         assert rel_l2(np64(outs["tc"][n]), np64(outs["simt"][n])) <= TOL["bf16"], n
 
 
+@pytest.mark.parametrize("h,f", [(256, 384), (384, 256)])
+def test_expert_forward_at_segment_length_edges(B, h, f):
+    """Gate/up (256-token chunks, more than 96 rows per expert on average) and DOWN (two M tiles
+    per unit when h % 256 == 0) over expert segments of 0..513 rows, built directly as PFT
+    offsets; every expert's rows of h1, h3, a and y against the oracle on their own."""
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    dt = torch.bfloat16
+    lens = np.array([0, 1, 15, 16, 17, 63, 64, 65, 255, 256, 257, 513], dtype=np.int64)
+    E = len(lens)
+    offsets = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    Tk = int(offsets[-1])
+    x = random_tensor((Tk, h), 61, dt, "cuda")
+    W1 = random_tensor((E, h, f), 62, dt, "cuda", std=h ** -0.5)
+    W3 = random_tensor((E, h, f), 63, dt, "cuda", std=h ** -0.5)
+    W2 = random_tensor((E, f, h), 64, dt, "cuda", std=f ** -0.5)
+    z = lambda *s: torch.full(s, float("nan"), dtype=dt, device="cuda")  # noqa: E731
+    ybuf, h1, h3, a = z(Tk, h), z(Tk, f), z(Tk, f), z(Tk, f)
+    ws = B.new_workspace(B.MOE_OP_ALL, Tk, h, E, 1, f, dt)
+    B.moe_expert_ffn(x, torch.from_numpy(offsets).cuda(), W1, W3, W2, ybuf, h1, h3, a, ws)
+    torch.cuda.synchronize()
+    want = O.expert_ffn(np64(x), offsets, np64(W1), np64(W3), np64(W2), "bf16")
+    for n, got in (("ybuf", ybuf), ("h1", h1), ("h3", h3), ("a", a)):
+        g = np64(got)
+        assert np.isfinite(g).all(), n
+        for e in range(E):
+            sl = slice(offsets[e], offsets[e + 1])
+            if lens[e]:
+                assert rel_l2(g[sl], want[n][sl]) <= TOL["bf16"], (n, e, lens[e])
+    assert B.moe_check_status(ws) == 0
+
+
 def test_weight_gradients_at_segment_length_edges(B):
     """Expert segments whose lengths straddle the 16-row MMA slice, the 64-row K step and the
     256-row resident chunk of the weight-gradient GEMMs (0, 1, 15, 16, 17, 63, 64, 65, 255, 256,
