@@ -111,7 +111,8 @@ def test_route_bwd(B, dt, T, h, E, k):
     assert B.moe_check_status(ws) == 0
 
 
-@pytest.mark.parametrize("T,h,E", [(300, 7168, 256), (4096, 2048, 64), (1000, 5120, 128), (257, 2048, 80)])
+@pytest.mark.parametrize("T,h,E", [(300, 7168, 256), (4096, 2048, 64), (1000, 5120, 128), (257, 2048, 80),
+                                   (100, 256, 1024)])
 def test_router_gemms_at_full_widths(B, T, h, E):
     """bf16 activations with an fp32 router at the pages' widths (long sums over h = 7168 and
     T = 4096): logits, dWg and dx stay within the fp32 tolerance of the exact sums."""
