@@ -87,9 +87,12 @@ template <int MODE> struct Cfg {
   static constexpr int EPI_WARPS = (MODE == GATEUP) ? 4 : 8;  // GATEUP_WIDE: 3 stages leave room for 8
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   // epilogue chunk: columns per TMEM load and per tensor store.  Weight gradients drain 32 at a
-  // time, one output after the other through a single transpose slot per warp.
+  // time and alternate between two transpose slots per warp, so two tensor stores are in flight.
   static constexpr int CW = TOKEN_N ? 16 : 32;
-  static constexpr int NSLOT = GU ? 3 : (BASE == DA) ? 2 : 1;
+  static constexpr int NSLOT = (GU || !TOKEN_N) ? (GU ? 3 : 2) : (BASE == DA) ? 2 : 1;
+  // per-expert tables in shared memory: token-N modes search the unit prefix sums; weight
+  // gradients have the same unit count per expert and read the two offsets they need directly
+  static constexpr int TABLE = TOKEN_N ? kMaxE + 1 : 1;
   static_assert(ACC_BUFS >= 1 && STAGES >= 2, "tile configuration");
 };
 
@@ -98,7 +101,7 @@ struct TcParams {
   CUtensorMap mapA1;  // GATEUP W3 | DX W3 | WGRAD13 dh3
   CUtensorMap mapB0;  // GATEUP xbuf | DOWN a | DA dybuf | DX dh1 | WGRAD13 xbuf | WGRAD2 a
   CUtensorMap mapB1;  // DX dh3
-  CUtensorMap mapO0;  // wgrad: dW1 | dW2 viewed [E * rows, cols], 32 x 16 boxes (TMA stores)
+  CUtensorMap mapO0;  // wgrad: dW1 | dW2 viewed [E * rows, cols], 32 x 32 boxes (TMA stores)
   CUtensorMap mapO1;  // WGRAD13: dW3
   const int* offsets;
   int E;
@@ -173,8 +176,8 @@ __device__ __forceinline__ Unit decode(int u, const Sched& sc, const int* s_pref
     const int r = u % per;
     w.m0 = (r / sc.nt) * BM;
     w.n0 = (r % sc.nt) * C::BN;
-    w.row0 = s_off[w.e];
-    w.rows = s_off[w.e + 1] - s_off[w.e];
+    w.row0 = __ldg(p.offsets + w.e);
+    w.rows = __ldg(p.offsets + w.e + 1) - w.row0;
     w.ncols = min(C::BN, p.Nw - w.n0);
     w.nmma = w.ncols;
     w.nk = (w.rows + BK - 1) / BK;
@@ -195,8 +198,8 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  __shared__ int s_off[kMaxE + 1];
-  __shared__ int s_pref[kMaxE + 1];
+  __shared__ int s_off[C::TABLE];
+  __shared__ int s_pref[C::TABLE];
   __shared__ Sched s_sched;
   // epilogue transpose buffers: one 16-column x 32-row bf16 block per warp and output slot
   __shared__ __align__(128) __nv_bfloat16 s_stage[C::EPI_WARPS][C::NSLOT][C::CW][32];
@@ -207,38 +210,44 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
   uint8_t* ring_ptr = dsmem + (ring - smem_u32(dsmem));
 
   // ------------------------------------------------------------------ schedule
-  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = __ldg(p.offsets + i);
-  __syncthreads();
-  if (warp == 0) {
-    // units per expert, then an inclusive scan into s_pref[1..E] (s_pref[0] = 0)
-    const int per = (p.E + 31) / 32;
-    const int b0 = min(lane * per, p.E), b1 = min(b0 + per, p.E);
-    const int mt = p.M / C::MT;
-    int local = 0;
-    for (int e = b0; e < b1; ++e) {
-      int ue;
-      if (C::TOKEN_N) ue = ((s_off[e + 1] - s_off[e] + C::BN - 1) / C::BN) * mt;
-      else ue = mt * ((p.Nw + C::BN - 1) / C::BN);
-      s_pref[e + 1] = ue;
-      local += ue;
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int run = incl - local;
-    for (int e = b0; e < b1; ++e) {
-      const int ue = s_pref[e + 1];
-      s_pref[e] = run;
-      run += ue;
-    }
-    if (lane == 31) {
-      s_pref[p.E] = incl;
-      s_sched.total = incl;
-      s_sched.mt = mt;
+  if constexpr (!C::TOKEN_N) {
+    if (threadIdx.x == 0) {
+      s_sched.mt = p.M / C::MT;
       s_sched.nt = (p.Nw + C::BN - 1) / C::BN;
+      s_sched.total = p.E * s_sched.mt * s_sched.nt;
+    }
+  } else {
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = __ldg(p.offsets + i);
+    __syncthreads();
+    if (warp == 0) {
+      // units per expert, then an inclusive scan into s_pref[1..E] (s_pref[0] = 0)
+      const int per = (p.E + 31) / 32;
+      const int b0 = min(lane * per, p.E), b1 = min(b0 + per, p.E);
+      const int mt = p.M / C::MT;
+      int local = 0;
+      for (int e = b0; e < b1; ++e) {
+        const int ue = ((s_off[e + 1] - s_off[e] + C::BN - 1) / C::BN) * mt;
+        s_pref[e + 1] = ue;
+        local += ue;
+      }
+      int incl = local;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      int run = incl - local;
+      for (int e = b0; e < b1; ++e) {
+        const int ue = s_pref[e + 1];
+        s_pref[e] = run;
+        run += ue;
+      }
+      if (lane == 31) {
+        s_pref[p.E] = incl;
+        s_sched.total = incl;
+        s_sched.mt = mt;
+        s_sched.nt = 0;
+      }
     }
   }
   __syncthreads();
@@ -405,6 +414,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
     const int cg = (warp - 2) >> 2;      // column group: chunks cg, cg + G, cg + 2G, ...
     constexpr int G = C::EPI_WARPS / 4;  // warps per lane quarter
     __nv_bfloat16 (*stg)[C::CW][32] = s_stage[warp - 2];  // this warp's transpose buffers
+    int slot = 0;  // weight gradients: the transpose slot of the next tensor store
     int it = 0;
     for (int u = blockIdx.x; u < sc.total; u += gridDim.x, ++it) {
       const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
@@ -417,37 +427,119 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       // output element (m, c) lives at [colbase + c][mbase + lane] (+ the expert's base for wgrad)
       const size_t colbase = C::TOKEN_N ? (size_t)w.row0 : (size_t)w.n0;
       const size_t ebase = C::TOKEN_N ? 0 : (size_t)w.e * (size_t)p.out_expert_stride;
-      // a paired unit's two M tiles go out one after the other (accumulators at t0 and t0 + BN)
-      for (int mtl = 0; mtl < (C::PAIR ? 2 : 1); ++mtl) {
-      const uint32_t t0 = t0u + (uint32_t)(mtl * C::BN);
-      const int mbase = w.m0 + mtl * BM + q * 32;
-      for (int c0 = C::CW * cg; c0 < w.ncols; c0 += C::CW * G) {
-        if constexpr (!C::TOKEN_N) {
-          // weight gradients: 32 columns per TMEM load and per 32 x 32 tensor store, one output
-          // (dW1 then dW3, or dW2) after the other
+      if constexpr (!C::TOKEN_N) {
+        // weight gradients: the warp's whole share of the accumulators (dW1 then dW3, or dW2;
+        // 32 columns per TMEM load) goes to registers as bf16 pairs, TMEM goes back to the MMA
+        // warp, and the 32 x 32 tensor stores overlap the next unit's main loop
+        constexpr int NOUT = (C::BASE == WGRAD13) ? 2 : 1;
+        constexpr int NCH = C::BN / (C::CW * G);  // 32-column chunks per warp
+        const int mbase = w.m0 + q * 32;
+        uint32_t pk[NOUT][NCH][16];
 #pragma unroll
-          for (int a = 0; a < (C::BASE == WGRAD13 ? 2 : 1); ++a) {
+        for (int j = 0; j < NCH; ++j) {
+          const int c0 = C::CW * (cg + G * j);
+#pragma unroll
+          for (int a = 0; a < NOUT; ++a) {
             float vv[32];
-            if (!zero) {
-              tmem_ld32(t0 + a * C::BN + c0, vv);
+            if (!zero && c0 < w.ncols) {
+              tmem_ld32(t0u + a * C::BN + c0, vv);
               tmem_wait_ld();
             } else {
 #pragma unroll
               for (int i = 0; i < 32; ++i) vv[i] = 0.f;
             }
-            if (lane == 0) bulk_wait_read<0>();  // the previous store has read the slot
+#pragma unroll
+            for (int i = 0; i < 16; ++i) pk[a][j][i] = pack_bf16x2(vv[2 * i], vv[2 * i + 1]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[b]);
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          const int c0 = C::CW * (cg + G * j);
+          if (c0 >= w.ncols) break;
+#pragma unroll
+          for (int a = 0; a < NOUT; ++a) {
+            // the two slots alternate store by store; the store two back has read this one
+            unsigned short* sw = reinterpret_cast<unsigned short*>(&stg[slot][0][0]);
+            slot ^= 1;
+            if (lane == 0) bulk_wait_read<1>();
             __syncwarp();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) stg[0][i][lane] = __float2bfloat16_rn(vv[i]);
+            for (int i = 0; i < 16; ++i) {
+              sw[(2 * i) * 32 + lane] = (unsigned short)(pk[a][j][i] & 0xFFFFu);
+              sw[(2 * i + 1) * 32 + lane] = (unsigned short)(pk[a][j][i] >> 16);
+            }
             __syncwarp();
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(a == 0 ? &p.mapO0 : &p.mapO1, smem_u32(&stg[0][0][0]), mbase, w.e * p.a_rows + w.n0 + c0);
+              tma_store_2d(a == 0 ? &p.mapO0 : &p.mapO1, smem_u32(sw), mbase, w.e * p.a_rows + w.n0 + c0);
               bulk_commit();
             }
           }
-        } else {
+        }
+      } else if constexpr (C::PAIR && C::BASE != DA) {
+        // down projection and dX with paired M tiles write the accumulators themselves: both
+        // tiles' columns (16 per TMEM load) go to registers as bf16 pairs, TMEM goes back to the
+        // MMA warp, and the 16-byte stores of the token rows overlap the next unit's main loop
+        constexpr int NCH = C::BN / (C::CW * G);  // 16-column chunks per warp and tile
+        uint32_t pk[2][NCH][8];
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          const int c0 = C::CW * (cg + G * j);
+          float v0[16], v1[16];
+          if (!zero && c0 < w.ncols) {
+            tmem_ld16(t0u + c0, v0);
+            tmem_ld16(t0u + C::BN + c0, v1);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) { v0[i] = 0.f; v1[i] = 0.f; }
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            pk[0][j][i] = pack_bf16x2(v0[2 * i], v0[2 * i + 1]);
+            pk[1][j][i] = pack_bf16x2(v1[2 * i], v1[2 * i + 1]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty_bar[b]);
+        unsigned short* sw = reinterpret_cast<unsigned short*>(&stg[0][0][0]);
+#pragma unroll
+        for (int mtl = 0; mtl < 2; ++mtl) {
+          const int mbase = w.m0 + mtl * BM + q * 32;
+#pragma unroll
+          for (int j = 0; j < NCH; ++j) {
+            const int c0 = C::CW * (cg + G * j);
+            if (c0 >= w.ncols) break;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              sw[(2 * i) * 32 + lane] = (unsigned short)(pk[mtl][j][i] & 0xFFFFu);
+              sw[(2 * i + 1) * 32 + lane] = (unsigned short)(pk[mtl][j][i] >> 16);
+            }
+            __syncwarp();
+            // four lanes cover one token row's 32 outputs (64 contiguous bytes)
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int v = lane + 32 * r, ci = v >> 2, part = v & 3;
+              if (c0 + ci < w.ncols) {
+                const size_t o = (colbase + c0 + ci) * (size_t)p.ld_out + mbase + part * 8;
+                *reinterpret_cast<uint4*>(p.out0 + o) = *reinterpret_cast<const uint4*>(sw + ci * 32 + part * 8);
+              }
+            }
+            __syncwarp();
+          }
+        }
+      } else {
+      // a paired unit's two M tiles go out one after the other (accumulators at t0 and t0 + BN)
+      for (int mtl = 0; mtl < (C::PAIR ? 2 : 1); ++mtl) {
+      const uint32_t t0 = t0u + (uint32_t)(mtl * C::BN);
+      const int mbase = w.m0 + mtl * BM + q * 32;
+      for (int c0 = C::CW * cg; c0 < w.ncols; c0 += C::CW * G) {
+        {
         // (1) DA: start the coalesced 16-byte loads of h1, h3 for these 16 columns
         uint4 in_a[2], in_b[2];
         if (C::BASE == DA) {
@@ -527,12 +619,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           }
         }
         __syncwarp();
-        }  // token-N
+        }
       }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[b]);
+      }  // token-N
     }
   }
 
