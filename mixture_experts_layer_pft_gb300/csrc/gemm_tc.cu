@@ -134,15 +134,21 @@ struct Unit {
   int ncols;    // columns of D to produce (token-N: rows; wgrad: N tile width)
   int nmma;     // MMA N (multiple of 16)
   int nk;       // K steps of BK
+  int na;       // accumulators (A tiles) in use: NUM_A, or 1 for a paired mode's split unit
 };
 
 // Token-N modes: expert e has nc_e = ceil(n_e / BN) chunks of about equal size (a multiple of
 // 16 rows, the last one shorter); its units are (m-tile, chunk) pairs, chunks innermost, so
 // the CTAs that stream one weight tile for different chunks run side by side.
+//
+// Paired modes balance the last wave: when the paired units leave a last wave at most half
+// full, each of its units is split into its two 128-row M tiles, which go after all full
+// pairs, so no CTA runs more than half a pair beyond the others.
 struct Sched {
   int total;
-  int mt;  // M tiles per expert
-  int nt;  // wgrad: N tiles
+  int mt;     // M tiles per expert
+  int nt;     // wgrad: N tiles
+  int pairs;  // paired modes: units that keep both M tiles (the rest are split)
 };
 
 template <int MODE>
@@ -150,6 +156,14 @@ __device__ __forceinline__ Unit decode(int u, const Sched& sc, const int* s_pref
                                        const TcParams& p) {
   using C = Cfg<MODE>;
   Unit w;
+  w.na = C::NUM_A;
+  int half = 0;  // paired modes: which M tile a split unit keeps
+  if (C::PAIR && u >= sc.pairs) {
+    const int v = u - sc.pairs;
+    u = sc.pairs + (v >> 1);
+    half = v & 1;
+    w.na = 1;
+  }
   if (C::TOKEN_N) {
     int lo = 0, hi = p.E - 1;  // largest e with s_pref[e] <= u
     while (lo < hi) {
@@ -163,7 +177,7 @@ __device__ __forceinline__ Unit decode(int u, const Sched& sc, const int* s_pref
     const int local = u - s_pref[e];
     const int mtile = local / nc, c = local % nc;
     w.e = e;
-    w.m0 = mtile * C::MT;
+    w.m0 = mtile * C::MT + half * BM;
     w.row0 = s_off[e] + c * cs;
     w.rows = min(cs, n - c * cs);
     w.n0 = 0;
@@ -215,6 +229,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       s_sched.mt = p.M / C::MT;
       s_sched.nt = (p.Nw + C::BN - 1) / C::BN;
       s_sched.total = p.E * s_sched.mt * s_sched.nt;
+      s_sched.pairs = s_sched.total;
     }
   } else {
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) s_off[i] = __ldg(p.offsets + i);
@@ -244,7 +259,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       }
       if (lane == 31) {
         s_pref[p.E] = incl;
-        s_sched.total = incl;
+        const int rem = incl % (int)gridDim.x;
+        const int pairs = (C::PAIR && rem > 0 && 2 * rem <= (int)gridDim.x) ? incl - rem : incl;
+        s_sched.pairs = pairs;
+        s_sched.total = pairs + 2 * (incl - pairs);
         s_sched.mt = mt;
         s_sched.nt = 0;
       }
@@ -283,7 +301,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       for (int u = blockIdx.x; u < sc.total && ok; u += gridDim.x) {
         const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
         const int nbB = C::TOKEN_N ? (w.nmma + 63) / 64 : C::BN / 64;
-        const uint32_t tx = C::A_BYTES + (uint32_t)nbB * kBox;
+        const uint32_t tx = (uint32_t)w.na * kATile + (uint32_t)nbB * kBox;
         for (int ks = 0; ks < w.nk; ++ks) {
           if (!mbar_wait(&empty_bar[s], ph ^ 1u, &s_abort, p.status)) { ok = false; break; }
           mbar_expect_tx(&full_bar[s], tx);
@@ -297,19 +315,19 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
             if (C::GU) {
               tma_load_2d(a_sm + kATile, &p.mapA1, &full_bar[s], w.m0, y);
               tma_load_2d(a_sm + kATile + kBox, &p.mapA1, &full_bar[s], w.m0 + 64, y);
-            } else if (C::PAIR) {
+            } else if (C::PAIR && w.na == 2) {
               tma_load_2d(a_sm + kATile, &p.mapA0, &full_bar[s], w.m0 + 128, y);
               tma_load_2d(a_sm + kATile + kBox, &p.mapA0, &full_bar[s], w.m0 + 192, y);
             }
             for (int j = 0; j < nbB; ++j) tma_load_2d(b_sm + j * kBox, &p.mapB0, &full_bar[s], k0, w.row0 + 64 * j);
           } else if (C::BASE == DA) {
-            for (int a = 0; a < C::NUM_A; ++a)
+            for (int a = 0; a < w.na; ++a)
               tma_load_2d(a_sm + a * kATile, &p.mapA0, &full_bar[s], k0, w.e * p.a_rows + w.m0 + a * BM);
             for (int j = 0; j < nbB; ++j) tma_load_2d(b_sm + j * kBox, &p.mapB0, &full_bar[s], k0, w.row0 + 64 * j);
           } else if (C::BASE == DX) {
             const bool second = k0 >= p.K;
             const int kk = second ? k0 - p.K : k0;
-            for (int a = 0; a < C::NUM_A; ++a)
+            for (int a = 0; a < w.na; ++a)
               tma_load_2d(a_sm + a * kATile, second ? &p.mapA1 : &p.mapA0, &full_bar[s], kk, w.e * p.a_rows + w.m0 + a * BM);
             for (int j = 0; j < nbB; ++j)
               tma_load_2d(b_sm + j * kBox, second ? &p.mapB1 : &p.mapB0, &full_bar[s], kk, w.row0 + 64 * j);
@@ -379,6 +397,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
         if (lane == 0) {
 #pragma unroll
           for (int a = 0; a < C::NUM_A; ++a) {
+            if (a >= w.na) break;
             const uint32_t a_base = a_sm + a * kATile;
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk) {
@@ -492,7 +511,12 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           float v0[16], v1[16];
           if (!zero && c0 < w.ncols) {
             tmem_ld16(t0u + c0, v0);
-            tmem_ld16(t0u + C::BN + c0, v1);
+            if (w.na == 2) {
+              tmem_ld16(t0u + C::BN + c0, v1);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) v1[i] = 0.f;
+            }
             tmem_wait_ld();
           } else {
 #pragma unroll
@@ -510,6 +534,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
         unsigned short* sw = reinterpret_cast<unsigned short*>(&stg[0][0][0]);
 #pragma unroll
         for (int mtl = 0; mtl < 2; ++mtl) {
+          if (mtl >= w.na) break;
           const int mbase = w.m0 + mtl * BM + q * 32;
 #pragma unroll
           for (int j = 0; j < NCH; ++j) {
@@ -535,7 +560,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
         }
       } else {
       // a paired unit's two M tiles go out one after the other (accumulators at t0 and t0 + BN)
-      for (int mtl = 0; mtl < (C::PAIR ? 2 : 1); ++mtl) {
+      for (int mtl = 0; mtl < (C::PAIR ? w.na : 1); ++mtl) {
       const uint32_t t0 = t0u + (uint32_t)(mtl * C::BN);
       const int mbase = w.m0 + mtl * BM + q * 32;
       for (int c0 = C::CW * cg; c0 < w.ncols; c0 += C::CW * G) {

@@ -359,6 +359,7 @@ EXPERT_SHAPES = [
     (96, 640, 64, 6, 384, torch.bfloat16, True),    # many empty and tiny segments
     (600, 256, 4, 2, 256, torch.bfloat16, False),   # > 160 rows per expert: 256-row gate/up chunks
     (520, 384, 4, 2, 128, torch.bfloat16, True),    # 256-row chunks over Zipf-sized segments
+    (400, 512, 80, 2, 512, torch.bfloat16, False),  # 160 paired units: the last 8 split into M tiles
 ]
 
 
