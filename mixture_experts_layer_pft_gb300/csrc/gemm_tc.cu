@@ -61,20 +61,21 @@ constexpr uint32_t kStageRegion = 196608;  // shared memory given to the stage r
 // rows of the weight dimension instead of once per 128 (one accumulator set, three stages).
 enum Mode {
   GATEUP = 0, DOWN = 1, DA = 2, DX = 3, WGRAD13 = 4, WGRAD2 = 5, GATEUP_WIDE = 6,
-  DOWN_PAIR = 7, DA_PAIR = 8, DX_PAIR = 9, WGRAD13_WIDE = 10
+  DOWN_PAIR = 7, DA_PAIR = 8, DX_PAIR = 9, WGRAD13_WIDE = 10, WGRAD2_PAIR = 11
 };
 
 template <int MODE> struct Cfg {
   static constexpr int BASE = MODE == GATEUP_WIDE ? GATEUP : MODE == DOWN_PAIR ? DOWN
                               : MODE == DA_PAIR ? DA : MODE == DX_PAIR ? DX
-                              : MODE == WGRAD13_WIDE ? WGRAD13 : MODE;
-  static constexpr bool PAIR = (MODE == DOWN_PAIR || MODE == DA_PAIR || MODE == DX_PAIR);
+                              : MODE == WGRAD13_WIDE ? WGRAD13 : MODE == WGRAD2_PAIR ? WGRAD2 : MODE;
+  static constexpr bool PAIR = (MODE == DOWN_PAIR || MODE == DA_PAIR || MODE == DX_PAIR);  // token-N pairs
+  static constexpr bool MPAIR = PAIR || MODE == WGRAD2_PAIR;  // two 128-row M tiles per unit
   static constexpr bool GU = (BASE == GATEUP);
-  static constexpr int NUM_A = (GU || BASE == WGRAD13 || PAIR) ? 2 : 1;  // accumulators per unit
+  static constexpr int NUM_A = (GU || BASE == WGRAD13 || MPAIR) ? 2 : 1;  // accumulators per unit
   static constexpr bool A_MN = (GU || BASE == DOWN || BASE == WGRAD13 || BASE == WGRAD2);
   static constexpr bool B_MN = (BASE == WGRAD13 || BASE == WGRAD2);
   static constexpr bool TOKEN_N = (BASE <= DX);
-  static constexpr int MT = PAIR ? 2 * BM : BM;  // rows of the weight (M) dimension per unit
+  static constexpr int MT = MPAIR ? 2 * BM : BM;  // rows of the weight (M) dimension per unit
   // gate/up and dW1/dW3 keep two accumulators per unit; 128-column tiles leave room to
   // double-buffer them (the _WIDE variants take 256 columns and one accumulator set)
   static constexpr int BN = (MODE == WGRAD13 || MODE == GATEUP) ? 128 : 256;
@@ -188,7 +189,7 @@ __device__ __forceinline__ Unit decode(int u, const Sched& sc, const int* s_pref
     const int per = sc.mt * sc.nt;
     w.e = u / per;
     const int r = u % per;
-    w.m0 = (r / sc.nt) * BM;
+    w.m0 = (r / sc.nt) * C::MT;
     w.n0 = (r % sc.nt) * C::BN;
     w.row0 = __ldg(p.offsets + w.e);
     w.rows = __ldg(p.offsets + w.e + 1) - w.row0;
@@ -338,6 +339,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
             if (C::BASE == WGRAD13) {
               tma_load_2d(a_sm + kATile, &p.mapA1, &full_bar[s], w.m0, y);
               tma_load_2d(a_sm + kATile + kBox, &p.mapA1, &full_bar[s], w.m0 + 64, y);
+            } else if (C::MPAIR) {
+              tma_load_2d(a_sm + kATile, &p.mapA0, &full_bar[s], w.m0 + 128, y);
+              tma_load_2d(a_sm + kATile + kBox, &p.mapA0, &full_bar[s], w.m0 + 192, y);
             }
             for (int j = 0; j < nbB; ++j) tma_load_2d(b_sm + j * kBox, &p.mapB0, &full_bar[s], w.n0 + 64 * j, y);
           }
@@ -447,10 +451,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       const size_t colbase = C::TOKEN_N ? (size_t)w.row0 : (size_t)w.n0;
       const size_t ebase = C::TOKEN_N ? 0 : (size_t)w.e * (size_t)p.out_expert_stride;
       if constexpr (!C::TOKEN_N) {
-        // weight gradients: the warp's whole share of the accumulators (dW1 then dW3, or dW2;
-        // 32 columns per TMEM load) goes to registers as bf16 pairs, TMEM goes back to the MMA
-        // warp, and the 32 x 32 tensor stores overlap the next unit's main loop
-        constexpr int NOUT = (C::BASE == WGRAD13) ? 2 : 1;
+        // weight gradients: the warp's whole share of the accumulators (dW1 then dW3, one or two
+        // M tiles of dW2; 32 columns per TMEM load) goes to registers as bf16 pairs, TMEM goes
+        // back to the MMA warp, and the 32 x 32 tensor stores overlap the next unit's main loop
+        constexpr int NOUT = C::NUM_A;
         constexpr int NCH = C::BN / (C::CW * G);  // 32-column chunks per warp
         const int mbase = w.m0 + q * 32;
         uint32_t pk[NOUT][NCH][16];
@@ -494,7 +498,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(a == 0 ? &p.mapO0 : &p.mapO1, smem_u32(sw), mbase, w.e * p.a_rows + w.n0 + c0);
+              if (C::BASE == WGRAD13)
+                tma_store_2d(a == 0 ? &p.mapO0 : &p.mapO1, smem_u32(sw), mbase, w.e * p.a_rows + w.n0 + c0);
+              else
+                tma_store_2d(&p.mapO0, smem_u32(sw), mbase + a * BM, w.e * p.a_rows + w.n0 + c0);
               bulk_commit();
             }
           }
@@ -792,7 +799,7 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
   w2.offsets = offsets; w2.E = E; w2.M = h; w2.Nw = f; w2.a_rows = f;
   w2.out0 = static_cast<__nv_bfloat16*>(dW2); w2.ld_out = h; w2.out_expert_stride = (long long)f * h;
   w2.status = status;
-  return launch<WGRAD2>(w2, st);
+  return h % 256 == 0 ? launch<WGRAD2_PAIR>(w2, st) : launch<WGRAD2>(w2, st);
 }
 
 }  // namespace moe
