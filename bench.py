@@ -506,13 +506,7 @@ def run_ours(args, w):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            inp["x"].copy_(hx, non_blocking=True)
-            if w.backward:
-                inp["dy"].copy_(hdy, non_blocking=True)
-            layer.step(inp, b)
-            hy.copy_(b.y, non_blocking=True)
-            if w.backward:
-                hdx.copy_(b.dx, non_blocking=True)
+            layer.step_host(inp, b, hx, hy, hdy, hdx)
             e1.record(stream)
             e1.synchronize()
             if s >= args.warmup:

@@ -2,7 +2,8 @@
 
 ``LayerBuffers`` allocates every device buffer of the layer once (PyTorch owns the memory);
 ``forward`` and ``backward`` issue the stage calls in order on the current stream.  Each stage
-runs in the library's kernels; this module only sequences them.
+runs in the library's kernels; this module only sequences them.  ``step_host`` runs a step whose
+tokens live in pinned host memory.
 """
 
 from __future__ import annotations
@@ -77,3 +78,36 @@ def step(inp: dict, b: LayerBuffers):
     forward(inp, b)
     if b.backward:
         backward(inp, inp["dy"], b)
+
+
+def step_host(inp: dict, b: LayerBuffers, hx: torch.Tensor, hy: torch.Tensor,
+              hdy: torch.Tensor | None = None, hdx: torch.Tensor | None = None):
+    """One layer step with the step's tokens in pinned host memory.
+
+    hx (and hdy) are copied into inp['x'] (and inp['dy']); y (and dx) come back into hy (and
+    hdx).  The upload of dy overlaps the forward and the download of y overlaps the backward, on
+    a second stream; the current stream waits for both, so the step is complete (host buffers
+    included) once the current stream is.
+    """
+    cur = torch.cuda.current_stream()
+    inp["x"].copy_(hx, non_blocking=True)
+    if not b.backward:
+        forward(inp, b)
+        hy.copy_(b.y, non_blocking=True)
+        return
+    side = getattr(b, "copy_stream", None)
+    if side is None:
+        side = b.copy_stream = torch.cuda.Stream(device=inp["x"].device)
+    side.wait_stream(cur)  # earlier readers of inp['dy'] and writers of hy are done
+    with torch.cuda.stream(side):
+        inp["dy"].copy_(hdy, non_blocking=True)
+        dy_ready = torch.cuda.Event()
+        dy_ready.record(side)
+    forward(inp, b)
+    side.wait_stream(cur)  # y is complete
+    with torch.cuda.stream(side):
+        hy.copy_(b.y, non_blocking=True)
+    cur.wait_event(dy_ready)
+    backward(inp, inp["dy"], b)
+    hdx.copy_(b.dx, non_blocking=True)
+    cur.wait_stream(side)

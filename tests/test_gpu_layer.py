@@ -216,3 +216,32 @@ def test_layer_step_is_bitwise_deterministic(M):
         outs.append([getattr(b, n).clone() for n in ("y", "dx", "dW1", "dW2", "dWg", "slot_of")])
     for a, c in zip(*outs):
         assert torch.equal(a, c)
+
+
+@pytest.mark.parametrize("cfg", [1, 4])
+def test_host_buffer_step_equals_device_step(M, cfg):
+    """step_host (pinned host tokens in, outputs back, copies overlapped on a second stream)
+    gives the same bits as the device-resident step, over two back-to-back steps."""
+    layer, workloads = M
+    w = workloads.WORKLOADS[cfg]
+    T = min(w.T, 2048)
+    inp = workloads.make_inputs(w, "cuda", T=T)
+    b = layer.LayerBuffers(T, w.h, w.E, w.k, w.f, w.torch_dtype(), backward=w.backward)
+    layer.step(inp, b)
+    torch.cuda.synchronize()
+    want_y = b.y.cpu()
+    want_dx = b.dx.cpu() if w.backward else None
+    hx = inp["x"].cpu().pin_memory()
+    hdy = inp["dy"].cpu().pin_memory()
+    hy = torch.empty_like(hx).pin_memory()
+    hdx = torch.empty_like(hx).pin_memory() if w.backward else None
+    for _ in range(2):
+        inp["x"].zero_()
+        inp["dy"].zero_()
+        b.y.zero_()
+        hy.zero_()
+        layer.step_host(inp, b, hx, hy, hdy, hdx)
+        torch.cuda.current_stream().synchronize()
+        assert torch.equal(hy, want_y)
+        if w.backward:
+            assert torch.equal(hdx, want_dx)
