@@ -9,6 +9,10 @@ dispatch backward.  Prints one JSON line (rank 0).
 Under torchrun each rank runs the step on its own GPU over its own tokens (weights drawn
 identically), with no collective on the data path; ``value`` is the whole-job throughput,
 the max over ranks of the timed region.
+
+The timed region replays the layer step captured as a CUDA graph (``--no-graph``: one host call
+per stage), one event pair per step.  Per-stage and per-kernel times, and the roofline's kernel
+duration, come from a second pass of the same steps with an event after every launch.
 """
 
 from __future__ import annotations
@@ -403,28 +407,54 @@ def run_ours(args, w):
     torch.cuda.synchronize()
     assert binding.moe_check_status(b.ws) == 0, "device status set during warm-up"
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
-    timer = binding.KernelTimer(64 * args.steps)
-    spans = [[] for _ in range(args.steps)]
+    # ---------------------------------------------------------------- timed region: whole steps
+    # Each step is the captured layer step (CUDA graph replay; --no-graph: one host call per
+    # stage), bracketed by one event pair; L2 is flushed between steps, outside the events.
+    if args.no_graph:
+        graph = None
+        per_step = None
+    else:
+        graph = layer.CapturedStep(lambda: run_stages(None))
+        per_step = graph.launches
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
     clocks = ClockSampler(device.index)
     clocks.start()
     n_launch0 = lib.moe_kernel_launches()
-    with timer:
-        barrier(world)
-        torch.cuda.synchronize()
-        for s in range(args.steps):
-            flush.zero_()  # evict L2 between steps (not timed: outside the step's events)
-            run_stages(events[s], timer, spans[s])
-        torch.cuda.synchronize()
-        barrier(world)
-    launches = lib.moe_kernel_launches() - n_launch0
+    barrier(world)
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        flush.zero_()
+        step_ev[s][0].record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            run_stages(None)
+        step_ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = (per_step * args.steps if graph is not None
+                else lib.moe_kernel_launches() - n_launch0)
     clk = clocks.stop()
     assert binding.moe_check_status(b.ws) == 0, "device status set during the timed region"
+    step_ms = [a.elapsed_time(e) for a, e in step_ev]
+    total_ms = max_over_ranks(sum(step_ms), world, device)
 
+    # ---------------------------------------------------------------- breakdown pass
+    # The same steps again, with an event before each stage call and after each kernel launch:
+    # per-stage and per-kernel times (the roofline's kernel duration) come from here.
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
+    timer = binding.KernelTimer(64 * args.steps)
+    spans = [[] for _ in range(args.steps)]
+    with timer:
+        torch.cuda.synchronize()
+        for s in range(args.steps):
+            flush.zero_()
+            run_stages(events[s], timer, spans[s])
+        torch.cuda.synchronize()
+    assert binding.moe_check_status(b.ws) == 0, "device status set during the breakdown pass"
     stage_ms = {STAGES[i]: [events[s][i].elapsed_time(events[s][i + 1]) for s in range(args.steps)]
                 for i in range(nst)}
-    step_ms = [events[s][0].elapsed_time(events[s][nst]) for s in range(args.steps)]
-    total_ms = max_over_ranks(sum(step_ms), world, device)
     ms_per_step = total_ms / args.steps
     flops = model_flops(w, T)
     value = world * flops / (ms_per_step * 1e-3) / 1e12
@@ -500,13 +530,18 @@ def run_ours(args, w):
         hdy.copy_(inp["dy"])
         hy = torch.empty_like(b.y, device="cpu").pin_memory()
         hdx = torch.empty_like(b.dx, device="cpu").pin_memory() if w.backward else None
+        host_step = lambda: layer.step_host(inp, b, hx, hy, hdy, hdx)  # noqa: E731
+        hgraph = None if args.no_graph else layer.CapturedStep(host_step)
         e_ms = []
         for s in range(args.steps + args.warmup):
             flush.zero_()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            layer.step_host(inp, b, hx, hy, hdy, hdx)
+            if hgraph is not None:
+                hgraph.replay()
+            else:
+                host_step()
             e1.record(stream)
             e1.synchronize()
             if s >= args.warmup:
@@ -537,6 +572,9 @@ def run_ours(args, w):
             "dispatch_GBps": stages["dispatch"]["GB/s"], "combine_GBps": stages["combine"]["GB/s"],
             "config": {"workload": workload_desc(w), "tokens_per_gpu": T,
                        "l2": "flushed between timed steps (256 MB write, outside the step events)",
+                       "step": ("one host call per stage" if args.no_graph else
+                                f"CUDA graph replay of the captured layer step ({per_step} library kernels)"),
+                       "breakdown": "stages and kernels timed in a second pass with an event after each launch",
                        "parallelism": f"replicas x{world} (independent tokens, no data-path collective)"},
             "stages": stages,
             "kernels": kernels,
@@ -562,6 +600,8 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time steps as one host call per stage instead of a CUDA graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget-tflop", type=float, default=0.1,
                     help="reference arm: algorithmic TFLOP per step of the oracle sample")

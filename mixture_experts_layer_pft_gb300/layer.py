@@ -3,7 +3,7 @@
 ``LayerBuffers`` allocates every device buffer of the layer once (PyTorch owns the memory);
 ``forward`` and ``backward`` issue the stage calls in order on the current stream.  Each stage
 runs in the library's kernels; this module only sequences them.  ``step_host`` runs a step whose
-tokens live in pinned host memory.
+tokens live in pinned host memory, and ``CapturedStep`` replays a captured step as one CUDA graph.
 """
 
 from __future__ import annotations
@@ -111,3 +111,30 @@ def step_host(inp: dict, b: LayerBuffers, hx: torch.Tensor, hy: torch.Tensor,
     backward(inp, inp["dy"], b)
     hdx.copy_(b.dx, non_blocking=True)
     cur.wait_stream(side)
+
+
+class CapturedStep:
+    """A layer step captured once as a CUDA graph and then replayed.
+
+    ``fn`` issues the step on the current stream (``lambda: step(inp, b)``, or ``step_host`` with
+    its host buffers); it must use the same tensors on every call, as the graph keeps their
+    addresses.  A replay runs the same kernels and copies in the same order on the caller's
+    current stream, with one graph launch in place of one host call per kernel.  ``launches`` is
+    the number of library kernels in the graph.
+    """
+
+    def __init__(self, fn, warmup: int = 1):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        n0 = B.lib().moe_kernel_launches()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn()
+        self.launches = B.lib().moe_kernel_launches() - n0
+
+    def replay(self):
+        self.graph.replay()

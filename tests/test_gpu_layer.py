@@ -245,3 +245,24 @@ def test_host_buffer_step_equals_device_step(M, cfg):
         assert torch.equal(hy, want_y)
         if w.backward:
             assert torch.equal(hdx, want_dx)
+
+
+def test_captured_step_replays_the_same_bits(M):
+    """CapturedStep (the step as one CUDA graph) reproduces the stream-launched step exactly."""
+    layer, workloads = M
+    w = workloads.WORKLOADS[1]
+    inp = workloads.make_inputs(w, "cuda")
+    b = layer.LayerBuffers(w.T, w.h, w.E, w.k, w.f, w.torch_dtype())
+    names = ("y", "dx", "dW1", "dW3", "dW2", "dWg", "slot_of")
+    layer.step(inp, b)
+    torch.cuda.synchronize()
+    want = [getattr(b, n).clone() for n in names]
+    g = layer.CapturedStep(lambda: layer.step(inp, b))
+    assert g.launches >= 15
+    for _ in range(2):
+        for n in names:
+            getattr(b, n).zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for n, t in zip(names, want):
+            assert torch.equal(getattr(b, n), t), n
