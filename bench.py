@@ -299,6 +299,8 @@ def kernel_names(stage, n, w):
         "dispatch_bwd": (["dispatch_bwd"], CSRC + "gather.cu"),
     }
     names, src = table[stage]
+    if stage == "dispatch" and n == 0:  # folded into the expert GEMMs
+        return [], src
     assert len(names) == n, (stage, n, names)
     return names, src
 
@@ -363,7 +365,8 @@ def run_ours(args, w):
     lib = binding.lib()
     T = w.T
     inp = workloads.make_inputs(w, device, token_seed=None if world == 1 else w.seed + 7919 * rank)
-    b = layer.LayerBuffers(T, w.h, w.E, w.k, w.f, w.torch_dtype(), device, backward=w.backward)
+    b = layer.LayerBuffers(T, w.h, w.E, w.k, w.f, w.torch_dtype(), device, backward=w.backward,
+                           fused=args.fused)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)  # 2x the 129 MB L2
     stream = torch.cuda.current_stream()
 
@@ -375,18 +378,25 @@ def run_ours(args, w):
                                       b.topk_idx, b.topk_w, b.ws),
             lambda: binding.moe_pft_build(b.topk_idx, w.E, b.num_ids, b.offsets, b.token_ids,
                                           b.expert_ids, b.slot_of, b.ws),
-            lambda: binding.moe_dispatch(inp["x"], b.token_ids, w.k, b.xbuf, b.ws),
-            lambda: binding.moe_expert_ffn(b.xbuf, b.offsets, inp["W1"], inp["W3"], inp["W2"],
-                                           b.ybuf, b.h1, b.h3, b.a, b.ws),
+            # fused: no dispatch call; the gate/up GEMM gathers its token rows from x
+            (lambda: None) if b.fused else
+            (lambda: binding.moe_dispatch(inp["x"], b.token_ids, w.k, b.xbuf, b.ws)),
+            (lambda: binding.moe_expert_ffn_gather(inp["x"], b.token_ids, b.offsets, inp["W1"], inp["W3"],
+                                                   inp["W2"], b.ybuf, b.h1, b.h3, b.a, b.ws)) if b.fused else
+            (lambda: binding.moe_expert_ffn(b.xbuf, b.offsets, inp["W1"], inp["W3"], inp["W2"],
+                                            b.ybuf, b.h1, b.h3, b.a, b.ws)),
             lambda: binding.moe_combine(b.ybuf, b.slot_of, b.topk_w, b.y, b.ws),
         ]
         if w.backward:
             calls += [
                 lambda: binding.moe_combine_bwd(inp["dy"], b.ybuf, b.slot_of, b.topk_w, b.dybuf,
                                                 b.d_topk_w, b.ws),
-                lambda: binding.moe_expert_ffn_bwd(b.dybuf, b.xbuf, b.h1, b.h3, b.a, b.offsets,
-                                                   inp["W1"], inp["W3"], inp["W2"], b.dxbuf,
-                                                   b.dW1, b.dW3, b.dW2, b.ws),
+                (lambda: binding.moe_expert_ffn_bwd_gather(b.dybuf, inp["x"], b.token_ids, b.h1, b.h3, b.a,
+                                                           b.offsets, inp["W1"], inp["W3"], inp["W2"],
+                                                           b.dxbuf, b.dW1, b.dW3, b.dW2, b.ws)) if b.fused else
+                (lambda: binding.moe_expert_ffn_bwd(b.dybuf, b.xbuf, b.h1, b.h3, b.a, b.offsets,
+                                                    inp["W1"], inp["W3"], inp["W2"], b.dxbuf,
+                                                    b.dW1, b.dW3, b.dW2, b.ws)),
                 lambda: binding.moe_route_bwd(inp["x"], inp["Wg"], b.probs, b.topk_idx, b.d_topk_w,
                                               b.d_logits, b.dWg, b.dx_router, b.ws),
                 lambda: binding.moe_dispatch_bwd(b.dxbuf, b.slot_of, b.dx_router, w.k, b.dx, b.ws),
@@ -464,6 +474,9 @@ def run_ours(args, w):
     for n, ms in stage_ms.items():
         avg = sum(ms) / len(ms)
         c = counts[n]
+        if b.fused and n == "dispatch":
+            stages[n] = {"ms": round(avg, 4), "GB/s": None, "note": "no launch: folded into the expert GEMMs"}
+            continue
         stages[n] = {"ms": round(avg, 4), "GB/s": round(c["bytes"] / (avg * 1e-3) / 1e9, 1)}
         if c["flops"] and n.startswith(("expert", "route")):
             stages[n]["TFLOP/s"] = round(c["flops"] / (avg * 1e-3) / 1e12, 2)
@@ -569,12 +582,15 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded N(0,1) tokens, random-init weights)",
             "tokens_per_s": world * T / (ms_per_step * 1e-3),
-            "dispatch_GBps": stages["dispatch"]["GB/s"], "combine_GBps": stages["combine"]["GB/s"],
+            "dispatch_GBps": None if b.fused else stages["dispatch"]["GB/s"],
+            "combine_GBps": stages["combine"]["GB/s"],
             "config": {"workload": workload_desc(w), "tokens_per_gpu": T,
                        "l2": "flushed between timed steps (256 MB write, outside the step events)",
                        "step": ("one host call per stage" if args.no_graph else
                                 f"CUDA graph replay of the captured layer step ({per_step} library kernels)"),
                        "breakdown": "stages and kernels timed in a second pass with an event after each launch",
+                       "dispatch": ("folded into the gate/up and dW1/dW3 GEMMs (rows gathered from x)"
+                                    if b.fused else "its own kernel writing the padding-free buffer"),
                        "parallelism": f"replicas x{world} (independent tokens, no data-path collective)"},
             "stages": stages,
             "kernels": kernels,
@@ -600,6 +616,8 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="fold dispatch into the expert GEMMs (bf16 tensor-core path; rows gathered from x)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time steps as one host call per stage instead of a CUDA graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")

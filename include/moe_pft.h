@@ -233,6 +233,31 @@ int moe_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, cons
                        void* dW1, void* dW3, void* dW2, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Dispatch folded into the expert GEMMs -- the fused single-GPU path of FlashDMoE's blog (§4,
+ * the persistent kernel that gathers its tokens itself instead of staging a dispatched copy).
+ * The same results, bit for bit, as moe_dispatch(x, token_ids) followed by moe_expert_ffn /
+ * moe_expert_ffn_bwd on the xbuf it writes, without materialising xbuf: the GEMMs that read it
+ * (gate/up in the forward, dW1/dW3 in the backward) load row p as x[token_ids[p]].
+ * x: [T,h] dtype.  token_ids: [Tk] int32 from moe_pft_build (an id outside [0,T) reads as a
+ * zero row and sets MOE_STATUS_BAD_INDEX, as moe_dispatch does).  Other arguments as in
+ * moe_expert_ffn / moe_expert_ffn_bwd.  Runs on the tensor-core engine only: bf16 with h and f
+ * multiples of 128 (moe_expert_ffn_gather_supported), and T * h < 2^31; otherwise
+ * MOE_ERR_UNSUPPORTED.
+ */
+int moe_expert_ffn_gather(const void* x, const int32_t* token_ids, int T, const int32_t* offsets,
+                          const void* W1, const void* W3, const void* W2, int Tk, int E, int h, int f,
+                          int dtype, void* ybuf, void* h1, void* h3, void* a, void* ws, size_t ws_bytes,
+                          void* stream);
+int moe_expert_ffn_bwd_gather(const void* dybuf, const void* x, const int32_t* token_ids, int T,
+                              const void* h1, const void* h3, const void* a, const int32_t* offsets,
+                              const void* W1, const void* W3, const void* W2, int Tk, int E, int h, int f,
+                              int dtype, void* dxbuf, void* dW1, void* dW3, void* dW2, void* ws,
+                              size_t ws_bytes, void* stream);
+/* 1 when moe_expert_ffn_gather / moe_expert_ffn_bwd_gather run for this shape and dtype, else 0
+ * (host only; no device access). */
+int moe_expert_ffn_gather_supported(int h, int f, int dtype);
+
+/*
  * Combine -- X-MoE review §3 "Training pipeline" step 6 and the FlashDMoE blog §1.1 (results
  * return to the origin and are merged with the gate weights):
  *   y[t,:] = sum_{j=0..k-1} topk_w[t,j] * ybuf[slot_of[t*k+j],:], j ascending, fp32, rounded once.

@@ -44,6 +44,11 @@ SIGNATURES = {
     "moe_expert_ffn": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_ffn_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                 _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_expert_ffn_gather": (_I, [_P, _P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                   _P, _Z, _P]),
+    "moe_expert_ffn_bwd_gather": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
+                                       _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_expert_ffn_gather_supported": (_I, [_I, _I, _I]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
 }
@@ -218,6 +223,29 @@ def moe_expert_ffn_bwd(dybuf, xbuf, h1, h3, a, offsets, W1, W3, W2, dxbuf, dW1, 
     _call("moe_expert_ffn_bwd", _p(dybuf), _p(xbuf), _p(h1), _p(h3), _p(a), _p(offsets), _p(W1),
           _p(W3), _p(W2), Tk, E, h, f, _dtype_code(xbuf), _p(dxbuf), _p(dW1), _p(dW3), _p(dW2),
           _p(ws), ws.numel(), _stream())
+
+
+def moe_expert_ffn_gather(x, token_ids, offsets, W1, W3, W2, ybuf, h1, h3, a, ws):
+    T, h = x.shape
+    Tk = token_ids.shape[0]
+    E, _, f = W1.shape
+    _call("moe_expert_ffn_gather", _p(x), _p(token_ids), T, _p(offsets), _p(W1), _p(W3), _p(W2), Tk, E,
+          h, f, _dtype_code(x), _p(ybuf), _p(h1), _p(h3), _p(a), _p(ws), ws.numel(), _stream())
+
+
+def moe_expert_ffn_bwd_gather(dybuf, x, token_ids, h1, h3, a, offsets, W1, W3, W2, dxbuf, dW1, dW3, dW2,
+                              ws):
+    T, h = x.shape
+    Tk = token_ids.shape[0]
+    E, _, f = W1.shape
+    _call("moe_expert_ffn_bwd_gather", _p(dybuf), _p(x), _p(token_ids), T, _p(h1), _p(h3), _p(a),
+          _p(offsets), _p(W1), _p(W3), _p(W2), Tk, E, h, f, _dtype_code(x), _p(dxbuf), _p(dW1), _p(dW3),
+          _p(dW2), _p(ws), ws.numel(), _stream())
+
+
+def moe_expert_ffn_gather_supported(h: int, f: int, dtype: torch.dtype) -> bool:
+    code = MOE_BF16 if dtype == torch.bfloat16 else MOE_F32
+    return bool(lib().moe_expert_ffn_gather_supported(h, f, code))
 
 
 def moe_combine(ybuf, slot_of, topk_w, y, ws):

@@ -290,37 +290,46 @@ int moe_dispatch_bwd(const void* dxbuf, const int32_t* slot_of, const float* dx_
   return check_launch("moe_dispatch_bwd");
 }
 
-int moe_expert_ffn(const void* xbuf, const int32_t* offsets, const void* W1, const void* W3,
-                   const void* W2, int Tk, int E, int h, int f, int dtype, void* ybuf, void* h1,
-                   void* h3, void* a, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+
+int expert_ffn_impl(const char* fn, TokenRows xr, const int32_t* offsets, const void* W1, const void* W3,
+                    const void* W2, int Tk, int E, int h, int f, int dtype, void* ybuf, void* h1, void* h3,
+                    void* a, void* ws, size_t ws_bytes, cudaStream_t st) {
   REQUIRE(Tk >= 0 && E >= 1 && E <= 1024 && h >= 8 && f >= 8, MOE_ERR_INVALID_ARG,
           "moe_expert_ffn: need Tk >= 0, 1 <= E <= 1024, h >= 8, f >= 8");
   REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_expert_ffn: bad dtype");
   REQUIRE(h % 8 == 0 && f % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_expert_ffn: h and f must be multiples of 8");
+  REQUIRE(xr.xbuf != nullptr || use_tensor_cores(dtype, h, f), MOE_ERR_UNSUPPORTED,
+          "moe_expert_ffn_gather: needs the tensor-core engine (bf16, h and f multiples of 128)");
   REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_EXPERT_FFN, Tk, h, E, 1, f, dtype),
           MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace too small");
   if (Tk == 0) return MOE_OK;
-  REQUIRE_PTR(xbuf); REQUIRE_PTR(offsets); REQUIRE_PTR(W1); REQUIRE_PTR(W3); REQUIRE_PTR(W2);
+  if (xr.xbuf == nullptr) {
+    REQUIRE(xr.T >= 1, MOE_ERR_INVALID_ARG, "moe_expert_ffn_gather: need T >= 1");
+    REQUIRE((long long)xr.T * h < (1LL << 31), MOE_ERR_UNSUPPORTED, "moe_expert_ffn_gather: T * h >= 2^31");
+    REQUIRE_PTR(xr.x); REQUIRE_PTR(xr.token_ids);
+  }
+  REQUIRE_PTR(offsets); REQUIRE_PTR(W1); REQUIRE_PTR(W3); REQUIRE_PTR(W2);
   REQUIRE_PTR(ybuf); REQUIRE_PTR(h1); REQUIRE_PTR(h3); REQUIRE_PTR(a);
   if (use_tensor_cores(dtype, h, f)) {
-    if (tc_expert_ffn(xbuf, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, status_of(ws),
-                      (cudaStream_t)stream) != 0)
-      return tc_failure("moe_expert_ffn");
+    if (tc_expert_ffn(xr, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, status_of(ws), st) != 0)
+      return tc_failure(fn);
   } else {
-    simt_expert_ffn(dtype, xbuf, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, (cudaStream_t)stream);
+    simt_expert_ffn(dtype, xr.xbuf, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, st);
   }
-  return check_launch("moe_expert_ffn");
+  return check_launch(fn);
 }
 
-int moe_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const void* h3,
-                       const void* a, const int32_t* offsets, const void* W1, const void* W3,
-                       const void* W2, int Tk, int E, int h, int f, int dtype, void* dxbuf,
-                       void* dW1, void* dW3, void* dW2, void* ws, size_t ws_bytes, void* stream) {
-  const cudaStream_t st = (cudaStream_t)stream;
+int expert_ffn_bwd_impl(const char* fn, const void* dybuf, TokenRows xr, const void* h1, const void* h3,
+                        const void* a, const int32_t* offsets, const void* W1, const void* W3, const void* W2,
+                        int Tk, int E, int h, int f, int dtype, void* dxbuf, void* dW1, void* dW3, void* dW2,
+                        void* ws, size_t ws_bytes, cudaStream_t st) {
   REQUIRE(Tk >= 0 && E >= 1 && E <= 1024 && h >= 8 && f >= 8, MOE_ERR_INVALID_ARG,
           "moe_expert_ffn_bwd: need Tk >= 0, 1 <= E <= 1024, h >= 8, f >= 8");
   REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_expert_ffn_bwd: bad dtype");
   REQUIRE(h % 8 == 0 && f % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_expert_ffn_bwd: h and f must be multiples of 8");
+  REQUIRE(xr.xbuf != nullptr || use_tensor_cores(dtype, h, f), MOE_ERR_UNSUPPORTED,
+          "moe_expert_ffn_bwd_gather: needs the tensor-core engine (bf16, h and f multiples of 128)");
   REQUIRE(ws != nullptr && aligned16(ws) &&
               ws_bytes >= moe_workspace_size(MOE_OP_EXPERT_FFN_BWD, Tk, h, E, 1, f, dtype),
           MOE_ERR_WORKSPACE, "moe_expert_ffn_bwd: workspace too small");
@@ -330,22 +339,69 @@ int moe_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, cons
     cudaMemsetAsync(dW1, 0, wb, st);
     cudaMemsetAsync(dW3, 0, wb, st);
     cudaMemsetAsync(dW2, 0, wb, st);
-    return check_launch("moe_expert_ffn_bwd");
+    return check_launch(fn);
   }
-  REQUIRE_PTR(dybuf); REQUIRE_PTR(xbuf); REQUIRE_PTR(h1); REQUIRE_PTR(h3); REQUIRE_PTR(a);
+  if (xr.xbuf == nullptr) {
+    REQUIRE(xr.T >= 1, MOE_ERR_INVALID_ARG, "moe_expert_ffn_bwd_gather: need T >= 1");
+    REQUIRE((long long)xr.T * h < (1LL << 31), MOE_ERR_UNSUPPORTED, "moe_expert_ffn_bwd_gather: T * h >= 2^31");
+    REQUIRE_PTR(xr.x); REQUIRE_PTR(xr.token_ids);
+  }
+  REQUIRE_PTR(dybuf); REQUIRE_PTR(h1); REQUIRE_PTR(h3); REQUIRE_PTR(a);
   REQUIRE_PTR(offsets); REQUIRE_PTR(W1); REQUIRE_PTR(W3); REQUIRE_PTR(W2); REQUIRE_PTR(dxbuf);
   char* base = static_cast<char*>(ws) + sizeof(WsHeader);
   void* dh1 = base;
   void* dh3 = base + round256((size_t)Tk * f * esize(dtype));
   if (use_tensor_cores(dtype, h, f)) {
-    if (tc_expert_ffn_bwd(dybuf, xbuf, h1, h3, a, offsets, W1, W3, W2, Tk, E, h, f, dxbuf, dW1, dW3, dW2,
+    if (tc_expert_ffn_bwd(dybuf, xr, h1, h3, a, offsets, W1, W3, W2, Tk, E, h, f, dxbuf, dW1, dW3, dW2,
                           dh1, dh3, status_of(ws), st) != 0)
-      return tc_failure("moe_expert_ffn_bwd");
+      return tc_failure(fn);
   } else {
-    simt_expert_ffn_bwd(dtype, dybuf, xbuf, h1, h3, a, offsets, W1, W3, W2, Tk, E, h, f, dxbuf, dW1,
+    simt_expert_ffn_bwd(dtype, dybuf, xr.xbuf, h1, h3, a, offsets, W1, W3, W2, Tk, E, h, f, dxbuf, dW1,
                         dW3, dW2, dh1, dh3, st);
   }
-  return check_launch("moe_expert_ffn_bwd");
+  return check_launch(fn);
+}
+
+}  // namespace
+
+int moe_expert_ffn(const void* xbuf, const int32_t* offsets, const void* W1, const void* W3,
+                   const void* W2, int Tk, int E, int h, int f, int dtype, void* ybuf, void* h1,
+                   void* h3, void* a, void* ws, size_t ws_bytes, void* stream) {
+  if (xbuf == nullptr && Tk > 0) return fail(MOE_ERR_INVALID_ARG, "moe_expert_ffn: null xbuf");
+  return expert_ffn_impl("moe_expert_ffn", TokenRows{xbuf, nullptr, nullptr, 0}, offsets, W1, W3, W2, Tk, E, h, f,
+                         dtype, ybuf, h1, h3, a, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int moe_expert_ffn_gather(const void* x, const int32_t* token_ids, int T, const int32_t* offsets,
+                          const void* W1, const void* W3, const void* W2, int Tk, int E, int h, int f,
+                          int dtype, void* ybuf, void* h1, void* h3, void* a, void* ws, size_t ws_bytes,
+                          void* stream) {
+  return expert_ffn_impl("moe_expert_ffn_gather", TokenRows{nullptr, x, token_ids, T}, offsets, W1, W3, W2, Tk,
+                         E, h, f, dtype, ybuf, h1, h3, a, ws, ws_bytes, (cudaStream_t)stream);
+}
+
+int moe_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const void* h3,
+                       const void* a, const int32_t* offsets, const void* W1, const void* W3,
+                       const void* W2, int Tk, int E, int h, int f, int dtype, void* dxbuf,
+                       void* dW1, void* dW3, void* dW2, void* ws, size_t ws_bytes, void* stream) {
+  if (xbuf == nullptr && Tk > 0) return fail(MOE_ERR_INVALID_ARG, "moe_expert_ffn_bwd: null xbuf");
+  return expert_ffn_bwd_impl("moe_expert_ffn_bwd", dybuf, TokenRows{xbuf, nullptr, nullptr, 0}, h1, h3, a,
+                             offsets, W1, W3, W2, Tk, E, h, f, dtype, dxbuf, dW1, dW3, dW2, ws, ws_bytes,
+                             (cudaStream_t)stream);
+}
+
+int moe_expert_ffn_bwd_gather(const void* dybuf, const void* x, const int32_t* token_ids, int T,
+                              const void* h1, const void* h3, const void* a, const int32_t* offsets,
+                              const void* W1, const void* W3, const void* W2, int Tk, int E, int h, int f,
+                              int dtype, void* dxbuf, void* dW1, void* dW3, void* dW2, void* ws,
+                              size_t ws_bytes, void* stream) {
+  return expert_ffn_bwd_impl("moe_expert_ffn_bwd_gather", dybuf, TokenRows{nullptr, x, token_ids, T}, h1, h3,
+                             a, offsets, W1, W3, W2, Tk, E, h, f, dtype, dxbuf, dW1, dW3, dW2, ws, ws_bytes,
+                             (cudaStream_t)stream);
+}
+
+int moe_expert_ffn_gather_supported(int h, int f, int dtype) {
+  return dtype_ok(dtype) && h >= 8 && f >= 8 && use_tensor_cores(dtype, h, f) ? 1 : 0;
 }
 
 int moe_combine(const void* ybuf, const int32_t* slot_of, const float* topk_w, int T, int k,

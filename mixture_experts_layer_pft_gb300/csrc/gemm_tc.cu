@@ -118,6 +118,12 @@ struct TcParams {
   int ld_out;
   long long out_expert_stride;  // wgrad: elements between consecutive experts' outputs
   int* status;
+  // gate/up and dW1/dW3 with gathered token rows: row p of the padding-free buffer is read as
+  // gx[gids[p]] (gx: [gx_rows, gx_ld]); null gx means the buffer comes through mapB0
+  const __nv_bfloat16* gx;
+  const int* gids;
+  int gx_rows;
+  int gx_ld;
 };
 
 // Logistic function for the bf16 epilogues: the fast exponential and division are accurate to a
@@ -275,7 +281,10 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
 
   // ------------------------------------------------------------------ barriers + TMEM
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
+    // gathered token rows: a stage's full barrier also takes one arrival per producer lane, made
+    // by the hardware once that lane's row copies have landed
+    const uint32_t full_count = ((C::GU || C::BASE == WGRAD13) && p.gx != nullptr) ? 33u : 1u;
+    for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full_bar[s], full_count); mbar_init(&empty_bar[s], 1); }
     for (int b = 0; b < C::ACC_BUFS; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], C::EPI_WARPS); }
     mbar_init(&drain_bar, 1);
     s_abort = 0;
@@ -294,8 +303,98 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
   const uint32_t tmem_base = s_tmem;
 
   if (warp == 0) {
-    // ================================================================ TMA producer
-    if (lane == 0) {
+    if ((C::GU || C::BASE == WGRAD13) && p.gx != nullptr) {
+      // ============================================================== producer, gathered rows
+      // The weight-side tiles come by TMA (lane 0).  The token-side tile is gathered from gx by
+      // the whole warp with 16-byte copies, written in the 128-byte swizzled layout a tensor
+      // map would produce (16-byte chunk c of row r lands at chunk c ^ (r & 7) of the row).
+      // Rows past the segment and columns past the matrix are zero-filled.  Every lane then
+      // arrives on the stage's full barrier through its copies' completion (cp.async arrive),
+      // so the warp never waits for its own copies; the MMA warp fences the landed rows into the
+      // async proxy before multiplying them.
+      constexpr int NR = C::GU ? C::BN / 32 : 2;  // row offsets per lane: rows lane + 32 j
+      const int g = lane >> 3, c = lane & 7;      // row group of 8 lanes; 16-byte chunk of the row
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      // element offset of buffer row p in gx, or -1 for a zero row (past the segment, bad id)
+      auto row_offset = [&](int rel, int limit, int prow) -> int {
+        if (rel >= limit) return -1;
+        const int t = __ldg(p.gids + prow);
+        if ((unsigned)t < (unsigned)p.gx_rows) return t * p.gx_ld;
+        flag_status(p.status, MOE_STATUS_BAD_INDEX);
+        return -1;
+      };
+      for (int u = blockIdx.x; u < sc.total && ok; u += gridDim.x) {
+        const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
+        const uint32_t tx = (uint32_t)w.na * kATile;
+        int roff[NR];
+        if (C::GU) {  // gate/up: the chunk's rows serve every K step of the unit
+#pragma unroll
+          for (int j = 0; j < NR; ++j) roff[j] = row_offset(lane + 32 * j, w.rows, w.row0 + lane + 32 * j);
+        }
+        for (int ks = 0; ks < w.nk; ++ks) {
+          const int k0 = ks * BK;
+          if (!C::GU) {  // dW1/dW3: this K step's 64 token rows
+#pragma unroll
+            for (int j = 0; j < NR; ++j)
+              roff[j] = row_offset(k0 + lane + 32 * j, w.rows, w.row0 + k0 + lane + 32 * j);
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[s], ph ^ 1u, &s_abort, p.status))) {
+            ok = false;
+            break;
+          }
+          const uint32_t a_sm = ring + s * C::STAGE_BYTES;
+          const uint32_t b_sm = a_sm + C::A_BYTES;
+          if (lane == 0) {
+            mbar_expect_tx(&full_bar[s], tx);
+            const int y = C::GU ? w.e * p.a_rows + k0 : w.row0 + k0;
+            tma_load_2d(a_sm, &p.mapA0, &full_bar[s], w.m0, y);
+            tma_load_2d(a_sm + kBox, &p.mapA0, &full_bar[s], w.m0 + 64, y);
+            tma_load_2d(a_sm + kATile, &p.mapA1, &full_bar[s], w.m0, y);
+            tma_load_2d(a_sm + kATile + kBox, &p.mapA1, &full_bar[s], w.m0 + 64, y);
+          }
+          // copy i moves chunk c of one row; the row's offset comes from the lane that loaded it
+          if (C::GU) {
+            // gate/up: row rr = 4 i + g of the chunk (K-major, one 64-row box per 64 rows), K = k0..
+#pragma unroll
+            for (int i = 0; i < C::BN / 4; ++i) {
+              const int rr = 4 * i + g;
+              const int off = __shfl_sync(0xffffffffu, roff[i >> 3], 4 * (i & 7) + g);
+              if (rr < w.nmma) {
+                const bool live = off >= 0;
+                cp_async_16(b_sm + (rr >> 6) * kBox + (rr & 63) * 128 + ((c ^ (rr & 7)) << 4),
+                            live ? p.gx + off + k0 + 8 * c : p.gx, live ? 16u : 0u);
+              }
+            }
+          } else {
+            // dW1/dW3: token row r = 4 m + g of the step (MN-major, one box per 64 columns of h)
+#pragma unroll
+            for (int i = 0; i < C::BN / 4; ++i) {
+              const int box = i >> 4, m = i & 15, r = 4 * m + g;
+              const int off = __shfl_sync(0xffffffffu, roff[m >> 3], 4 * (m & 7) + g);
+              const int col = w.n0 + 64 * box;
+              if (64 * box < w.ncols) {
+                const bool live = off >= 0 && col < p.Nw;
+                cp_async_16(b_sm + box * kBox + r * 128 + ((c ^ (r & 7)) << 4),
+                            live ? p.gx + off + col + 8 * c : p.gx, live ? 16u : 0u);
+              }
+            }
+          }
+          cp_async_arrive_noinc(&full_bar[s]);
+          if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      cp_async_wait<0>();  // no copy of this warp outlives it
+      if (lane == 0) {
+        if (!ok) {
+          const unsigned long long t0 = globaltimer();
+          while (globaltimer() - t0 < 2000000ull) {
+          }
+        }
+      }
+    } else if (lane == 0) {
+      // ============================================================== TMA producer
       int s = 0;
       uint32_t ph = 0;
       bool ok = true;
@@ -375,6 +474,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       const uint32_t d0 = tmem_base + (uint32_t)(b * C::NUM_A * C::BN);
       for (int ks = 0; ks < w.nk; ++ks) {
         if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], ph, &s_abort, p.status))) { ok = false; break; }
+        if ((C::GU || C::BASE == WGRAD13) && p.gx != nullptr) {
+          // gathered rows were written by cp.async (generic proxy); the MMAs read them through
+          // the async proxy
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        }
         const uint32_t a_sm = ring + s * C::STAGE_BYTES;
         const uint32_t b_sm = a_sm + C::A_BYTES;
         int nsl = BK / 16;  // K slices of 16 to multiply in this stage
@@ -734,11 +838,23 @@ bool tc_supported(int dtype, int h, int f) {
   return dtype == MOE_BF16 && h % 128 == 0 && f % 128 == 0 && encode_fn() != nullptr;
 }
 
-int tc_expert_ffn(const void* xbuf, const int* offsets, const void* W1, const void* W3, const void* W2, int Tk,
+namespace {
+// The token-side operand of gate/up and dW1/dW3: the buffer's tensor map, or the gather source.
+bool set_token_rows(TcParams* p, const TokenRows& xr, int Tk, int h) {
+  if (xr.xbuf != nullptr) return tc_make_map(&p->mapB0, xr.xbuf, Tk, h, 64, 64);
+  p->gx = static_cast<const __nv_bfloat16*>(xr.x);
+  p->gids = xr.token_ids;
+  p->gx_rows = xr.T;
+  p->gx_ld = h;
+  return xr.x != nullptr && xr.token_ids != nullptr;
+}
+}  // namespace
+
+int tc_expert_ffn(TokenRows xr, const int* offsets, const void* W1, const void* W3, const void* W2, int Tk,
                   int E, int h, int f, void* ybuf, void* h1, void* h3, void* a, int* status, cudaStream_t st) {
   TcParams g = blank_params();
   bool ok = tc_make_map(&g.mapA0, W1, (long long)E * h, f, 64, 64) &&
-            tc_make_map(&g.mapA1, W3, (long long)E * h, f, 64, 64) && tc_make_map(&g.mapB0, xbuf, Tk, h, 64, 64);
+            tc_make_map(&g.mapA1, W3, (long long)E * h, f, 64, 64) && set_token_rows(&g, xr, Tk, h);
   if (!ok) return -1;
   g.offsets = offsets; g.E = E; g.M = f; g.K = h; g.a_rows = h;
   g.out0 = static_cast<__nv_bfloat16*>(h1); g.out1 = static_cast<__nv_bfloat16*>(h3);
@@ -754,7 +870,7 @@ int tc_expert_ffn(const void* xbuf, const int* offsets, const void* W1, const vo
   return h % 256 == 0 ? launch<DOWN_PAIR>(d, st) : launch<DOWN>(d, st);
 }
 
-int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const void* h3, const void* a,
+int tc_expert_ffn_bwd(const void* dybuf, TokenRows xr, const void* h1, const void* h3, const void* a,
                       const int* offsets, const void* W1, const void* W3, const void* W2, int Tk, int E, int h,
                       int f, void* dxbuf, void* dW1, void* dW3, void* dW2, void* dh1, void* dh3, int* status,
                       cudaStream_t st) {
@@ -780,7 +896,7 @@ int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const
   // dW1[e]^T = dh1^T X, dW3[e]^T = dh3^T X  (stored as dW1[e][h][f])
   TcParams w13 = blank_params();
   ok = tc_make_map(&w13.mapA0, dh1, Tk, f, 64, 64) && tc_make_map(&w13.mapA1, dh3, Tk, f, 64, 64) &&
-       tc_make_map(&w13.mapB0, xbuf, Tk, h, 64, 64);
+       set_token_rows(&w13, xr, Tk, h);
   if (!ok) return -1;
   ok = tc_make_map(&w13.mapO0, dW1, (long long)E * h, f, 32, Cfg<WGRAD13>::CW, false) &&
        tc_make_map(&w13.mapO1, dW3, (long long)E * h, f, 32, Cfg<WGRAD13>::CW, false);

@@ -74,10 +74,18 @@ int tc_router_bwd(const void* x, const float* Wg, const float* d_logits, int T, 
 
 // gemm_tc.cu -- tcgen05/TMEM/TMA grouped GEMMs (bf16; h and f multiples of 128)
 bool tc_supported(int dtype, int h, int f);
-int tc_expert_ffn(const void* xbuf, const int* offsets, const void* W1, const void* W3, const void* W2,
+// Token rows of the padding-free buffer: either xbuf itself ([Tk,h]), or, with xbuf null, row p
+// read as x[token_ids[p]] (x: [T,h]) by the GEMMs that consume it (gate/up, dW1/dW3).
+struct TokenRows {
+  const void* xbuf;
+  const void* x;
+  const int* token_ids;
+  int T;
+};
+int tc_expert_ffn(TokenRows xr, const int* offsets, const void* W1, const void* W3, const void* W2,
                   int Tk, int E, int h, int f, void* ybuf, void* h1, void* h3, void* a, int* status,
                   cudaStream_t st);
-int tc_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, const void* h3, const void* a,
+int tc_expert_ffn_bwd(const void* dybuf, TokenRows xr, const void* h1, const void* h3, const void* a,
                       const int* offsets, const void* W1, const void* W3, const void* W2, int Tk, int E,
                       int h, int f, void* dxbuf, void* dW1, void* dW3, void* dW2, void* dh1, void* dh3,
                       int* status, cudaStream_t st);

@@ -14,9 +14,23 @@ from . import binding as B
 
 
 class LayerBuffers:
+    """Device buffers of one layer.
+
+    With ``fused`` the expert GEMMs gather their token rows from x (the library's
+    moe_expert_ffn_gather / moe_expert_ffn_bwd_gather: bf16, h and f multiples of 128), so the
+    dispatched buffer xbuf is never written and ``xbuf`` is None.  The results are the same bits
+    as the dispatched path.  The default is the dispatched path: the gathered loads, 16-byte
+    copies from one producer warp, keep too few bytes in flight to match the tensor loads of
+    a dispatched buffer.
+    """
+
     def __init__(self, T: int, h: int, E: int, k: int, f: int, dtype: torch.dtype, device="cuda",
-                 backward: bool = True, gate: str = "softmax", renorm: bool = False):
+                 backward: bool = True, gate: str = "softmax", renorm: bool = False,
+                 fused: bool = False):
         self.T, self.h, self.E, self.k, self.f, self.dtype = T, h, E, k, f, dtype
+        if fused and not B.moe_expert_ffn_gather_supported(h, f, dtype):
+            raise ValueError("fused layer needs bf16 with h and f multiples of 128")
+        self.fused = bool(fused)
         self.gate, self.renorm = gate, renorm
         Tk = T * k
         f32, i32 = torch.float32, torch.int32
@@ -30,7 +44,7 @@ class LayerBuffers:
         self.token_ids = torch.empty(Tk, dtype=i32, **d)
         self.expert_ids = torch.empty(Tk, dtype=i32, **d)
         self.slot_of = torch.empty(Tk, dtype=i32, **d)
-        self.xbuf = torch.empty(Tk, h, dtype=dtype, **d)
+        self.xbuf = None if self.fused else torch.empty(Tk, h, dtype=dtype, **d)
         self.h1 = torch.empty(Tk, f, dtype=dtype, **d)
         self.h3 = torch.empty(Tk, f, dtype=dtype, **d)
         self.a = torch.empty(Tk, f, dtype=dtype, **d)
@@ -52,12 +66,17 @@ class LayerBuffers:
 
 
 def forward(inp: dict, b: LayerBuffers):
-    """Gate -> PFT build -> dispatch -> experts -> combine.  Returns b.y."""
+    """Gate -> PFT build -> dispatch -> experts -> combine (dispatch folded into the expert
+    GEMMs when b.fused).  Returns b.y."""
     B.moe_route(inp["x"], inp["Wg"], inp.get("bias"), b.k, b.logits, b.probs, b.topk_idx, b.topk_w, b.ws,
                 gate=b.gate, renorm=b.renorm)
     B.moe_pft_build(b.topk_idx, b.E, b.num_ids, b.offsets, b.token_ids, b.expert_ids, b.slot_of, b.ws)
-    B.moe_dispatch(inp["x"], b.token_ids, b.k, b.xbuf, b.ws)
-    B.moe_expert_ffn(b.xbuf, b.offsets, inp["W1"], inp["W3"], inp["W2"], b.ybuf, b.h1, b.h3, b.a, b.ws)
+    if b.fused:
+        B.moe_expert_ffn_gather(inp["x"], b.token_ids, b.offsets, inp["W1"], inp["W3"], inp["W2"], b.ybuf,
+                                b.h1, b.h3, b.a, b.ws)
+    else:
+        B.moe_dispatch(inp["x"], b.token_ids, b.k, b.xbuf, b.ws)
+        B.moe_expert_ffn(b.xbuf, b.offsets, inp["W1"], inp["W3"], inp["W2"], b.ybuf, b.h1, b.h3, b.a, b.ws)
     B.moe_combine(b.ybuf, b.slot_of, b.topk_w, b.y, b.ws)
     return b.y
 
@@ -65,8 +84,12 @@ def forward(inp: dict, b: LayerBuffers):
 def backward(inp: dict, dy: torch.Tensor, b: LayerBuffers):
     """Combine bwd -> experts bwd -> gate bwd -> dispatch bwd.  Returns b.dx."""
     B.moe_combine_bwd(dy, b.ybuf, b.slot_of, b.topk_w, b.dybuf, b.d_topk_w, b.ws)
-    B.moe_expert_ffn_bwd(b.dybuf, b.xbuf, b.h1, b.h3, b.a, b.offsets, inp["W1"], inp["W3"], inp["W2"],
-                         b.dxbuf, b.dW1, b.dW3, b.dW2, b.ws)
+    if b.fused:
+        B.moe_expert_ffn_bwd_gather(b.dybuf, inp["x"], b.token_ids, b.h1, b.h3, b.a, b.offsets, inp["W1"],
+                                    inp["W3"], inp["W2"], b.dxbuf, b.dW1, b.dW3, b.dW2, b.ws)
+    else:
+        B.moe_expert_ffn_bwd(b.dybuf, b.xbuf, b.h1, b.h3, b.a, b.offsets, inp["W1"], inp["W3"], inp["W2"],
+                             b.dxbuf, b.dW1, b.dW3, b.dW2, b.ws)
     B.moe_route_bwd(inp["x"], inp["Wg"], b.probs, b.topk_idx, b.d_topk_w, b.d_logits, b.dWg,
                     b.dx_router, b.ws, gate=b.gate, renorm=b.renorm)
     B.moe_dispatch_bwd(b.dxbuf, b.slot_of, b.dx_router, b.k, b.dx, b.ws)

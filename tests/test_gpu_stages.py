@@ -489,3 +489,61 @@ def test_expert_ffn_forward_and_backward(B, T, h, E, k, f, dt, skew):
     for e in empty:
         assert (np64(dW1[e]) == 0).all() and (np64(dW2[e]) == 0).all()
     assert B.moe_check_status(ws) == 0
+
+
+GATHER_SHAPES = [s for s in EXPERT_SHAPES if s[5] == torch.bfloat16 and s[1] % 128 == 0 and s[4] % 128 == 0]
+
+
+@pytest.mark.parametrize("bad_id", [False, True])
+@pytest.mark.parametrize("T,h,E,k,f,dt,skew", GATHER_SHAPES)
+def test_gathered_expert_ffn_equals_dispatch_then_ffn(B, T, h, E, k, f, dt, skew, bad_id):
+    """The expert GEMMs that gather their token rows from x give the same bits as dispatching
+    xbuf first, forward and backward; an out-of-range token id reads as a zero row and sets the
+    status bit on both paths."""
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    assert B.moe_expert_ffn_gather_supported(h, f, dt)
+    p, d = expert_inputs(T, h, E, k, f, dt, 70 + T, skew)
+    Tk = T * k
+    x = random_tensor((T, h), 90 + T, dt, "cuda")
+    tok = torch.from_numpy(p["token_ids"]).cuda()
+    if bad_id:
+        tok[Tk // 2] = T + 3
+    z = lambda *s: torch.empty(*s, dtype=dt, device="cuda")  # noqa: E731
+    outs = []
+    for gathered in (False, True):
+        ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, dt)
+        ybuf, h1, h3, a = z(Tk, h), z(Tk, f), z(Tk, f), z(Tk, f)
+        dxbuf, dW1, dW3, dW2 = z(Tk, h), z(E, h, f), z(E, h, f), z(E, f, h)
+        if gathered:
+            B.moe_expert_ffn_gather(x, tok, d["offsets"], d["W1"], d["W3"], d["W2"], ybuf, h1, h3, a, ws)
+            B.moe_expert_ffn_bwd_gather(d["dybuf"], x, tok, h1, h3, a, d["offsets"], d["W1"], d["W3"], d["W2"],
+                                        dxbuf, dW1, dW3, dW2, ws)
+        else:
+            xbuf = z(Tk, h)
+            B.moe_dispatch(x, tok, k, xbuf, ws)
+            B.moe_expert_ffn(xbuf, d["offsets"], d["W1"], d["W3"], d["W2"], ybuf, h1, h3, a, ws)
+            B.moe_expert_ffn_bwd(d["dybuf"], xbuf, h1, h3, a, d["offsets"], d["W1"], d["W3"], d["W2"],
+                                 dxbuf, dW1, dW3, dW2, ws)
+        torch.cuda.synchronize()
+        status = B.moe_check_status(ws)
+        assert status == (B.MOE_STATUS_BAD_INDEX if bad_id else 0)
+        outs.append({"ybuf": ybuf, "h1": h1, "h3": h3, "a": a, "dxbuf": dxbuf, "dW1": dW1, "dW3": dW3,
+                     "dW2": dW2})
+    for n, t in outs[0].items():
+        assert torch.equal(outs[1][n], t), n
+
+
+def test_gathered_expert_ffn_rejects_the_simt_engine(B):
+    """fp32 (FMA engine) has no gathered form: the call reports MOE_ERR_UNSUPPORTED."""
+    assert not B.moe_expert_ffn_gather_supported(256, 256, torch.float32)
+    assert not B.moe_expert_ffn_gather_supported(256, 192, torch.bfloat16)
+    T, h, E, k, f = 16, 256, 4, 2, 256
+    x = torch.zeros(T, h, device="cuda")
+    tok = torch.zeros(T * k, dtype=torch.int32, device="cuda")
+    off = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    W = torch.zeros(E, h, f, device="cuda")
+    o = torch.zeros(T * k, h, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, torch.float32)
+    with pytest.raises(B.MoEError):
+        B.moe_expert_ffn_gather(x, tok, off, W, W, W.transpose(1, 2).contiguous(), o, o, o, o, ws)
