@@ -306,7 +306,7 @@ def kernel_names(stage, n, w):
 
 
 def kernel_counts(w, T, e_active, binding=None):
-    """Algorithmic FLOPs and HBM bytes of one launch of each kernel (DESIGN.md section 5)."""
+    """Algorithmic FLOPs and HBM bytes of one launch of each kernel."""
     s = 2 if w.dtype == "bf16" else 4
     h, E, k, f = w.h, w.E, w.k, w.f
     Tk = T * k
