@@ -2,7 +2,7 @@
 //
 // All four are row gathers: every row of h elements moves as 16-byte vectors, a group of
 // `tpr` threads per row (tpr is a power of two, 32..256, chosen so each thread handles at
-// most four vectors per pass; rows wider than 256 x 4 vectors take several passes),
+// most two vectors per pass; rows wider than 256 x 2 vectors take several passes),
 // `256 / tpr` rows per 256-thread block.  Loads are issued before the dependent stores, and
 // the k-way gathers issue the loads of four source rows before summing any of them, so that
 // each thread keeps several 16-byte requests in flight.  Sums run in fp32 in a fixed order
@@ -15,7 +15,7 @@ namespace moe {
 namespace {
 
 constexpr int kBlock = 256;
-constexpr int kMaxVecPerThread = 4;
+constexpr int kMaxVecPerThread = 2;
 // The k-way gathers (combine, dispatch backward) issue the loads of kJB source rows before
 // consuming any, with at most kGatherVec vectors per thread per row, so each thread keeps
 // kJB * kGatherVec 16-byte loads in flight.
