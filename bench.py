@@ -299,7 +299,7 @@ def kernel_names(stage, n, w):
         "dispatch_bwd": (["dispatch_bwd"], CSRC + "gather.cu"),
     }
     names, src = table[stage]
-    if stage == "dispatch" and n == 0:  # folded into the expert GEMMs
+    if stage in ("dispatch", "combine") and n == 0:  # folded into the expert GEMMs
         return [], src
     assert len(names) == n, (stage, n, names)
     return names, src
@@ -366,7 +366,7 @@ def run_ours(args, w):
     T = w.T
     inp = workloads.make_inputs(w, device, token_seed=None if world == 1 else w.seed + 7919 * rank)
     b = layer.LayerBuffers(T, w.h, w.E, w.k, w.f, w.torch_dtype(), device, backward=w.backward,
-                           fused=args.fused)
+                           fused=args.fused, fold_combine=args.fold_combine)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)  # 2x the 129 MB L2
     stream = torch.cuda.current_stream()
 
@@ -381,11 +381,16 @@ def run_ours(args, w):
             # fused: no dispatch call; the gate/up GEMM gathers its token rows from x
             (lambda: None) if b.fused else
             (lambda: binding.moe_dispatch(inp["x"], b.token_ids, w.k, b.xbuf, b.ws)),
+            (lambda: binding.moe_expert_ffn_fused(b.xbuf, inp["x"], b.token_ids, b.slot_of, b.topk_w, b.offsets,
+                                                  inp["W1"], inp["W3"], inp["W2"], b.ybuf, b.h1, b.h3, b.a,
+                                                  b.y, b.ws)) if b.fold_combine else
             (lambda: binding.moe_expert_ffn_gather(inp["x"], b.token_ids, b.offsets, inp["W1"], inp["W3"],
                                                    inp["W2"], b.ybuf, b.h1, b.h3, b.a, b.ws)) if b.fused else
             (lambda: binding.moe_expert_ffn(b.xbuf, b.offsets, inp["W1"], inp["W3"], inp["W2"],
                                             b.ybuf, b.h1, b.h3, b.a, b.ws)),
-            lambda: binding.moe_combine(b.ybuf, b.slot_of, b.topk_w, b.y, b.ws),
+            # fold_combine: the down projection already wrote y
+            (lambda: None) if b.fold_combine else
+            (lambda: binding.moe_combine(b.ybuf, b.slot_of, b.topk_w, b.y, b.ws)),
         ]
         if w.backward:
             calls += [
@@ -474,7 +479,7 @@ def run_ours(args, w):
     for n, ms in stage_ms.items():
         avg = sum(ms) / len(ms)
         c = counts[n]
-        if b.fused and n == "dispatch":
+        if (b.fused and n == "dispatch") or (b.fold_combine and n == "combine"):
             stages[n] = {"ms": round(avg, 4), "GB/s": None, "note": "no launch: folded into the expert GEMMs"}
             continue
         stages[n] = {"ms": round(avg, 4), "GB/s": round(c["bytes"] / (avg * 1e-3) / 1e9, 1)}
@@ -583,7 +588,7 @@ def run_ours(args, w):
             "dtype": w.dtype, "data": "synthetic (seeded N(0,1) tokens, random-init weights)",
             "tokens_per_s": world * T / (ms_per_step * 1e-3),
             "dispatch_GBps": None if b.fused else stages["dispatch"]["GB/s"],
-            "combine_GBps": stages["combine"]["GB/s"],
+            "combine_GBps": None if b.fold_combine else stages["combine"]["GB/s"],
             "config": {"workload": workload_desc(w), "tokens_per_gpu": T,
                        "l2": "flushed between timed steps (256 MB write, outside the step events)",
                        "step": ("one host call per stage" if args.no_graph else
@@ -591,6 +596,8 @@ def run_ours(args, w):
                        "breakdown": "stages and kernels timed in a second pass with an event after each launch",
                        "dispatch": ("folded into the gate/up and dW1/dW3 GEMMs (rows gathered from x)"
                                     if b.fused else "its own kernel writing the padding-free buffer"),
+                       "combine": ("folded into the down projection's epilogue" if b.fold_combine
+                                   else "its own kernel over ybuf"),
                        "parallelism": f"replicas x{world} (independent tokens, no data-path collective)"},
             "stages": stages,
             "kernels": kernels,
@@ -618,6 +625,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fused", action="store_true",
                     help="fold dispatch into the expert GEMMs (bf16 tensor-core path; rows gathered from x)")
+    ap.add_argument("--fold-combine", action="store_true",
+                    help="fold the combine into the down projection (bf16 tensor-core path, h % 256 == 0)")
     ap.add_argument("--no-graph", action="store_true",
                     help="time steps as one host call per stage instead of a CUDA graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")

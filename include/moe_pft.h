@@ -258,6 +258,25 @@ int moe_expert_ffn_bwd_gather(const void* dybuf, const void* x, const int32_t* t
 int moe_expert_ffn_gather_supported(int h, int f, int dtype);
 
 /*
+ * The fused single-GPU forward of FlashDMoE's blog (§5: one kernel gathers its tokens and
+ * combines its results): moe_expert_ffn with the dispatch and/or the combine folded in.
+ * xbuf non-NULL: the gate/up GEMM reads xbuf; xbuf NULL: it gathers row p as x[token_ids[p]]
+ * (as moe_expert_ffn_gather).  y non-NULL: the down projection also writes
+ *   y[t,:] = sum_j topk_w[t,j] * ybuf[slot_of[t*k+j],:]
+ * bit for bit as moe_combine does (j ascending, fp32, one rounding); the unit that completes
+ * token t's k rows of a 128-row tile of h sums that tile (contribution counters in the
+ * workspace, zeroed by the call).  ybuf is written either way.
+ * token_ids: [Tk] and slot_of: [Tk] int32 from moe_pft_build; topk_w: [T,k] fp32; Tk == T*k.
+ * Tensor-core engine only (bf16, h and f multiples of 128); the combine fold also needs
+ * h % 256 == 0; otherwise MOE_ERR_UNSUPPORTED.  The workspace (16-byte aligned) needs
+ * moe_workspace_size(MOE_OP_EXPERT_FFN, ...) bytes and, with y, at least 256 + 4*T*(h/128).
+ */
+int moe_expert_ffn_fused(const void* xbuf, const void* x, const int32_t* token_ids, int T, int k,
+                         const int32_t* slot_of, const float* topk_w, const int32_t* offsets, const void* W1,
+                         const void* W3, const void* W2, int Tk, int E, int h, int f, int dtype, void* ybuf,
+                         void* h1, void* h3, void* a, void* y, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Combine -- X-MoE review §3 "Training pipeline" step 6 and the FlashDMoE blog §1.1 (results
  * return to the origin and are merged with the gate weights):
  *   y[t,:] = sum_{j=0..k-1} topk_w[t,j] * ybuf[slot_of[t*k+j],:], j ascending, fp32, rounded once.

@@ -49,6 +49,8 @@ SIGNATURES = {
     "moe_expert_ffn_bwd_gather": (_I, [_P, _P, _P, _I, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I,
                                        _P, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_ffn_gather_supported": (_I, [_I, _I, _I]),
+    "moe_expert_ffn_fused": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P,
+                                  _P, _P, _Z, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
 }
@@ -246,6 +248,19 @@ def moe_expert_ffn_bwd_gather(dybuf, x, token_ids, h1, h3, a, offsets, W1, W3, W
 def moe_expert_ffn_gather_supported(h: int, f: int, dtype: torch.dtype) -> bool:
     code = MOE_BF16 if dtype == torch.bfloat16 else MOE_F32
     return bool(lib().moe_expert_ffn_gather_supported(h, f, code))
+
+
+def moe_expert_ffn_fused(xbuf, x, token_ids, slot_of, topk_w, offsets, W1, W3, W2, ybuf, h1, h3, a, y, ws):
+    """Expert FFN with the dispatch (xbuf None: rows gathered from x) and/or the combine (y not
+    None) folded into its GEMMs."""
+    T, k = topk_w.shape
+    Tk = token_ids.shape[0]
+    E, h, f = W1.shape
+    dt = (xbuf if xbuf is not None else x).dtype
+    code = MOE_BF16 if dt == torch.bfloat16 else MOE_F32
+    _call("moe_expert_ffn_fused", _p(xbuf), _p(x), _p(token_ids), T, k, _p(slot_of), _p(topk_w), _p(offsets),
+          _p(W1), _p(W3), _p(W2), Tk, E, h, f, code, _p(ybuf), _p(h1), _p(h3), _p(a), _p(y), _p(ws), ws.numel(),
+          _stream())
 
 
 def moe_combine(ybuf, slot_of, topk_w, y, ws):

@@ -294,7 +294,7 @@ namespace {
 
 int expert_ffn_impl(const char* fn, TokenRows xr, const int32_t* offsets, const void* W1, const void* W3,
                     const void* W2, int Tk, int E, int h, int f, int dtype, void* ybuf, void* h1, void* h3,
-                    void* a, void* ws, size_t ws_bytes, cudaStream_t st) {
+                    void* a, void* ws, size_t ws_bytes, cudaStream_t st, const CombineFold* fold = nullptr) {
   REQUIRE(Tk >= 0 && E >= 1 && E <= 1024 && h >= 8 && f >= 8, MOE_ERR_INVALID_ARG,
           "moe_expert_ffn: need Tk >= 0, 1 <= E <= 1024, h >= 8, f >= 8");
   REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_expert_ffn: bad dtype");
@@ -312,7 +312,7 @@ int expert_ffn_impl(const char* fn, TokenRows xr, const int32_t* offsets, const 
   REQUIRE_PTR(offsets); REQUIRE_PTR(W1); REQUIRE_PTR(W3); REQUIRE_PTR(W2);
   REQUIRE_PTR(ybuf); REQUIRE_PTR(h1); REQUIRE_PTR(h3); REQUIRE_PTR(a);
   if (use_tensor_cores(dtype, h, f)) {
-    if (tc_expert_ffn(xr, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, status_of(ws), st) != 0)
+    if (tc_expert_ffn(xr, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, status_of(ws), st, fold) != 0)
       return tc_failure(fn);
   } else {
     simt_expert_ffn(dtype, xr.xbuf, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, st);
@@ -398,6 +398,29 @@ int moe_expert_ffn_bwd_gather(const void* dybuf, const void* x, const int32_t* t
   return expert_ffn_bwd_impl("moe_expert_ffn_bwd_gather", dybuf, TokenRows{nullptr, x, token_ids, T}, h1, h3,
                              a, offsets, W1, W3, W2, Tk, E, h, f, dtype, dxbuf, dW1, dW3, dW2, ws, ws_bytes,
                              (cudaStream_t)stream);
+}
+
+int moe_expert_ffn_fused(const void* xbuf, const void* x, const int32_t* token_ids, int T, int k,
+                         const int32_t* slot_of, const float* topk_w, const int32_t* offsets, const void* W1,
+                         const void* W3, const void* W2, int Tk, int E, int h, int f, int dtype, void* ybuf,
+                         void* h1, void* h3, void* a, void* y, void* ws, size_t ws_bytes, void* stream) {
+  const char* fn = "moe_expert_ffn_fused";
+  REQUIRE(T >= 1 && k >= 1 && (long long)T * k == Tk, MOE_ERR_INVALID_ARG, "moe_expert_ffn_fused: need Tk == T * k");
+  REQUIRE(use_tensor_cores(dtype, h, f), MOE_ERR_UNSUPPORTED,
+          "moe_expert_ffn_fused: needs the tensor-core engine (bf16, h and f multiples of 128)");
+  REQUIRE(y == nullptr || h % 256 == 0, MOE_ERR_UNSUPPORTED, "moe_expert_ffn_fused: the combine fold needs h % 256 == 0");
+  REQUIRE_PTR(token_ids);
+  CombineFold cf{};
+  if (y != nullptr) {
+    REQUIRE_PTR(slot_of); REQUIRE_PTR(topk_w);
+    const size_t need = sizeof(WsHeader) + (size_t)T * (h / 128) * sizeof(int);
+    REQUIRE(ws != nullptr && aligned16(ws) && ws_bytes >= need, MOE_ERR_WORKSPACE,
+            "moe_expert_ffn_fused: workspace too small for the combine counters");
+    cf = CombineFold{y, token_ids, slot_of, topk_w, T, k, reinterpret_cast<int*>(static_cast<char*>(ws) + sizeof(WsHeader))};
+  }
+  const TokenRows xr = xbuf != nullptr ? TokenRows{xbuf, nullptr, nullptr, 0} : TokenRows{nullptr, x, token_ids, T};
+  return expert_ffn_impl(fn, xr, offsets, W1, W3, W2, Tk, E, h, f, dtype, ybuf, h1, h3, a, ws, ws_bytes,
+                         (cudaStream_t)stream, y != nullptr ? &cf : nullptr);
 }
 
 int moe_expert_ffn_gather_supported(int h, int f, int dtype) {

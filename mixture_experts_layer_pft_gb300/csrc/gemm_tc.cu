@@ -124,6 +124,14 @@ struct TcParams {
   const int* gids;
   int gx_rows;
   int gx_ld;
+  // down projection with the combine folded in (paired M tiles): y[t, m] = sum_j w[t,j] ybuf[slot(t,j), m]
+  // is summed by the unit that completes token t's k rows of a 128-row M tile (c_cnt counts them)
+  __nv_bfloat16* c_y;  // null: no combine
+  const int* c_tok;    // token of each buffer row (the PFT's token_ids)
+  const int* c_slot;   // [T*k] buffer row of (t, j)
+  const float* c_w;    // [T*k] gate weights
+  int* c_cnt;          // [T * c_mt] contribution counters, zero at launch
+  int c_T, c_k, c_mt;  // tokens, top-k, 128-row M tiles per token row
 };
 
 // Logistic function for the bf16 epilogues: the fast exponential and division are accurate to a
@@ -206,6 +214,67 @@ __device__ __forceinline__ Unit decode(int u, const Sched& sc, const int* s_pref
   return w;
 }
 
+// ---------------------------------------------------------------------------- combine fold
+// Down projection with the combine folded in (kept out of line, away from the epilogue's
+// registers).  fold_count: count this unit's (token row, M tile) contributions; a cell reaching
+// k contributions joins this CTA's list.  fold_sum: one warp per listed cell sums the token's k
+// rows of that 128-row M tile from ybuf (read through L2), j ascending in fp32, one rounding,
+// as the combine kernel does.
+static __device__ __noinline__ void fold_count(const TcParams* pp, int row0, int ncols, int na, int tile0,
+                                               int et, int nthreads, int* own, int* nown) {
+  const TcParams& p = *pp;
+  for (int cq = et; cq < ncols * na; cq += nthreads) {
+    const int c = cq % ncols, tl = cq / ncols;
+    const int t = __ldg(p.c_tok + row0 + c);
+    if ((unsigned)t < (unsigned)p.c_T) {
+      const int cell = t * p.c_mt + tile0 + tl;
+      if (atomicAdd(p.c_cnt + cell, 1) == p.c_k - 1) own[atomicAdd(nown, 1)] = cell;
+    } else {
+      flag_status(p.status, MOE_STATUS_BAD_INDEX);
+    }
+  }
+}
+
+static __device__ __noinline__ void fold_sum(const TcParams* pp, const int* own, int nown, int ew, int nwarps,
+                                             int lane) {
+  const TcParams& p = *pp;
+  for (int i = ew; i < nown; i += nwarps) {
+    const int cell = own[i];
+    const int t = cell / p.c_mt;
+    const size_t m = (size_t)(cell % p.c_mt) * BM + 4 * lane;  // this lane's 4 outputs
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j0 = 0; j0 < p.c_k; j0 += 4) {
+      int sj[4];
+      float wj[4];
+      uint2 r[4];
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        sj[jj] = -1;
+        wj[jj] = 0.f;
+        if (j0 + jj < p.c_k) {
+          const int sl = __ldg(p.c_slot + (size_t)t * p.c_k + j0 + jj);
+          wj[jj] = __ldg(p.c_w + (size_t)t * p.c_k + j0 + jj);
+          if ((unsigned)sl < (unsigned)(p.c_T * p.c_k)) sj[jj] = sl;
+          else flag_status(p.status, MOE_STATUS_BAD_INDEX);
+        }
+      }
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj)
+        if (sj[jj] >= 0) r[jj] = __ldcg(reinterpret_cast<const uint2*>(p.out0 + (size_t)sj[jj] * p.ld_out + m));
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        if (sj[jj] < 0) continue;
+        acc[0] = fmaf(wj[jj], __uint_as_float(r[jj].x << 16), acc[0]);
+        acc[1] = fmaf(wj[jj], __uint_as_float(r[jj].x & 0xFFFF0000u), acc[1]);
+        acc[2] = fmaf(wj[jj], __uint_as_float(r[jj].y << 16), acc[2]);
+        acc[3] = fmaf(wj[jj], __uint_as_float(r[jj].y & 0xFFFF0000u), acc[3]);
+      }
+    }
+    *reinterpret_cast<uint2*>(p.c_y + (size_t)t * p.ld_out + m) =
+        make_uint2(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]));
+  }
+}
+
 // ---------------------------------------------------------------------------- the kernel
 
 template <int MODE>
@@ -224,6 +293,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
   __shared__ Sched s_sched;
   // epilogue transpose buffers: one 16-column x 32-row bf16 block per warp and output slot
   __shared__ __align__(128) __nv_bfloat16 s_stage[C::EPI_WARPS][C::NSLOT][C::CW][32];
+  // down projection with the combine folded in: (token, M tile) cells this CTA owns, per unit parity
+  constexpr int kOwn = (C::PAIR && C::BASE == DOWN) ? 2 * C::BN : 1;
+  __shared__ int s_own[2][kOwn];
+  __shared__ int s_nown[2];
+  __shared__ __align__(8) uint64_t comb_bar;  // the epilogue warps meet here
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   // stage ring aligned to 1024 bytes (the swizzle atom)
@@ -287,6 +361,9 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
     for (int s = 0; s < C::STAGES; ++s) { mbar_init(&full_bar[s], full_count); mbar_init(&empty_bar[s], 1); }
     for (int b = 0; b < C::ACC_BUFS; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], C::EPI_WARPS); }
     mbar_init(&drain_bar, 1);
+    mbar_init(&comb_bar, C::EPI_WARPS);
+    s_nown[0] = 0;
+    s_nown[1] = 0;
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -542,6 +619,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
     constexpr int G = C::EPI_WARPS / 4;  // warps per lane quarter
     __nv_bfloat16 (*stg)[C::CW][32] = s_stage[warp - 2];  // this warp's transpose buffers
     int slot = 0;  // weight gradients: the transpose slot of the next tensor store
+    uint32_t cph = 0;  // combine fold: phase of comb_bar
     int it = 0;
     for (int u = blockIdx.x; u < sc.total; u += gridDim.x, ++it) {
       const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
@@ -668,6 +746,27 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
             }
             __syncwarp();
           }
+        }
+        if (C::BASE == DOWN && p.c_y != nullptr) {
+          // Combine folded in.  Every epilogue thread fences its ybuf stores device-wide; after
+          // the warps meet, the contributions are counted, and after they meet again the cells
+          // this unit completed are summed (fold_count, fold_sum).
+          const int et = (warp - 2) * 32 + lane, ew = warp - 2;
+          const int par = it & 1;
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comb_bar);
+          if (!__all_sync(0xffffffffu, mbar_wait(&comb_bar, cph, &s_abort, p.status))) break;
+          cph ^= 1u;
+          fold_count(&p, w.row0, w.ncols, w.na, w.m0 / BM, et, C::EPI_WARPS * 32, s_own[par], &s_nown[par]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&comb_bar);
+          if (!__all_sync(0xffffffffu, mbar_wait(&comb_bar, cph, &s_abort, p.status))) break;
+          cph ^= 1u;
+          __threadfence();
+          const int nown = s_nown[par];
+          if (et == 0) s_nown[par ^ 1] = 0;  // the next unit's list; its readers are past this unit's meetings
+          fold_sum(&p, s_own[par], nown, ew, C::EPI_WARPS, lane);
         }
       } else {
       // a paired unit's two M tiles go out one after the other (accumulators at t0 and t0 + BN)
@@ -851,7 +950,9 @@ bool set_token_rows(TcParams* p, const TokenRows& xr, int Tk, int h) {
 }  // namespace
 
 int tc_expert_ffn(TokenRows xr, const int* offsets, const void* W1, const void* W3, const void* W2, int Tk,
-                  int E, int h, int f, void* ybuf, void* h1, void* h3, void* a, int* status, cudaStream_t st) {
+                  int E, int h, int f, void* ybuf, void* h1, void* h3, void* a, int* status, cudaStream_t st,
+                  const CombineFold* fold) {
+  if (fold != nullptr && h % 256 != 0) return -1;  // the fold lives in the paired down projection
   TcParams g = blank_params();
   bool ok = tc_make_map(&g.mapA0, W1, (long long)E * h, f, 64, 64) &&
             tc_make_map(&g.mapA1, W3, (long long)E * h, f, 64, 64) && set_token_rows(&g, xr, Tk, h);
@@ -867,6 +968,12 @@ int tc_expert_ffn(TokenRows xr, const int* offsets, const void* W1, const void* 
   if (!ok) return -1;
   d.offsets = offsets; d.E = E; d.M = h; d.K = f; d.a_rows = f;
   d.out0 = static_cast<__nv_bfloat16*>(ybuf); d.ld_out = h; d.status = status;
+  if (fold != nullptr) {
+    d.c_y = static_cast<__nv_bfloat16*>(fold->y);
+    d.c_tok = fold->token_ids; d.c_slot = fold->slot_of; d.c_w = fold->topk_w; d.c_cnt = fold->cnt;
+    d.c_T = fold->T; d.c_k = fold->k; d.c_mt = h / BM;
+    if (cudaMemsetAsync(fold->cnt, 0, (size_t)fold->T * (h / BM) * sizeof(int), st) != cudaSuccess) return -1;
+  }
   return h % 256 == 0 ? launch<DOWN_PAIR>(d, st) : launch<DOWN>(d, st);
 }
 

@@ -82,9 +82,19 @@ struct TokenRows {
   const int* token_ids;
   int T;
 };
+// The combine folded into the down projection (h % 256 == 0): y[t] from ybuf by the unit that
+// completes token t's k rows of each 128-row M tile; cnt is [T * h/128] int scratch.
+struct CombineFold {
+  void* y;
+  const int* token_ids;
+  const int* slot_of;
+  const float* topk_w;
+  int T, k;
+  int* cnt;
+};
 int tc_expert_ffn(TokenRows xr, const int* offsets, const void* W1, const void* W3, const void* W2,
                   int Tk, int E, int h, int f, void* ybuf, void* h1, void* h3, void* a, int* status,
-                  cudaStream_t st);
+                  cudaStream_t st, const CombineFold* fold = nullptr);
 int tc_expert_ffn_bwd(const void* dybuf, TokenRows xr, const void* h1, const void* h3, const void* a,
                       const int* offsets, const void* W1, const void* W3, const void* W2, int Tk, int E,
                       int h, int f, void* dxbuf, void* dW1, void* dW3, void* dW2, void* dh1, void* dh3,

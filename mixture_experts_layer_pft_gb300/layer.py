@@ -18,19 +18,23 @@ class LayerBuffers:
 
     With ``fused`` the expert GEMMs gather their token rows from x (the library's
     moe_expert_ffn_gather / moe_expert_ffn_bwd_gather: bf16, h and f multiples of 128), so the
-    dispatched buffer xbuf is never written and ``xbuf`` is None.  The results are the same bits
-    as the dispatched path.  The default is the dispatched path: the gathered loads, 16-byte
-    copies from one producer warp, keep too few bytes in flight to match the tensor loads of
-    a dispatched buffer.
+    dispatched buffer xbuf is never written and ``xbuf`` is None.  With ``fold_combine`` the down
+    projection also writes y (moe_expert_ffn_fused; h a multiple of 256), so no combine call
+    runs.  Either way the results are the same bits as the separate calls.  The defaults are
+    the separate calls: the gathered loads, 16-byte copies from one producer warp, keep too few
+    bytes in flight to match the tensor loads of a dispatched buffer.
     """
 
     def __init__(self, T: int, h: int, E: int, k: int, f: int, dtype: torch.dtype, device="cuda",
                  backward: bool = True, gate: str = "softmax", renorm: bool = False,
-                 fused: bool = False):
+                 fused: bool = False, fold_combine: bool = False):
         self.T, self.h, self.E, self.k, self.f, self.dtype = T, h, E, k, f, dtype
-        if fused and not B.moe_expert_ffn_gather_supported(h, f, dtype):
+        if (fused or fold_combine) and not B.moe_expert_ffn_gather_supported(h, f, dtype):
             raise ValueError("fused layer needs bf16 with h and f multiples of 128")
+        if fold_combine and h % 256 != 0:
+            raise ValueError("the combine fold needs h a multiple of 256")
         self.fused = bool(fused)
+        self.fold_combine = bool(fold_combine)
         self.gate, self.renorm = gate, renorm
         Tk = T * k
         f32, i32 = torch.float32, torch.int32
@@ -67,15 +71,21 @@ class LayerBuffers:
 
 def forward(inp: dict, b: LayerBuffers):
     """Gate -> PFT build -> dispatch -> experts -> combine (dispatch folded into the expert
-    GEMMs when b.fused).  Returns b.y."""
+    GEMMs when b.fused, combine folded into the down projection when b.fold_combine).
+    Returns b.y."""
     B.moe_route(inp["x"], inp["Wg"], inp.get("bias"), b.k, b.logits, b.probs, b.topk_idx, b.topk_w, b.ws,
                 gate=b.gate, renorm=b.renorm)
     B.moe_pft_build(b.topk_idx, b.E, b.num_ids, b.offsets, b.token_ids, b.expert_ids, b.slot_of, b.ws)
+    if not b.fused:
+        B.moe_dispatch(inp["x"], b.token_ids, b.k, b.xbuf, b.ws)
+    if b.fold_combine:
+        B.moe_expert_ffn_fused(b.xbuf, inp["x"], b.token_ids, b.slot_of, b.topk_w, b.offsets, inp["W1"],
+                               inp["W3"], inp["W2"], b.ybuf, b.h1, b.h3, b.a, b.y, b.ws)
+        return b.y
     if b.fused:
         B.moe_expert_ffn_gather(inp["x"], b.token_ids, b.offsets, inp["W1"], inp["W3"], inp["W2"], b.ybuf,
                                 b.h1, b.h3, b.a, b.ws)
     else:
-        B.moe_dispatch(inp["x"], b.token_ids, b.k, b.xbuf, b.ws)
         B.moe_expert_ffn(b.xbuf, b.offsets, inp["W1"], inp["W3"], inp["W2"], b.ybuf, b.h1, b.h3, b.a, b.ws)
     B.moe_combine(b.ybuf, b.slot_of, b.topk_w, b.y, b.ws)
     return b.y

@@ -271,19 +271,21 @@ def test_captured_step_replays_the_same_bits(M):
 
 @pytest.mark.parametrize("cfg", [1, 2])
 def test_fused_layer_equals_dispatched_layer(M, cfg):
-    """Dispatch folded into the expert GEMMs gives the same bits as the dispatched buffer."""
+    """Dispatch folded into the expert GEMMs, the combine folded into the down projection, or
+    both, give the same bits as the separate calls."""
     layer, workloads = M
     w = workloads.WORKLOADS[cfg]
     T = min(w.T, 2048)
     inp = workloads.make_inputs(w, "cuda", T=T)
     outs = []
-    for fused in (False, True):
-        b = layer.LayerBuffers(T, w.h, w.E, w.k, w.f, w.torch_dtype(), fused=fused)
+    for fused, fold in ((False, False), (True, False), (False, True), (True, True)):
+        b = layer.LayerBuffers(T, w.h, w.E, w.k, w.f, w.torch_dtype(), fused=fused, fold_combine=fold)
         assert b.fused == fused and (b.xbuf is None) == fused
         layer.step(inp, b)
         torch.cuda.synchronize()
         outs.append({n: getattr(b, n).clone() for n in ("ybuf", "h1", "h3", "a", "y", "dxbuf", "dW1", "dW3",
                                                         "dW2", "dWg", "dx")})
         del b
-    for n, t in outs[0].items():
-        assert torch.equal(outs[1][n], t), n
+    for o in outs[1:]:
+        for n, t in outs[0].items():
+            assert torch.equal(o[n], t), n

@@ -547,3 +547,49 @@ def test_gathered_expert_ffn_rejects_the_simt_engine(B):
     ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, torch.float32)
     with pytest.raises(B.MoEError):
         B.moe_expert_ffn_gather(x, tok, off, W, W, W.transpose(1, 2).contiguous(), o, o, o, o, ws)
+
+
+FOLD_SHAPES = [s for s in GATHER_SHAPES if s[1] % 256 == 0]
+
+
+@pytest.mark.parametrize("gathered", [False, True])
+@pytest.mark.parametrize("T,h,E,k,f,dt,skew", FOLD_SHAPES)
+def test_combine_folded_into_down_projection(B, T, h, E, k, f, dt, skew, gathered):
+    """moe_expert_ffn_fused with y: the down projection's epilogue writes the same y, bit for
+    bit, as moe_combine over its ybuf (and the same ybuf, h1, h3, a as moe_expert_ffn), with the
+    dispatch separate or folded in too."""
+    from mixture_experts_layer_pft_gb300.workloads import random_tensor
+
+    p, d = expert_inputs(T, h, E, k, f, dt, 110 + T, skew)
+    Tk = T * k
+    x = random_tensor((T, h), 120 + T, dt, "cuda")
+    tok = torch.from_numpy(p["token_ids"]).cuda()
+    slot = torch.from_numpy(p["slot_of"]).cuda()
+    w = torch.rand(T, k, generator=torch.Generator().manual_seed(T), dtype=torch.float32).cuda()
+    z = lambda *s: torch.empty(*s, dtype=dt, device="cuda")  # noqa: E731
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, dt)
+    xbuf = z(Tk, h)
+    B.moe_dispatch(x, tok, k, xbuf, ws)
+    want = {n: z(*sh) for n, sh in (("ybuf", (Tk, h)), ("h1", (Tk, f)), ("h3", (Tk, f)), ("a", (Tk, f)), ("y", (T, h)))}
+    B.moe_expert_ffn(xbuf, d["offsets"], d["W1"], d["W3"], d["W2"], want["ybuf"], want["h1"], want["h3"], want["a"], ws)
+    B.moe_combine(want["ybuf"], slot, w, want["y"], ws)
+    got = {n: torch.full_like(t, float("nan")) for n, t in want.items()}
+    for _ in range(2):  # the counters are zeroed by each call
+        B.moe_expert_ffn_fused(None if gathered else xbuf, x, tok, slot, w, d["offsets"], d["W1"], d["W3"],
+                               d["W2"], got["ybuf"], got["h1"], got["h3"], got["a"], got["y"], ws)
+        torch.cuda.synchronize()
+        for n in want:
+            assert torch.equal(got[n], want[n]), n
+    assert B.moe_check_status(ws) == 0
+
+
+def test_combine_fold_rejects_unsupported_shapes(B):
+    """The combine fold lives in the paired down projection: h % 256 != 0 is MOE_ERR_UNSUPPORTED."""
+    T, h, E, k, f = 16, 384, 4, 2, 128
+    dt = torch.bfloat16
+    z = lambda *s, d=dt: torch.zeros(*s, dtype=d, device="cuda")  # noqa: E731
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, dt)
+    with pytest.raises(B.MoEError):
+        B.moe_expert_ffn_fused(z(T * k, h), z(T, h), z(T * k, d=torch.int32), z(T * k, d=torch.int32),
+                               z(T, k, d=torch.float32), z(E + 1, d=torch.int32), z(E, h, f), z(E, h, f), z(E, f, h),
+                               z(T * k, h), z(T * k, f), z(T * k, f), z(T * k, f), z(T, h), ws)
