@@ -122,7 +122,9 @@ uint64_t moe_profile_count(void);
  *   sum.  The same gate flags must be passed to moe_route_bwd.
  * x: [T,h] dtype.  Wg: [h,E] fp32.  bias: [E] fp32 or NULL.  logits, probs: [T,E] fp32
  * (logits is an input when flags has MOE_ROUTE_FROM_LOGITS; x, Wg, bias may then be NULL).
- * topk_idx: [T,k] int32.  topk_w: [T,k] fp32.  Requires 1 <= k <= E <= 1024, h % 8 == 0.
+ * topk_idx: [T,k] int32.  topk_w: [T,k] fp32.  Requires 1 <= k <= E <= 1024, h % 8 == 0, and,
+ * when the logits are computed from x, E % 4 == 0 (16-byte rows of W_g); MOE_ERR_UNSUPPORTED
+ * otherwise.
  */
 int moe_route(const void* x, const float* Wg, const float* bias, int T, int h, int E, int k,
               int dtype, int flags, float* logits, float* probs, int32_t* topk_idx,

@@ -215,12 +215,12 @@ int moe_route_bwd(const void* x, const float* Wg, const float* probs, const int3
           "moe_route_bwd: h must be a multiple of 8 and E of 4");
   REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_ROUTE_BWD, T, h, E, k, 0, dtype),
           MOE_ERR_WORKSPACE, "moe_route_bwd: workspace too small");
-  REQUIRE_PTR(Wg); REQUIRE_PTR(dWg); REQUIRE_PTR(x);
-  if (T == 0) {
+  REQUIRE_PTR(Wg); REQUIRE_PTR(dWg);
+  if (T == 0) {  // no tokens: dW_g is exactly zero (x, like every [T, ...] array, may be empty)
     cudaMemsetAsync(dWg, 0, sizeof(float) * (size_t)h * E, st);
     return check_launch("moe_route_bwd");
   }
-  REQUIRE_PTR(probs); REQUIRE_PTR(topk_idx); REQUIRE_PTR(d_topk_w); REQUIRE_PTR(d_logits);
+  REQUIRE_PTR(x); REQUIRE_PTR(probs); REQUIRE_PTR(topk_idx); REQUIRE_PTR(d_topk_w); REQUIRE_PTR(d_logits);
   REQUIRE(dx_router == nullptr || aligned16(dx_router), MOE_ERR_INVALID_ARG,
           "moe_route_bwd: dx_router not aligned");
   REQUIRE(aligned16(ws), MOE_ERR_WORKSPACE, "moe_route_bwd: workspace not 16-byte aligned");

@@ -161,7 +161,8 @@ def test_full_size_layer_sampled(M, cfg, ntok, nexp):
 
 
 @pytest.mark.parametrize("T,h,E,k,f,dt", [(1, 128, 8, 2, 64, torch.float32), (5, 64, 4, 4, 16, torch.bfloat16),
-                                          (33, 72, 12, 12, 24, torch.float32), (17, 256, 4, 1, 128, torch.bfloat16)])
+                                          (33, 72, 12, 12, 24, torch.float32), (17, 256, 4, 1, 128, torch.bfloat16),
+                                          (300, 256, 4, 4, 256, torch.bfloat16)])  # k = E on the tensor cores
 def test_edge_case_layers(M, T, h, E, k, f, dt):
     layer, workloads = M
     w = workloads.Workload("edge", T, h, E, k, f, dtype_name(dt), False, True, 7)
@@ -289,3 +290,21 @@ def test_fused_layer_equals_dispatched_layer(M, cfg):
     for o in outs[1:]:
         for n, t in outs[0].items():
             assert torch.equal(o[n], t), n
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_empty_batch_layer(M, dt):
+    """A step over zero tokens runs every stage, leaves nothing to route or combine and gives
+    exactly zero weight gradients."""
+    layer, workloads = M
+    w = workloads.Workload("empty", 0, 256, 8, 2, 256, dtype_name(dt), False, True, 9)
+    inp = workloads.make_inputs(w, "cuda")
+    b = layer.LayerBuffers(0, w.h, w.E, w.k, w.f, dt)
+    for n in ("dW1", "dW3", "dW2", "dWg"):
+        getattr(b, n).fill_(1.0)
+    layer.step(inp, b)
+    torch.cuda.synchronize()
+    assert b.y.shape == (0, w.h) and b.dx.shape == (0, w.h)
+    assert int(b.offsets.abs().sum()) == 0 and int(b.num_ids.abs().sum()) == 0
+    for n in ("dW1", "dW3", "dW2", "dWg"):
+        assert int(torch.count_nonzero(getattr(b, n))) == 0, n
