@@ -299,11 +299,11 @@ int expert_ffn_impl(const char* fn, TokenRows xr, const int32_t* offsets, const 
           "moe_expert_ffn: need Tk >= 0, 1 <= E <= 1024, h >= 8, f >= 8");
   REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_expert_ffn: bad dtype");
   REQUIRE(h % 8 == 0 && f % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_expert_ffn: h and f must be multiples of 8");
-  REQUIRE(xr.xbuf != nullptr || use_tensor_cores(dtype, h, f), MOE_ERR_UNSUPPORTED,
-          "moe_expert_ffn_gather: needs the tensor-core engine (bf16, h and f multiples of 128)");
   REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_EXPERT_FFN, Tk, h, E, 1, f, dtype),
           MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace too small");
   if (Tk == 0) return MOE_OK;
+  REQUIRE(xr.xbuf != nullptr || use_tensor_cores(dtype, h, f), MOE_ERR_UNSUPPORTED,
+          "moe_expert_ffn_gather: needs the tensor-core engine (bf16, h and f multiples of 128)");
   if (xr.xbuf == nullptr) {
     REQUIRE(xr.T >= 1, MOE_ERR_INVALID_ARG, "moe_expert_ffn_gather: need T >= 1");
     REQUIRE((long long)xr.T * h < (1LL << 31), MOE_ERR_UNSUPPORTED, "moe_expert_ffn_gather: T * h >= 2^31");
@@ -328,8 +328,6 @@ int expert_ffn_bwd_impl(const char* fn, const void* dybuf, TokenRows xr, const v
           "moe_expert_ffn_bwd: need Tk >= 0, 1 <= E <= 1024, h >= 8, f >= 8");
   REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_expert_ffn_bwd: bad dtype");
   REQUIRE(h % 8 == 0 && f % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_expert_ffn_bwd: h and f must be multiples of 8");
-  REQUIRE(xr.xbuf != nullptr || use_tensor_cores(dtype, h, f), MOE_ERR_UNSUPPORTED,
-          "moe_expert_ffn_bwd_gather: needs the tensor-core engine (bf16, h and f multiples of 128)");
   REQUIRE(ws != nullptr && aligned16(ws) &&
               ws_bytes >= moe_workspace_size(MOE_OP_EXPERT_FFN_BWD, Tk, h, E, 1, f, dtype),
           MOE_ERR_WORKSPACE, "moe_expert_ffn_bwd: workspace too small");
@@ -341,6 +339,8 @@ int expert_ffn_bwd_impl(const char* fn, const void* dybuf, TokenRows xr, const v
     cudaMemsetAsync(dW2, 0, wb, st);
     return check_launch(fn);
   }
+  REQUIRE(xr.xbuf != nullptr || use_tensor_cores(dtype, h, f), MOE_ERR_UNSUPPORTED,
+          "moe_expert_ffn_bwd_gather: needs the tensor-core engine (bf16, h and f multiples of 128)");
   if (xr.xbuf == nullptr) {
     REQUIRE(xr.T >= 1, MOE_ERR_INVALID_ARG, "moe_expert_ffn_bwd_gather: need T >= 1");
     REQUIRE((long long)xr.T * h < (1LL << 31), MOE_ERR_UNSUPPORTED, "moe_expert_ffn_bwd_gather: T * h >= 2^31");
