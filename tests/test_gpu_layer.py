@@ -308,3 +308,51 @@ def test_empty_batch_layer(M, dt):
     assert int(b.offsets.abs().sum()) == 0 and int(b.num_ids.abs().sum()) == 0
     for n in ("dW1", "dW3", "dW2", "dWg"):
         assert int(torch.count_nonzero(getattr(b, n))) == 0, n
+
+
+def _random_layer_shapes(n, seed):
+    g = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        E = 4 * int(g.integers(1, 41))
+        out.append((int(g.choice([1, 7, 64, 129, 300, 513, 1000, 2047])), 128 * int(g.integers(1, 7)), E,
+                    int(g.integers(1, min(8, E) + 1)), 128 * int(g.integers(1, 7)), bool(g.random() < 0.4)))
+    return out
+
+
+@pytest.mark.parametrize("T,h,E,k,f,skew", _random_layer_shapes(24, 2024))
+def test_random_bf16_layers(M, T, h, E, k, f, skew):
+    """Seeded random shapes on the tensor-core path: the layer against the oracle (where the
+    routing is unique), and the gathered and combine-folded layers bit for bit against it."""
+    layer, workloads = M
+    w = workloads.Workload("random", T, h, E, k, f, "bf16", skew, True, T + h + E)
+    inp = workloads.make_inputs(w, "cuda")
+    b = layer.LayerBuffers(T, h, E, k, f, torch.bfloat16)
+    layer.step(inp, b)
+    torch.cuda.synchronize()
+    x, Wg = np64(inp["x"]), np64(inp["Wg"])
+    bias = None if inp["bias"] is None else np64(inp["bias"])
+    exact = O.router_logits(x, Wg, bias, "f64")
+    una = routing_checks(b, exact, k)
+    if una.all():
+        W1, W3, W2, dy = np64(inp["W1"]), np64(inp["W3"]), np64(inp["W2"]), np64(inp["dy"])
+        fw = O.layer_forward(x, Wg, W1, W3, W2, k, bias, "bf16")
+        bw = O.layer_backward(fw, x, Wg, W1, W3, W2, dy, "bf16")
+        assert rel_l2(np64(b.y), fw["y"]) <= TOL["bf16"]
+        for n in ("dx", "dW1", "dW3", "dW2", "dWg"):
+            assert rel_l2(np64(getattr(b, n)), bw[n]) <= TOL["bf16"], n
+    ref = {n: getattr(b, n).clone() for n in ("y", "dx", "dW1", "dW3", "dW2", "dWg")}
+    for fused, fold in [(True, False)] + ([(False, True), (True, True)] if h % 256 == 0 else []):
+        bf = layer.LayerBuffers(T, h, E, k, f, torch.bfloat16, fused=fused, fold_combine=fold)
+        layer.step(inp, bf)
+        torch.cuda.synchronize()
+        assert binding_status(bf) == 0
+        for n, t in ref.items():
+            assert torch.equal(getattr(bf, n), t), (fused, fold, n)
+    assert binding_status(b) == 0
+
+
+def binding_status(b):
+    from mixture_experts_layer_pft_gb300 import binding
+
+    return binding.moe_check_status(b.ws)
