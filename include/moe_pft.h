@@ -171,20 +171,23 @@ int moe_pft_build(const int32_t* topk_idx, int T, int E, int k, int32_t* num_ids
  * is fixed at start-up.  It computes exactly what moe_pft_build computes, from the same
  * arguments minus the workspace.  Its scratch is a 1 MiB array in the library's static device
  * memory, which every GPU that loads the library keeps until the process exits.
- *   - Limit: the scratch needed, moe_workspace_size(MOE_OP_PFT_BUILD, T, 0, E, k, 0, 0), must
- *     not exceed 1 MiB (1,048,576 bytes).  With E <= 431 every T*k the library accepts fits;
- *     with E = 1024, T*k up to 261,120.  Larger requests return MOE_ERR_UNSUPPORTED and
- *     moe_last_error() says why.
+ *   - Limits: T*k <= 2^30, as for moe_pft_build, and the scratch needed,
+ *     moe_workspace_size(MOE_OP_PFT_BUILD, T, 0, E, k, 0, 0), must not exceed 1 MiB
+ *     (1,048,576 bytes).  With E <= 431 every T*k up to 2^30 fits; with E = 1024, T*k up to
+ *     261,120.  Larger requests return MOE_ERR_UNSUPPORTED and moe_last_error() says why.
+ *     T = 0 (an empty batch) zero-fills num_ids and offsets, as moe_pft_build does.
  *   - No allocation: it calls no cudaMalloc, cudaFree or allocating library routine.  The first
  *     call on each device looks up the array's device address (with that device current); make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The address is kept per device together with
+ *     the id of the CUDA context it belongs to; after a device reset (a new primary context) the
+ *     next call looks it up again, so that call too should come before any stream capture.
  *   - Shared state: every call on a device uses the same array.  Each call clears the array's
  *     header (status word and counter) on `stream` before its kernels run, so calls queued one
  *     after another on one stream are safe; calls that overlap on the GPU (different streams,
  *     or different host threads without ordering) race and corrupt each other's results.
  *   - Errors: an expert id outside [0,E) is dropped and its slot_of entry set to -1, as in
  *     moe_pft_build; there is no status word to read back.
- * Requires T >= 1 and 1 <= k <= E <= 1024.
+ * Requires T >= 0 and 1 <= k <= E <= 1024.
  */
 int moe_pft_build_noalloc(const int32_t* topk_idx, int T, int E, int k, int32_t* num_ids,
                           int32_t* offsets, int32_t* token_ids, int32_t* expert_ids,

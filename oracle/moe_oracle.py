@@ -387,11 +387,3 @@ def layer_backward(fwd, x, Wg, W1, W3, W2, dy, dtype="f32"):
     out.update(rb)
     return out
 
-
-def layer_flops(T, h, E, k, f, backward=True):
-    """Algorithmic FLOPs of the layer: expert GEMMs (6 Tk h f forward, 12 Tk h f
-    backward) plus the router GEMMs (2 T h E forward, 4 T h E backward)."""
-    Tk = T * k
-    fwd = 6 * Tk * h * f + 2 * T * h * E
-    bwd = 12 * Tk * h * f + 4 * T * h * E
-    return fwd + (bwd if backward else 0)
