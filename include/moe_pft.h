@@ -110,6 +110,18 @@ int moe_profile_events(void* const* events, int capacity);
 /* Launches recorded since the current moe_profile_events installation. */
 uint64_t moe_profile_count(void);
 
+/* Test hook for the bounded waits of the tensor-core kernels (failure injected on the host; off
+ * unless called).  The next `launches` tcgen05 kernel launches (expert GEMMs and router GEMMs,
+ * in launch order, from any host thread) run with their TMA producer withholding the first
+ * pipeline stage of each CTA's first unit: the stage's barrier is never completed, so the MMA
+ * warp's wait for it can only end by running out.  The kernel then sets MOE_STATUS_TIMEOUT in
+ * the status word, every warp role unwinds, loads already in flight are given time to land, the
+ * tensor memory is released and the CTAs exit; the outputs of that launch are invalid.  Those
+ * launches wait at most `wait_limit_ns` (1 ms .. 2 s; 0 keeps the default of about 2 s) per wait.
+ * A CUDA graph captured while a request is pending keeps the hook in its launches.  Returns
+ * MOE_ERR_INVALID_ARG for a negative count or a limit outside that range; 0 launches cancels. */
+int moe_debug_withhold_stage(int launches, unsigned long long wait_limit_ns);
+
 /*
  * Gate -- X-MoE review §3 "Training pipeline" step 2 (padding-free gating, no dispatch_mask)
  * and the FlashDMoE blog §1.1 "DMoE operator definition" (each token picks a few experts).

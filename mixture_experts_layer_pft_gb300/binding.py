@@ -31,6 +31,7 @@ SIGNATURES = {
     "moe_kernel_launches": (ctypes.c_uint64, []),
     "moe_profile_events": (_I, [ctypes.POINTER(ctypes.c_void_p), _I]),
     "moe_profile_count": (ctypes.c_uint64, []),
+    "moe_debug_withhold_stage": (_I, [_I, ctypes.c_ulonglong]),
     "moe_last_error": (ctypes.c_char_p, []),
     "moe_workspace_size": (_Z, [_I, _I, _I, _I, _I, _I, _I]),
     "moe_status_reset": (_I, [_P, _P]),
@@ -158,6 +159,15 @@ def moe_check_status(ws) -> int:
     if rc not in (MOE_OK, MOE_ERR_DEVICE):
         raise MoEError("moe_check_status", rc, (lib().moe_last_error() or b"").decode())
     return code.value
+
+
+def moe_debug_withhold_stage(launches: int, wait_limit_ns: int = 0):
+    """Test hook: the next ``launches`` tensor-core kernel launches withhold their first pipeline
+    stage, so their bounded waits run out (after ``wait_limit_ns``; 0 = the default limit) and
+    they report MOE_STATUS_TIMEOUT.  ``launches=0`` cancels."""
+    rc = lib().moe_debug_withhold_stage(int(launches), int(wait_limit_ns))
+    if rc != MOE_OK:
+        raise MoEError("moe_debug_withhold_stage", rc, (lib().moe_last_error() or b"").decode())
 
 
 def gate_flags(gate: str = "softmax", renorm: bool = False) -> int:

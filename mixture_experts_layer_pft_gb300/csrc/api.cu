@@ -81,6 +81,22 @@ void count_launch(cudaStream_t st) {
 
 void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
 
+// moe_debug_withhold_stage: tcgen05 launches still to withhold a stage, and their wait limit.
+static std::atomic<int> g_withhold{0};
+static std::atomic<unsigned long long> g_withhold_wait_ns{0};
+
+bool debug_take_withhold(unsigned long long* wait_ns) {
+  *wait_ns = 0;
+  int n = g_withhold.load(std::memory_order_relaxed);
+  while (n > 0) {
+    if (g_withhold.compare_exchange_weak(n, n - 1, std::memory_order_relaxed)) {
+      *wait_ns = g_withhold_wait_ns.load(std::memory_order_relaxed);
+      return true;
+    }
+  }
+  return false;
+}
+
 int num_sms() {
   static int cached[64] = {0};
   int dev = 0;
@@ -116,6 +132,17 @@ int moe_profile_events(void* const* events, int capacity) {
 }
 
 uint64_t moe_profile_count(void) { return g_prof_count.load(std::memory_order_relaxed); }
+
+int moe_debug_withhold_stage(int launches, unsigned long long wait_limit_ns) {
+  if (launches < 0 || (launches > 0 && wait_limit_ns != 0 && wait_limit_ns < 1000000ull) ||
+      wait_limit_ns > 2000000000ull) {
+    set_last_error("moe_debug_withhold_stage: need launches >= 0 and a wait limit of 0 or 1 ms .. 2 s");
+    return MOE_ERR_INVALID_ARG;
+  }
+  g_withhold_wait_ns.store(wait_limit_ns, std::memory_order_relaxed);
+  g_withhold.store(launches, std::memory_order_relaxed);
+  return MOE_OK;
+}
 
 const char* moe_last_error(void) { return g_err; }
 

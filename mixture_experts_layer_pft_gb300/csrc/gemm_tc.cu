@@ -132,6 +132,10 @@ struct TcParams {
   const float* c_w;    // [T*k] gate weights
   int* c_cnt;          // [T * c_mt] contribution counters, zero at launch
   int c_T, c_k, c_mt;  // tokens, top-k, 128-row M tiles per token row
+  // bounded waits: limit per wait in ns (0: the default); withhold != 0 is the test hook of
+  // moe_debug_withhold_stage (the producer never fills the first stage of the first unit)
+  unsigned long long wait_ns;
+  int withhold;
 };
 
 // Logistic function for the bf16 epilogues: the fast exponential and division are accurate to a
@@ -417,9 +421,13 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
             for (int j = 0; j < NR; ++j)
               roff[j] = row_offset(k0 + lane + 32 * j, w.rows, w.row0 + k0 + lane + 32 * j);
           }
-          if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[s], ph ^ 1u, &s_abort, p.status))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[s], ph ^ 1u, &s_abort, p.status, p.wait_ns))) {
             ok = false;
             break;
+          }
+          if (p.withhold && u == (int)blockIdx.x && ks == 0) {  // test hook: a stage nobody fills
+            if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+            continue;
           }
           const uint32_t a_sm = ring + s * C::STAGE_BYTES;
           const uint32_t b_sm = a_sm + C::A_BYTES;
@@ -464,7 +472,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       }
       cp_async_wait<0>();  // no copy of this warp outlives it
       if (lane == 0) {
-        if (!ok) {
+        if (!ok || s_abort) {
           const unsigned long long t0 = globaltimer();
           while (globaltimer() - t0 < 2000000ull) {
           }
@@ -480,7 +488,11 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
         const int nbB = C::TOKEN_N ? (w.nmma + 63) / 64 : C::BN / 64;
         const uint32_t tx = (uint32_t)w.na * kATile + (uint32_t)nbB * kBox;
         for (int ks = 0; ks < w.nk; ++ks) {
-          if (!mbar_wait(&empty_bar[s], ph ^ 1u, &s_abort, p.status)) { ok = false; break; }
+          if (!mbar_wait(&empty_bar[s], ph ^ 1u, &s_abort, p.status, p.wait_ns)) { ok = false; break; }
+          if (p.withhold && u == (int)blockIdx.x && ks == 0) {  // test hook: a stage nobody fills
+            if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+            continue;
+          }
           mbar_expect_tx(&full_bar[s], tx);
           const uint32_t a_sm = ring + s * C::STAGE_BYTES;
           const uint32_t b_sm = a_sm + C::A_BYTES;
@@ -524,7 +536,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           if (++s == C::STAGES) { s = 0; ph ^= 1u; }
         }
       }
-      if (!ok) {
+      if (!ok || s_abort) {
         // give the loads already in flight (a few microseconds each) time to land
         const unsigned long long t0 = globaltimer();
         while (globaltimer() - t0 < 2000000ull) {
@@ -541,7 +553,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
       const int b = it % C::ACC_BUFS;
       const uint32_t aph = (uint32_t)(it / C::ACC_BUFS) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(&tempty_bar[b], aph ^ 1u, &s_abort, p.status))) { ok = false; break; }
+      if (!__all_sync(0xffffffffu, mbar_wait(&tempty_bar[b], aph ^ 1u, &s_abort, p.status, p.wait_ns))) { ok = false; break; }
       tc_fence_after();
       if (w.nk == 0) {  // an expert without rows (wgrad): nothing to multiply
         if (lane == 0) mbar_arrive(&tfull_bar[b]);
@@ -550,7 +562,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       const uint32_t idesc = idesc_bf16(w.nmma, C::A_MN, C::B_MN);
       const uint32_t d0 = tmem_base + (uint32_t)(b * C::NUM_A * C::BN);
       for (int ks = 0; ks < w.nk; ++ks) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], ph, &s_abort, p.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], ph, &s_abort, p.status, p.wait_ns))) { ok = false; break; }
         if ((C::GU || C::BASE == WGRAD13) && p.gx != nullptr) {
           // gathered rows were written by cp.async (generic proxy); the MMAs read them through
           // the async proxy
@@ -625,7 +637,7 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
       const Unit w = decode<MODE>(u, sc, s_pref, s_off, p);
       const int b = it % C::ACC_BUFS;
       const uint32_t aph = (uint32_t)(it / C::ACC_BUFS) & 1u;
-      if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[b], aph, &s_abort, p.status))) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[b], aph, &s_abort, p.status, p.wait_ns))) break;
       tc_fence_after();
       const uint32_t t0u = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * C::NUM_A * C::BN);
       const bool zero = (w.nk == 0);
@@ -756,12 +768,12 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
           __threadfence();
           __syncwarp();
           if (lane == 0) mbar_arrive(&comb_bar);
-          if (!__all_sync(0xffffffffu, mbar_wait(&comb_bar, cph, &s_abort, p.status))) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(&comb_bar, cph, &s_abort, p.status, p.wait_ns))) break;
           cph ^= 1u;
           fold_count(&p, w.row0, w.ncols, w.na, w.m0 / BM, et, C::EPI_WARPS * 32, s_own[par], &s_nown[par]);
           __syncwarp();
           if (lane == 0) mbar_arrive(&comb_bar);
-          if (!__all_sync(0xffffffffu, mbar_wait(&comb_bar, cph, &s_abort, p.status))) break;
+          if (!__all_sync(0xffffffffu, mbar_wait(&comb_bar, cph, &s_abort, p.status, p.wait_ns))) break;
           cph ^= 1u;
           __threadfence();
           const int nown = s_nown[par];
@@ -914,8 +926,10 @@ bool tc_make_map(CUtensorMap* m, const void* base, long long rows, long long col
 namespace {
 
 template <int MODE>
-int launch(const TcParams& p, cudaStream_t st) {
+int launch(const TcParams& p0, cudaStream_t st) {
   using C = Cfg<MODE>;
+  TcParams p = p0;
+  p.withhold = debug_take_withhold(&p.wait_ns) ? 1 : 0;
   const int smem = (int)(C::STAGES * C::STAGE_BYTES + 1024);
   if (cudaFuncSetAttribute(tc_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)

@@ -11,6 +11,10 @@ int num_sms();  // SM count of the current device (cached per device)
 // ring is installed (moe_profile_events), record its next event on `st`.
 void count_launch(cudaStream_t st);
 void set_last_error(const char* msg);  // the text moe_last_error() returns on this thread
+// Test hook behind moe_debug_withhold_stage: true when the tcgen05 launch being prepared must
+// withhold its first pipeline stage (one pending request is used up); *wait_ns gets the wait
+// limit for that launch (0: the default).
+bool debug_take_withhold(unsigned long long* wait_ns);
 
 // gather.cu
 void launch_dispatch(int dtype, const void* x, const int* token_ids, int T, int rows, int h,

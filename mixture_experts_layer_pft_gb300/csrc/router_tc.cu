@@ -67,6 +67,10 @@ struct RouterParams {
   float* out;       // z > 1: partials [z][M][N]; else the result [M][N]
   const float* bias;  // FWD with one slice: [N] added to the result (nullable)
   int* status;
+  // bounded waits: limit per wait in ns (0: the default); withhold != 0 is the test hook of
+  // moe_debug_withhold_stage (the producer never fills the first stage of the first unit)
+  unsigned long long wait_ns;
+  int withhold;
 };
 
 struct RUnit {
@@ -136,7 +140,11 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
         const int nbB = C::B_MN ? (w.ncols + 63) / 64 : 2;  // 64-column boxes per B plane
         const uint32_t tx = C::NA * kPlane + C::NB * (uint32_t)nbB * 8192u;
         for (int ks = 0; ks < w.nsteps; ++ks) {
-          if (!mbar_wait(&empty_bar[s], ph ^ 1u, &s_abort, p.status)) { ok = false; break; }
+          if (!mbar_wait(&empty_bar[s], ph ^ 1u, &s_abort, p.status, p.wait_ns)) { ok = false; break; }
+          if (p.withhold && u == (int)blockIdx.x && ks == 0) {  // test hook: a stage nobody fills
+            if (++s == C::STAGES) { s = 0; ph ^= 1u; }
+            continue;
+          }
           mbar_expect_tx(&full_bar[s], tx);
           const uint32_t a_sm = ring + s * C::STAGE_BYTES;
           const uint32_t b_sm = a_sm + C::NA * kPlane;
@@ -162,7 +170,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
           if (++s == C::STAGES) { s = 0; ph ^= 1u; }
         }
       }
-      if (!ok) {
+      if (!ok || s_abort) {  // give the loads already in flight time to land
         const unsigned long long t0 = globaltimer();
         while (globaltimer() - t0 < 2000000ull) {
         }
@@ -180,13 +188,13 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
       for (int c0 = 0; c0 < w.nsteps && ok; c0 += kChunkSteps, ++cc) {
         const int b = cc & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(&tempty_bar[b], ((uint32_t)(cc >> 1) & 1u) ^ 1u, &s_abort,
-                                               p.status))) { ok = false; break; }
+                                               p.status, p.wait_ns))) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_main = tmem_base + (uint32_t)(b * 2 * RBN);
         const uint32_t d_corr = d_main + RBN;
         const int c1 = min(w.nsteps, c0 + kChunkSteps);
         for (int ks = c0; ks < c1; ++ks) {
-          if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], ph, &s_abort, p.status))) { ok = false; break; }
+          if (!__all_sync(0xffffffffu, mbar_wait(&full_bar[s], ph, &s_abort, p.status, p.wait_ns))) { ok = false; break; }
           tc_fence_after();
           if (lane == 0) {
             const uint32_t a_sm = ring + s * C::STAGE_BYTES;
@@ -242,7 +250,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
       for (int i = 0; i < RBN; ++i) run[i] = 0.f;
       for (int c0 = 0; c0 < w.nsteps; c0 += kChunkSteps, ++cc) {
         const int b = cc & 1;
-        if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[b], (uint32_t)(cc >> 1) & 1u, &s_abort, p.status))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[b], (uint32_t)(cc >> 1) & 1u, &s_abort, p.status, p.wait_ns))) {
           ok = false;
           break;
         }
@@ -328,8 +336,10 @@ void pick_slices(int tiles, int K, int* kslice, int* z) {
 }
 
 template <int MODE>
-int rlaunch(const RouterParams& p, cudaStream_t st) {
+int rlaunch(const RouterParams& p0, cudaStream_t st) {
   using C = RCfg<MODE>;
+  RouterParams p = p0;
+  p.withhold = debug_take_withhold(&p.wait_ns) ? 1 : 0;
   const int smem = (int)(C::STAGES * C::STAGE_BYTES + 1024);
   if (cudaFuncSetAttribute(router_tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
       cudaSuccess)

@@ -42,17 +42,18 @@ __device__ __forceinline__ unsigned long long globaltimer() {
   return t;
 }
 
-// Wait for the phase of `bar` with parity `parity`.  Gives up after kWaitLimitNs or when
-// another role has already given up; then returns false.
+// Wait for the phase of `bar` with parity `parity`.  Gives up after `limit_ns` (0: kWaitLimitNs)
+// or when another role has already given up; then returns false.
 static __device__ __noinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                       int* status) {
+                                       int* status, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer();
+  const unsigned long long limit = limit_ns ? limit_ns : kWaitLimitNs;
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (globaltimer() - t0 > limit) {
         atomicOr(status, MOE_STATUS_TIMEOUT);
         *abort_flag = 1;
         return false;

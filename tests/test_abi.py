@@ -86,3 +86,15 @@ def test_argument_errors_return_before_any_launch(lib):
     r.argtypes = B.SIGNATURES["moe_route"][1]
     # k > E
     assert r(p, p, None, 4, 16, 8, 9, B.MOE_F32, 0, p, p, p, p, ws, 512, None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_withhold_hook_checks_its_arguments(lib):
+    from mixture_experts_layer_pft_gb300 import binding as B
+
+    fn = lib.moe_debug_withhold_stage
+    fn.restype = ctypes.c_int
+    fn.argtypes = B.SIGNATURES["moe_debug_withhold_stage"][1]
+    assert fn(-1, 0) == B.MOE_ERR_INVALID_ARG
+    assert fn(1, 1000) == B.MOE_ERR_INVALID_ARG  # below 1 ms
+    assert fn(1, 3_000_000_000) == B.MOE_ERR_INVALID_ARG  # above 2 s
+    assert fn(0, 0) == B.MOE_OK  # cancel: nothing pending
