@@ -77,8 +77,9 @@ def test_full_layer_small_workloads(M, cfg):
     exact = O.router_logits(x, Wg, bias, "f64")
     una = routing_checks(b, exact, w.k)
     assert rel_l2(np64(b.logits), fw["logits"]) <= TOL["f32"]
+    check_layer_against_oracle(b, fw, bw, una, npi(b.topk_idx), O.topk(exact, w.k), w.E, dn)
     if not una.all():
-        pytest.skip(f"{(~una).sum()} tokens with near-tied logits; covered by the sampled test")
+        pytest.skip(f"{(~una).sum()} tokens with near-tied logits: compared token by token above")
     for n in ("num_ids", "offsets", "token_ids", "expert_ids", "slot_of"):
         np.testing.assert_array_equal(npi(getattr(b, n)), fw[n], err_msg=n)
     if b.xbuf is not None:  # the fused layer never writes the dispatched buffer
@@ -95,54 +96,133 @@ def test_full_layer_small_workloads(M, cfg):
         assert rel_l2(np64(getattr(b, n)), bw[n]) <= TOL[dn], n
 
 
-def _sample(n, hi, seed):
+def _sample_unambiguous(n, una, seed):
+    """n unambiguous tokens in a seeded order, plus the first and last token when unambiguous."""
+    T = una.shape[0]
     g = np.random.default_rng(seed)
-    s = set(g.choice(hi, size=min(n, hi), replace=False).tolist()) | {0, hi - 1}
-    return np.array(sorted(s))
+    cand = [t for t in g.permutation(T) if una[t]][:n]
+    cand += [t for t in (0, T - 1) if una[t]]
+    return np.array(sorted(set(int(t) for t in cand)))
 
 
-@pytest.mark.parametrize("cfg,ntok,nexp", [(2, 6, 2), (3, 4, 2), (4, 16, 0), (5, 3, 1)])
-def test_full_size_layer_sampled(M, cfg, ntok, nexp):
-    _, workloads = M
-    w = workloads.WORKLOADS[cfg]
-    dn = w.dtype
-    inp, b = gpu_step(M, w)
+def oracle_token_rows(x_s, Wg, bias, W1, W3, W2, k, dn, dy_s=None):
+    """The oracle's layer on a token sample, stage by stage as layer_forward / layer_backward
+    compose it, with the expert backward run one expert at a time (so no E x h x f array of
+    weight gradients is allocated).  Every per-token output (y, dx, the token's buffer rows) depends
+    only on that token and the weights, so these rows equal the full layer's rows."""
+    E = W1.shape[0]
+    r = O.route(x_s, Wg, k, bias, dn)
+    pft = O.pft_build(r["topk_idx"], E)
+    xbuf = O.dispatch(x_s, pft["token_ids"])
+    ffn = O.expert_ffn(xbuf, pft["offsets"], W1, W3, W2, dn)
+    out = dict(r)
+    out.update(pft)
+    out.update(ffn)
+    out["xbuf"] = xbuf
+    out["y"] = O.combine(ffn["ybuf"], pft["slot_of"], r["topk_w"], dn)
+    if dy_s is None:
+        return out
+    dybuf, d_w = O.combine_bwd(dy_s, ffn["ybuf"], pft["slot_of"], r["topk_w"], dn)
+    off = pft["offsets"]
+    Tk_s, h = xbuf.shape
+    f = ffn["h1"].shape[1]
+    dxbuf, dh1, dh3 = np.zeros((Tk_s, h)), np.zeros((Tk_s, f)), np.zeros((Tk_s, f))
+    for e in np.nonzero(np.diff(off))[0]:
+        sl = slice(off[e], off[e + 1])
+        one = np.array([0, off[e + 1] - off[e]])
+        We = [LazyExperts(t.t[e:e + 1]) if isinstance(t, LazyExperts) else t[e:e + 1] for t in (W1, W3, W2)]
+        eb = O.expert_ffn_bwd(dybuf[sl], xbuf[sl], ffn["h1"][sl], ffn["h3"][sl], ffn["a"][sl], one, *We, dn)
+        dxbuf[sl], dh1[sl], dh3[sl] = eb["dxbuf"], eb["dh1"], eb["dh3"]
+    rb = O.route_bwd(x_s, Wg, r["probs"], r["topk_idx"], d_w, dn)
+    out.update({"dybuf": dybuf, "d_topk_w": d_w, "dxbuf": dxbuf, "dh1": dh1, "dh3": dh3,
+                "d_logits": rb["d_logits"], "dx_router": rb["dx_router"],
+                "dx": O.dispatch_bwd(dxbuf, pft["slot_of"], k, rb["dx_router"], dn)})
+    return out
+
+
+def take(t: torch.Tensor, idx) -> torch.Tensor:
+    """Rows idx (a numpy integer array) of a device tensor."""
+    return t[torch.as_tensor(np.asarray(idx, np.int64), device=t.device)]
+
+
+def assert_rows_close(got, want, tol, what):
+    """rel-L2 <= tol on every row on its own, so one wrong row cannot hide in a norm."""
+    got, want = np.atleast_2d(got), np.atleast_2d(want)
+    assert got.shape == want.shape, (what, got.shape, want.shape)
+    for i in range(got.shape[0]):
+        r = rel_l2(got[i], want[i])
+        assert r <= tol, (what, i, r)
+
+
+def check_sampled_tokens(b, inp, w, S, dn):
+    """GPU outputs on the token sample S (unambiguous tokens) against the oracle's rows."""
     x, Wg = np64(inp["x"]), np64(inp["Wg"])
     bias = None if inp["bias"] is None else np64(inp["bias"])
     W1, W3, W2 = LazyExperts(inp["W1"]), LazyExperts(inp["W3"]), LazyExperts(inp["W2"])
-    exact = O.router_logits(x, Wg, bias, "f64")
-    una = routing_checks(b, exact, w.k)
-    # invariants of the PFT arrays at full size
-    Tk = w.T * w.k
-    off = npi(b.offsets)
-    assert off[0] == 0 and off[-1] == Tk and (np.diff(off) == npi(b.num_ids)).all()
-    tok, slot, idx = npi(b.token_ids), npi(b.slot_of), npi(b.topk_idx)
-    assert (tok[slot] == np.repeat(np.arange(w.T), w.k)).all()
-    assert (npi(b.expert_ids)[slot] == idx.ravel()).all()
-
-    S = [t for t in _sample(ntok, w.T, cfg) if una[t]]
-    assert S, "no unambiguous sampled token"
-    fw = O.layer_forward(x[S], Wg, W1, W3, W2, w.k, bias, dn)
-    assert rel_l2(np64(b.y[S]), fw["y"]) <= TOL[dn]
-    assert rel_l2(np64(b.topk_w[S]), fw["topk_w"]) <= TOL["f32"]
-    if not w.backward:
+    dy_s = np64(take(inp["dy"], S)) if b.backward else None
+    o = oracle_token_rows(x[S], Wg, bias, W1, W3, W2, w.k, dn, dy_s)
+    np.testing.assert_array_equal(npi(take(b.topk_idx, S)), o["topk_idx"])
+    assert_rows_close(np64(take(b.y, S)), o["y"], TOL[dn], "y")
+    assert_rows_close(np64(take(b.topk_w, S)), o["topk_w"], TOL["f32"], "topk_w")
+    assert_rows_close(np64(take(b.probs, S)), o["probs"], TOL["f32"], "probs")
+    # the token's k buffer rows: GPU row slot_of[t*k+j] against the sample's row for (s, j)
+    g_rows = npi(b.slot_of).reshape(-1, w.k)[S].ravel()
+    o_rows = o["slot_of"]
+    np.testing.assert_array_equal(npi(b.token_ids)[g_rows], np.repeat(S, w.k))
+    np.testing.assert_array_equal(npi(b.expert_ids)[g_rows], o["expert_ids"][o_rows])
+    for n in ("h1", "h3", "a", "ybuf"):
+        assert_rows_close(np64(take(getattr(b, n), g_rows)), o[n][o_rows], TOL[dn], n)
+    if b.xbuf is not None:
+        np.testing.assert_array_equal(np64(take(b.xbuf, g_rows)), o["xbuf"][o_rows])
+    if not b.backward:
         return
-    dy = np64(inp["dy"])
-    bw = O.layer_backward(fw, x[S], Wg, W1, W3, W2, dy[S], dn)
-    assert rel_l2(np64(b.dx[S]), bw["dx"]) <= TOL[dn]
-    assert rel_l2(np64(b.d_topk_w[S]), bw["d_topk_w"]) <= TOL[dn]
+    assert_rows_close(np64(take(b.dx, S)), o["dx"], TOL[dn], "dx")
+    assert_rows_close(np64(take(b.dybuf, g_rows)), o["dybuf"][o_rows], TOL[dn], "dybuf")
+    assert_rows_close(np64(take(b.dxbuf, g_rows)), o["dxbuf"][o_rows], TOL[dn], "dxbuf")
+    # fp32 gate gradients carry ybuf's rounding in the layer's dtype (d_w = <dy, ybuf>)
+    assert rel_l2(np64(take(b.d_topk_w, S)), o["d_topk_w"]) <= TOL[dn]
+    assert rel_l2(np64(take(b.d_logits, S)), o["d_logits"]) <= TOL[dn]
+    assert rel_l2(np64(take(b.dx_router, S)), o["dx_router"]) <= TOL[dn]
 
-    # weight gradients of sampled experts whose token set is unambiguous
+
+def check_router_gemms_at_full_size(b, inp):
+    """The router GEMMs are fp32 sums of exact products: dW_g = x^T d_logits and the router's
+    part of dx = d_logits W_g^T, checked against the definition in fp64 on the GPU's own d_logits
+    (a property that holds at any size)."""
+    x, Wg, dl = np64(inp["x"]), np64(inp["Wg"]), np64(b.d_logits)
+    assert rel_l2(np64(b.dWg), x.T @ dl) <= TOL["f32"]
+    assert rel_l2(np64(b.dx_router), dl @ Wg.T) <= TOL["f32"]
+
+
+def unambiguous_experts(exact_idx, gpu_idx, una, E):
+    """Experts every one of whose tokens -- in the exact routing and in the GPU's -- is
+    unambiguous: their token sets are unique, so their weight gradients have one correct value."""
+    amb = ~una
+    touched_by_ambiguous = np.zeros(E, bool)
+    touched_by_ambiguous[exact_idx[amb].ravel()] = True
+    touched_by_ambiguous[gpu_idx[amb].ravel()] = True
+    used = np.bincount(exact_idx.ravel(), minlength=E) > 0
+    return np.nonzero(used & ~touched_by_ambiguous)[0]
+
+
+def check_sampled_experts(b, inp, w, exact, una, nexp, seed, dn):
+    """Weight gradients of nexp seeded experts whose token sets are unambiguous, each against the
+    oracle's single-expert forward and backward over exactly that expert's tokens."""
+    x, Wg = np64(inp["x"]), np64(inp["Wg"])
+    bias = None if inp["bias"] is None else np64(inp["bias"])
+    dy = np64(inp["dy"])
+    tok, off = npi(b.token_ids), npi(b.offsets)
     ex_idx = O.topk(exact, w.k)
-    counts = np.bincount(ex_idx.ravel(), minlength=w.E)
-    g = np.random.default_rng(100 + cfg)
+    eligible = unambiguous_experts(ex_idx, npi(b.topk_idx), una, w.E)
+    assert len(eligible) >= nexp // 2, f"only {len(eligible)} experts with unambiguous token sets"
+    nexp = min(nexp, len(eligible))
+    g = np.random.default_rng(seed)
     checked = 0
-    for e in g.permutation(np.nonzero(counts)[0]):
+    for e in g.permutation(eligible):
         toks = np.nonzero((ex_idx == e).any(axis=1))[0]
-        if not una[toks].all():
-            continue
         np.testing.assert_array_equal(tok[off[e]:off[e + 1]], toks)
-        wts = O.route(x[toks], Wg, w.k, bias, dn)["probs"][:, e]
+        r = O.route(x[toks], Wg, w.k, bias, dn)
+        wts = r["probs"][:, e]
         xe = x[toks]
         dyb = O.store(wts[:, None] * dy[toks], dn)
         one = np.array([0, len(toks)])
@@ -158,6 +238,37 @@ def test_full_size_layer_sampled(M, cfg, ntok, nexp):
     empty = np.nonzero(npi(b.num_ids) == 0)[0]
     for e in empty[:4]:
         assert (np64(b.dW1[e]) == 0).all() and (np64(b.dW2[e]) == 0).all()
+
+
+@pytest.mark.parametrize("cfg,ntok,nexp", [(2, 64, 16), (3, 64, 16), (4, 64, 0), (5, 64, 16)])
+def test_full_size_layer_sampled(M, cfg, ntok, nexp):
+    """The benchmark's full-size layers: 64 unambiguous tokens row by row (outputs, the tokens'
+    buffer rows, gate gradients), the router GEMMs against their definition, and the weight
+    gradients of 16 sampled experts."""
+    _, workloads = M
+    w = workloads.WORKLOADS[cfg]
+    dn = w.dtype
+    inp, b = gpu_step(M, w)
+    x, Wg = np64(inp["x"]), np64(inp["Wg"])
+    bias = None if inp["bias"] is None else np64(inp["bias"])
+    exact = O.router_logits(x, Wg, bias, "f64")
+    una = routing_checks(b, exact, w.k)
+    assert rel_l2(np64(b.logits), O.router_logits(x, Wg, bias, "f32")) <= TOL["f32"]
+    # invariants of the PFT arrays at full size
+    Tk = w.T * w.k
+    off = npi(b.offsets)
+    assert off[0] == 0 and off[-1] == Tk and (np.diff(off) == npi(b.num_ids)).all()
+    tok, slot, idx = npi(b.token_ids), npi(b.slot_of), npi(b.topk_idx)
+    assert (tok[slot] == np.repeat(np.arange(w.T), w.k)).all()
+    assert (npi(b.expert_ids)[slot] == idx.ravel()).all()
+
+    S = _sample_unambiguous(ntok, una, cfg)
+    assert len(S) >= ntok, f"only {len(S)} unambiguous sampled tokens"
+    check_sampled_tokens(b, inp, w, S, dn)
+    if not w.backward:
+        return
+    check_router_gemms_at_full_size(b, inp)
+    check_sampled_experts(b, inp, w, exact, una, nexp, 100 + cfg, dn)
 
 
 @pytest.mark.parametrize("T,h,E,k,f,dt", [(1, 128, 8, 2, 64, torch.float32), (5, 64, 4, 4, 16, torch.bfloat16),
@@ -320,10 +431,33 @@ def _random_layer_shapes(n, seed):
     return out
 
 
+def check_layer_against_oracle(v, fw, bw, una, gpu_idx, exact_idx, E, dn):
+    """A whole layer step against the oracle's full layer: every unambiguous token row by row
+    (y, dx and, with the token's own buffer rows, h1, h3, a, ybuf, dybuf, dxbuf), and every
+    expert whose token set is unambiguous (dW1, dW3, dW2); all of it when no token is ambiguous."""
+    S = np.nonzero(una)[0]
+    if len(S):
+        assert_rows_close(np64(take(v.y, S)), fw["y"][S], TOL[dn], "y")
+        assert_rows_close(np64(take(v.dx, S)), bw["dx"][S], TOL[dn], "dx")
+        k = gpu_idx.shape[1]
+        g_rows = npi(v.slot_of).reshape(-1, k)[S].ravel()
+        o_rows = fw["slot_of"].reshape(-1, k)[S].ravel()
+        for n in ("h1", "h3", "a", "ybuf"):
+            assert_rows_close(np64(take(getattr(v, n), g_rows)), fw[n][o_rows], TOL[dn], n)
+        for n in ("dybuf", "dxbuf"):
+            assert_rows_close(np64(take(getattr(v, n), g_rows)), bw[n][o_rows], TOL[dn], n)
+    for e in unambiguous_experts(exact_idx, gpu_idx, una, E):
+        for n in ("dW1", "dW3", "dW2"):
+            assert rel_l2(np64(getattr(v, n)[e]), bw[n][e]) <= TOL[dn], (n, e)
+    if una.all():
+        assert rel_l2(np64(v.dWg), bw["dWg"]) <= TOL[dn]
+
+
 @pytest.mark.parametrize("T,h,E,k,f,skew", _random_layer_shapes(24, 2024))
 def test_random_bf16_layers(M, T, h, E, k, f, skew):
-    """Seeded random shapes on the tensor-core path: the layer against the oracle (where the
-    routing is unique), and the gathered and combine-folded layers bit for bit against it."""
+    """Seeded random shapes on the tensor-core path: the layer, the gathered layer and the
+    combine-folded layers each against the oracle (unambiguous tokens and experts), and the
+    folded layers bit for bit against the layer with separate calls."""
     layer, workloads = M
     w = workloads.Workload("random", T, h, E, k, f, "bf16", skew, True, T + h + E)
     inp = workloads.make_inputs(w, "cuda")
@@ -334,19 +468,18 @@ def test_random_bf16_layers(M, T, h, E, k, f, skew):
     bias = None if inp["bias"] is None else np64(inp["bias"])
     exact = O.router_logits(x, Wg, bias, "f64")
     una = routing_checks(b, exact, k)
-    if una.all():
-        W1, W3, W2, dy = np64(inp["W1"]), np64(inp["W3"]), np64(inp["W2"]), np64(inp["dy"])
-        fw = O.layer_forward(x, Wg, W1, W3, W2, k, bias, "bf16")
-        bw = O.layer_backward(fw, x, Wg, W1, W3, W2, dy, "bf16")
-        assert rel_l2(np64(b.y), fw["y"]) <= TOL["bf16"]
-        for n in ("dx", "dW1", "dW3", "dW2", "dWg"):
-            assert rel_l2(np64(getattr(b, n)), bw[n]) <= TOL["bf16"], n
+    W1, W3, W2, dy = np64(inp["W1"]), np64(inp["W3"]), np64(inp["W2"]), np64(inp["dy"])
+    fw = O.layer_forward(x, Wg, W1, W3, W2, k, bias, "bf16")
+    bw = O.layer_backward(fw, x, Wg, W1, W3, W2, dy, "bf16")
+    gpu_idx, exact_idx = npi(b.topk_idx), O.topk(exact, k)
+    check_layer_against_oracle(b, fw, bw, una, gpu_idx, exact_idx, E, "bf16")
     ref = {n: getattr(b, n).clone() for n in ("y", "dx", "dW1", "dW3", "dW2", "dWg")}
     for fused, fold in [(True, False)] + ([(False, True), (True, True)] if h % 256 == 0 else []):
         bf = layer.LayerBuffers(T, h, E, k, f, torch.bfloat16, fused=fused, fold_combine=fold)
         layer.step(inp, bf)
         torch.cuda.synchronize()
         assert binding_status(bf) == 0
+        check_layer_against_oracle(bf, fw, bw, una, npi(bf.topk_idx), exact_idx, E, "bf16")
         for n, t in ref.items():
             assert torch.equal(getattr(bf, n), t), (fused, fold, n)
     assert binding_status(b) == 0

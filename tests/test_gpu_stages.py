@@ -251,6 +251,35 @@ def test_pft_build_bitexact(B, T, E, k, skew):
         np.testing.assert_array_equal(npi(out2[n]), want[n])
 
 
+def test_pft_build_at_the_scaled_benchmark_size(B):
+    """T = 2^20 tokens, k = 8, E = 256 (8.4 M rows), where the oracle's plain loops would take
+    minutes: properties that fix the arrays uniquely.  The pairs (token_ids[p], expert_ids[p]) are
+    exactly the flattened (t, topk_idx[t, j]) (slot_of is a permutation and their inverse), sorted by
+    the unique key (expert, token), with num_ids and offsets the counts and their scan."""
+    from mixture_experts_layer_pft_gb300.workloads import random_logits
+
+    T, E, k = 1 << 20, 256, 8
+    idx = torch.topk(random_logits(T, E, 77, "cuda"), k, dim=1).indices.to(torch.int32).contiguous()
+    Tk = T * k
+    out = {n: torch.full((Tk,), -7, dtype=torch.int32, device="cuda") for n in ("token_ids", "expert_ids", "slot_of")}
+    num_ids = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    ws = B.new_workspace(B.MOE_OP_PFT_BUILD, T, 8, E, k, 8, torch.float32)
+    B.moe_pft_build(idx, E, num_ids, offsets, out["token_ids"], out["expert_ids"], out["slot_of"], ws)
+    assert B.moe_check_status(ws) == 0
+    ids = npi(idx).ravel()
+    tok, exp, slot = npi(out["token_ids"]), npi(out["expert_ids"]), npi(out["slot_of"])
+    cnt = np.bincount(ids, minlength=E)
+    np.testing.assert_array_equal(npi(num_ids), cnt)
+    np.testing.assert_array_equal(npi(offsets), np.concatenate([[0], np.cumsum(cnt)]))
+    np.testing.assert_array_equal(exp, np.repeat(np.arange(E), cnt))
+    assert (np.bincount(slot, minlength=Tk) == 1).all()  # a permutation of the rows
+    np.testing.assert_array_equal(tok[slot], np.repeat(np.arange(T), k))
+    np.testing.assert_array_equal(exp[slot], ids)
+    same = exp[1:] == exp[:-1]
+    assert (tok[1:][same] > tok[:-1][same]).all()  # tokens ascending inside every segment
+
+
 def test_pft_build_all_tokens_to_one_expert(B):
     T, E = 3000, 16
     idx = np.zeros((T, 1), np.int32)
@@ -474,8 +503,14 @@ def test_expert_ffn_forward_and_backward(B, T, h, E, k, f, dt, skew):
     B.moe_expert_ffn(d["xbuf"], d["offsets"], d["W1"], d["W3"], d["W2"], ybuf, h1, h3, a, ws)
     dn = dtype_name(dt)
     want = O.expert_ffn(np64(d["xbuf"]), p["offsets"], np64(d["W1"]), np64(d["W3"]), np64(d["W2"]), dn)
+    off = p["offsets"]
     for n, got in (("ybuf", ybuf), ("h1", h1), ("h3", h3), ("a", a)):
-        assert rel_l2(np64(got), want[n]) <= TOL[dn], n
+        g = np64(got)
+        assert rel_l2(g, want[n]) <= TOL[dn], n
+        for e in range(E):  # every expert segment on its own, so a wrong one cannot hide in the norm
+            if off[e + 1] > off[e]:
+                sl = slice(off[e], off[e + 1])
+                assert rel_l2(g[sl], want[n][sl]) <= TOL[dn], (n, e)
     dxbuf, dW1, dW3, dW2 = z(Tk, h), z(E, h, f), z(E, h, f), z(E, f, h)
     # both sides of the backward get the oracle forward's saved tensors (exact in dtype)
     sv = {n: torch.from_numpy(want[n]).to(dt).cuda() for n in ("h1", "h3", "a")}
@@ -484,7 +519,16 @@ def test_expert_ffn_forward_and_backward(B, T, h, E, k, f, dt, skew):
     wb = O.expert_ffn_bwd(np64(d["dybuf"]), np64(d["xbuf"]), want["h1"], want["h3"], want["a"],
                           p["offsets"], np64(d["W1"]), np64(d["W3"]), np64(d["W2"]), dn)
     for n, got in (("dxbuf", dxbuf), ("dW1", dW1), ("dW3", dW3), ("dW2", dW2)):
-        assert rel_l2(np64(got), wb[n]) <= TOL[dn], n
+        g = np64(got)
+        assert rel_l2(g, wb[n]) <= TOL[dn], n
+        for e in range(E):
+            if off[e + 1] == off[e]:
+                continue
+            if n == "dxbuf":
+                sl = slice(off[e], off[e + 1])
+                assert rel_l2(g[sl], wb[n][sl]) <= TOL[dn], (n, e)
+            else:
+                assert rel_l2(g[e], wb[n][e]) <= TOL[dn], (n, e)
     empty = np.nonzero(p["num_ids"] == 0)[0]
     for e in empty:
         assert (np64(dW1[e]) == 0).all() and (np64(dW2[e]) == 0).all()
