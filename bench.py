@@ -31,7 +31,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE layer fwd+bwd TFLOPS & tokens/s on 1×GB300; dispatch/combine HBM GB/s"
-DEFAULT_CONFIG = 1  # the X-MoE Small layer, bf16, forward + backward
+DEFAULT_CONFIG = 3  # the X-MoE Large layer, bf16, forward + backward
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP32_ALU_TFLOPS_NOMINAL = 152 * 128 * 2 * 2.07e9 / 1e12  # SMs x FP32 lanes x FMA x max clock
 
@@ -114,7 +114,7 @@ def recorded_traffic(kernel_key, src_hash):
 
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 100 ms while the timed region runs."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -130,7 +130,7 @@ class ClockSampler:
             self.out = open(os.devnull, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.gpu)],
+                 "-lms", "100", "-i", str(self.gpu)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -197,27 +197,105 @@ def barrier(world: int):
 # ----------------------------------------------------------------------------- CPU oracle baseline
 
 
-def oracle_sample_tokens(w, budget_flops=1.2e12):
-    """Token count of a bounded oracle sample (about 10-30 s of fp64 numpy on a CPU host)."""
+def oracle_sample_tokens(w, budget_flops=1.2e12, host_bytes=6e9):
+    """Token count of a bounded oracle sample: about ``budget_flops`` of layer work (10-30 s of
+    fp64 numpy on a CPU host), and no more tokens than keep the fp64 weights of the experts they
+    can reach (at most k per token) within ``host_bytes``."""
     per_tok = model_flops(w, 1)
-    return int(max(16, min(w.T, budget_flops // per_tok)))
+    Ts = int(budget_flops // per_tok)
+    per_expert = 3 * w.h * w.f * 8
+    max_experts = int(host_bytes // per_expert)
+    if w.E > max_experts:
+        Ts = min(Ts, max(1, max_experts // w.k))
+    return int(max(1, min(w.T, Ts)))
 
 
-def time_oracle(w, Ts, steps=1):
-    """Time the oracle on Ts tokens of workload ``w`` (inputs drawn on the CPU)."""
+class HostExperts:
+    """Expert weights of one kind (W1, W3 or W2) as fp64 host arrays for the experts a sample
+    reaches, indexed like the stacked [E, ...] array the oracle takes."""
+
+    def __init__(self, per_expert, shape):
+        self.w = per_expert
+        self.shape = tuple(shape)
+
+    def __getitem__(self, e):
+        if isinstance(e, slice):  # a one-expert view for the per-expert backward
+            return HostExperts({0: self.w[int(e.start)]}, (1,) + self.shape[1:])
+        return self.w[int(e)]
+
+
+def oracle_step(w, x_s, Wg, bias, W1, W3, W2, dy_s):
+    """One layer step of the oracle on a token sample, stage by stage in the order the oracle's
+    layer_forward and layer_backward take them; the expert backward runs one expert at a time so
+    that only one expert's fp64 weight gradients exist at once.  Returns (y, dx) of the sample."""
+    import numpy as np
+
+    from oracle import moe_oracle as O
+
+    dn = w.dtype
+    r = O.route(x_s, Wg, w.k, bias, dn)
+    pft = O.pft_build(r["topk_idx"], w.E)
+    xbuf = O.dispatch(x_s, pft["token_ids"])
+    ffn = O.expert_ffn(xbuf, pft["offsets"], W1, W3, W2, dn)
+    y = O.combine(ffn["ybuf"], pft["slot_of"], r["topk_w"], dn)
+    if dy_s is None:
+        return y, None
+    dybuf, d_w = O.combine_bwd(dy_s, ffn["ybuf"], pft["slot_of"], r["topk_w"], dn)
+    off = pft["offsets"]
+    dxbuf = np.zeros_like(xbuf)
+    for e in np.nonzero(np.diff(off))[0]:
+        sl = slice(off[e], off[e + 1])
+        one = np.array([0, off[e + 1] - off[e]])
+        eb = O.expert_ffn_bwd(dybuf[sl], xbuf[sl], ffn["h1"][sl], ffn["h3"][sl], ffn["a"][sl], one,
+                              W1[e:e + 1], W3[e:e + 1], W2[e:e + 1], dn)
+        dxbuf[sl] = eb["dxbuf"]
+    rb = O.route_bwd(x_s, Wg, r["probs"], r["topk_idx"], d_w, dn)
+    return y, O.dispatch_bwd(dxbuf, pft["slot_of"], w.k, rb["dx_router"], dn)
+
+
+def oracle_inputs(w, Ts, inp=None):
+    """Host inputs of an oracle sample of Ts tokens: from the benchmark's device inputs ``inp``
+    (a seeded choice of tokens, and only the experts they reach), or, without them, drawn on the
+    host (workloads.make_token_sample / make_expert_sample)."""
+    import numpy as np
+    import torch
+
     from mixture_experts_layer_pft_gb300 import workloads
     from oracle import moe_oracle as O
 
-    inp = workloads.make_inputs(w, "cpu", T=Ts)
-    c = {k: (None if v is None else v.double().numpy()) for k, v in inp.items()}
+    if inp is not None:
+        sel = np.sort(np.random.default_rng(w.seed).choice(w.T, size=Ts, replace=False))
+        ix = torch.as_tensor(sel, device=inp["x"].device)
+        x_s = inp["x"][ix].double().cpu().numpy()
+        dy_s = inp["dy"][ix].double().cpu().numpy() if w.backward else None
+        Wg = inp["Wg"].double().cpu().numpy()
+        bias = None if inp["bias"] is None else inp["bias"].double().cpu().numpy()
+    else:
+        smp = workloads.make_token_sample(w, Ts, "cpu")
+        x_s, Wg = smp["x"].double().numpy(), smp["Wg"].double().numpy()
+        dy_s = smp["dy"].double().numpy() if w.backward else None
+        bias = None if smp["bias"] is None else smp["bias"].double().numpy()
+    # the experts the sample reaches (the oracle's own gate decides)
+    experts = np.unique(O.route(x_s, Wg, w.k, bias, w.dtype)["topk_idx"])
+    if inp is not None:
+        ws = {int(e): tuple(inp[n][int(e)].double().cpu().numpy() for n in ("W1", "W3", "W2")) for e in experts}
+    else:
+        ws = {e: tuple(t.double().numpy() for t in v) for e, v in workloads.make_expert_sample(w, experts).items()}
+    W1 = HostExperts({e: v[0] for e, v in ws.items()}, (w.E, w.h, w.f))
+    W3 = HostExperts({e: v[1] for e, v in ws.items()}, (w.E, w.h, w.f))
+    W2 = HostExperts({e: v[2] for e, v in ws.items()}, (w.E, w.f, w.h))
+    return (x_s, Wg, bias, W1, W3, W2, dy_s), len(experts)
+
+
+def time_oracle(w, Ts, steps=1, inp=None):
+    """Time the oracle on Ts tokens of workload ``w``; returns (seconds per step, experts reached)."""
+    args, n_exp = oracle_inputs(w, Ts, inp)
     times = []
     for _ in range(steps):
         t0 = time.perf_counter()
-        fw = O.layer_forward(c["x"], c["Wg"], c["W1"], c["W3"], c["W2"], w.k, c["bias"], w.dtype)
-        if w.backward:
-            O.layer_backward(fw, c["x"], c["Wg"], c["W1"], c["W3"], c["W2"], c["dy"], w.dtype)
+        oracle_step(w, *args)
         times.append(time.perf_counter() - t0)
-    return times
+    return times, n_exp
 
 
 def cpu_cores():
@@ -236,14 +314,21 @@ def run_reference(args, w):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    Ts = oracle_sample_tokens(w, budget_flops=float(args.ref_budget_tflop) * 1e12)
+    # about 10 s of oracle work per step at most: the warm-up and timed steps end within minutes
+    Ts = oracle_sample_tokens(w, budget_flops=float(args.ref_budget_tflop) * 1e12, host_bytes=3e9)
+    args_o, n_exp = oracle_inputs(w, Ts)
     for _ in range(args.warmup):
-        time_oracle(w, Ts, 1)
-    ts = time_oracle(w, Ts, args.steps)
+        oracle_step(w, *args_o)
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(w, *args_o)
+        ts.append(time.perf_counter() - t0)
     tot = sum(ts)
     flops = model_flops(w, Ts) * len(ts)
     value = flops / tot / 1e12
-    sample = f"{Ts} of {w.T} tokens per step (full expert set), fp64 numpy, forward{'+backward' if w.backward else ''}"
+    sample = (f"{Ts} of {w.T} tokens per step and the {n_exp} experts they reach (weights drawn on the host "
+              f"per expert, held in fp64), fp64 numpy, forward{'+backward' if w.backward else ''}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -301,11 +386,12 @@ def kernel_names(stage, n, w):
     names, src = table[stage]
     if stage in ("dispatch", "combine") and n == 0:  # folded into the expert GEMMs
         return [], src
-    assert len(names) == n, (stage, n, names)
+    if len(names) != n:  # a launch sequence this table does not know: numbered, not named
+        return [f"{stage}#{j}" for j in range(n)], src
     return names, src
 
 
-def kernel_counts(w, T, e_active, binding=None):
+def kernel_counts(w, T, e_active):
     """Algorithmic FLOPs and HBM bytes of one launch of each kernel."""
     s = 2 if w.dtype == "bf16" else 4
     h, E, k, f = w.h, w.E, w.k, w.f
@@ -346,6 +432,233 @@ def kernel_counts(w, T, e_active, binding=None):
     return d
 
 
+def stage_calls(binding, w, inp, b):
+    """The layer step's C-ABI calls, one per stage (a no-op where a stage is folded away)."""
+    calls = [
+        lambda: binding.moe_route(inp["x"], inp["Wg"], inp["bias"], w.k, b.logits, b.probs,
+                                  b.topk_idx, b.topk_w, b.ws),
+        lambda: binding.moe_pft_build(b.topk_idx, w.E, b.num_ids, b.offsets, b.token_ids,
+                                      b.expert_ids, b.slot_of, b.ws),
+        # fused: no dispatch call; the gate/up GEMM gathers its token rows from x
+        (lambda: None) if b.fused else
+        (lambda: binding.moe_dispatch(inp["x"], b.token_ids, w.k, b.xbuf, b.ws)),
+        (lambda: binding.moe_expert_ffn_fused(b.xbuf, inp["x"], b.token_ids, b.slot_of, b.topk_w, b.offsets,
+                                              inp["W1"], inp["W3"], inp["W2"], b.ybuf, b.h1, b.h3, b.a,
+                                              b.y, b.ws)) if b.fold_combine else
+        (lambda: binding.moe_expert_ffn_gather(inp["x"], b.token_ids, b.offsets, inp["W1"], inp["W3"],
+                                               inp["W2"], b.ybuf, b.h1, b.h3, b.a, b.ws)) if b.fused else
+        (lambda: binding.moe_expert_ffn(b.xbuf, b.offsets, inp["W1"], inp["W3"], inp["W2"],
+                                        b.ybuf, b.h1, b.h3, b.a, b.ws)),
+        # fold_combine: the down projection already wrote y
+        (lambda: None) if b.fold_combine else
+        (lambda: binding.moe_combine(b.ybuf, b.slot_of, b.topk_w, b.y, b.ws)),
+    ]
+    if w.backward:
+        calls += [
+            lambda: binding.moe_combine_bwd(inp["dy"], b.ybuf, b.slot_of, b.topk_w, b.dybuf,
+                                            b.d_topk_w, b.ws),
+            (lambda: binding.moe_expert_ffn_bwd_gather(b.dybuf, inp["x"], b.token_ids, b.h1, b.h3, b.a,
+                                                       b.offsets, inp["W1"], inp["W3"], inp["W2"],
+                                                       b.dxbuf, b.dW1, b.dW3, b.dW2, b.ws)) if b.fused else
+            (lambda: binding.moe_expert_ffn_bwd(b.dybuf, b.xbuf, b.h1, b.h3, b.a, b.offsets,
+                                                inp["W1"], inp["W3"], inp["W2"], b.dxbuf,
+                                                b.dW1, b.dW3, b.dW2, b.ws)),
+            lambda: binding.moe_route_bwd(inp["x"], inp["Wg"], b.probs, b.topk_idx, b.d_topk_w,
+                                          b.d_logits, b.dWg, b.dx_router, b.ws),
+            lambda: binding.moe_dispatch_bwd(b.dxbuf, b.slot_of, b.dx_router, w.k, b.dx, b.ws),
+        ]
+    return calls
+
+
+def run_calls(calls, stream, ev=None, timer=None, spans=None):
+    """One step with an event before each stage call and one after the last.  With a kernel
+    timer, spans[i] = (first, last) ring index of the launches call i made."""
+    for i, c in enumerate(calls):
+        if ev is not None:
+            ev[i].record(stream)
+        n0 = timer.count() if timer else 0
+        c()
+        if timer is not None:
+            spans.append((n0, timer.count()))
+    if ev is not None:
+        ev[len(calls)].record(stream)
+
+
+def measure_layer(w, T, inp, b, steps, warmup, flush, world, device, no_graph=False, clocks=None):
+    """Warm-up, the timed region (whole steps; the captured step replayed as a CUDA graph unless
+    no_graph, L2 flushed between steps outside the events) and the breakdown pass (an event
+    before each stage call and after each kernel launch).  Returns a dict of the measurements."""
+    import torch
+
+    from mixture_experts_layer_pft_gb300 import binding, layer
+
+    lib = binding.lib()
+    stream = torch.cuda.current_stream()
+    calls = stage_calls(binding, w, inp, b)
+    nst = len(calls)
+    for _ in range(warmup):
+        run_calls(calls, stream)
+    torch.cuda.synchronize()
+    assert binding.moe_check_status(b.ws) == 0, "device status set during warm-up"
+
+    graph = None if no_graph else layer.CapturedStep(lambda: run_calls(calls, stream))
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+    if clocks is not None:
+        clocks.start()
+    n_launch0 = lib.moe_kernel_launches()
+    barrier(world)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        flush.zero_()
+        step_ev[s][0].record(stream)
+        if graph is not None:
+            graph.replay()
+        else:
+            run_calls(calls, stream)
+        step_ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    launches = graph.launches * steps if graph is not None else lib.moe_kernel_launches() - n_launch0
+    clk = clocks.stop() if clocks is not None else None
+    assert binding.moe_check_status(b.ws) == 0, "device status set during the timed region"
+    step_ms = [a.elapsed_time(e) for a, e in step_ev]
+    total_ms = max_over_ranks(sum(step_ms), world, device)
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(steps)]
+    timer = binding.KernelTimer(64 * steps)
+    spans = [[] for _ in range(steps)]
+    with timer:
+        torch.cuda.synchronize()
+        for s in range(steps):
+            flush.zero_()
+            run_calls(calls, stream, events[s], timer, spans[s])
+        torch.cuda.synchronize()
+    assert binding.moe_check_status(b.ws) == 0, "device status set during the breakdown pass"
+    stage_ms = {STAGES[i]: [events[s][i].elapsed_time(events[s][i + 1]) for s in range(steps)]
+                for i in range(nst)}
+    kern_ms, kern_src = {}, {}
+    for s in range(steps):
+        for i, (a0, a1) in enumerate(spans[s]):
+            names, src = kernel_names(STAGES[i], a1 - a0, w)
+            prev = events[s][i]
+            for j, q in enumerate(range(a0, a1)):
+                ev = timer.event(q)
+                kern_ms.setdefault(names[j], []).append(prev.elapsed_time(ev))
+                kern_src[names[j]] = src
+                prev = ev
+    del graph
+    return {"ms_per_step": total_ms / steps, "launches": int(launches),
+            "per_step_launches": int(launches // steps), "graph": not no_graph, "clocks": clk,
+            "stage_ms": stage_ms, "kern_ms": kern_ms, "kern_src": kern_src,
+            "e_active": int((b.num_ids > 0).sum().item())}
+
+
+def kernel_table(w, T, m):
+    """Per-kernel average time, GB/s and TFLOP/s from a measure_layer result."""
+    kc = kernel_counts(w, T, m["e_active"])
+    kernels = {}
+    for n, ms in m["kern_ms"].items():
+        avg = sum(ms) / len(ms)
+        c = kc.get(n, {"flops": 0, "bytes": 0})
+        kernels[n] = {"us": round(1e3 * avg, 2), "GB/s": round(c["bytes"] / (avg * 1e-3) / 1e9, 1)}
+        if c["flops"]:
+            kernels[n]["TFLOP/s"] = round(c["flops"] / (avg * 1e-3) / 1e12, 2)
+    return kernels, kc
+
+
+def measure_pft_scaled(binding, flush, peaks, steps=20, T=1 << 20, k=8, E=256, seed=20):
+    """moe_pft_build at a size where its HBM fraction means something (T = 2^20 tokens, k = 8,
+    E = 256: 8.4 M routed rows): the mean of `steps` launches, L2 flushed before each, with the
+    two kernels timed apart through the library's event ring."""
+    import torch
+
+    from mixture_experts_layer_pft_gb300 import workloads
+
+    dev = flush.device
+    logits = workloads.random_logits(T, E, seed, dev)
+    idx = torch.topk(logits, k, dim=1).indices.to(torch.int32).contiguous()
+    del logits
+    Tk = T * k
+    out = {n: torch.empty(Tk, dtype=torch.int32, device=dev) for n in ("token_ids", "expert_ids", "slot_of")}
+    num_ids = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    ws = binding.new_workspace(binding.MOE_OP_PFT_BUILD, T, 8, E, k, 8, torch.float32, dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        binding.moe_pft_build(idx, E, num_ids, offsets, out["token_ids"], out["expert_ids"], out["slot_of"], ws)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    timer = binding.KernelTimer(8 * steps)
+    per_kernel = []
+    with timer:
+        for s in range(steps):
+            flush.zero_()
+            ev[s][0].record(stream)
+            n0 = timer.count()
+            call()
+            n1 = timer.count()
+            ev[s][1].record(stream)
+            per_kernel.append((n0, n1))
+        torch.cuda.synchronize()
+    assert binding.moe_check_status(ws) == 0, "device status set by the scaled PFT build"
+    us = 1e3 * sum(a.elapsed_time(e) for a, e in ev) / steps
+    kus = {}
+    names = ["pft_hist", "pft_scatter"]
+    for s, (n0, n1) in enumerate(per_kernel):
+        prev = ev[s][0]
+        for j, q in enumerate(range(n0, n1)):
+            e = timer.event(q)
+            name = names[j] if n1 - n0 == len(names) else f"launch{j}"
+            kus.setdefault(name, []).append(1e3 * prev.elapsed_time(e))
+            prev = e
+    byts = 16 * Tk + 8 * E + 4
+    gbs = byts / (us * 1e-6) / 1e9
+    return {"T": T, "k": k, "E": E, "rows": Tk, "us": round(us, 2), "GB/s": round(gbs, 1),
+            "frac_of_hbm": round(gbs / float(peaks["hbm_gbs"]), 4),
+            "algorithmic_bytes": byts, "bytes_note": "topk_idx read once (4 Tk) + token_ids, expert_ids, "
+            "slot_of written (12 Tk) + num_ids, offsets",
+            "kernels_us": {n: round(sum(v) / len(v), 2) for n, v in kus.items()},
+            "l2": "flushed before each launch (256 MB write)"}
+
+
+def measure_supplementary(w, inp, peaks, flush, world, device, steps, warmup, T=16384):
+    """The Large layer shape at T tokens per GPU (512 rows per expert at T = 16384), where the
+    expert GEMMs' arithmetic intensity is above the bf16 ridge: step time, layer TFLOP/s and the
+    fraction of the measured bf16 peak, for the step and for the tensor-core expert GEMMs alone."""
+    import torch
+
+    from mixture_experts_layer_pft_gb300 import layer, workloads
+
+    ws_ = w.with_tokens(T)
+    tok = workloads.make_token_sample(ws_, T, device)
+    sup = {"x": tok["x"], "dy": tok["dy"], "Wg": inp["Wg"], "bias": inp["bias"],
+           "W1": inp["W1"], "W3": inp["W3"], "W2": inp["W2"]}
+    b = layer.LayerBuffers(T, w.h, w.E, w.k, w.f, w.torch_dtype(), device, backward=w.backward)
+    m = measure_layer(ws_, T, sup, b, steps, warmup, flush, world, device)
+    kernels, kc = kernel_table(ws_, T, m)
+    fkey = "bf16_tflops"
+    peak = float(peaks[fkey])
+    flops = model_flops(ws_, T)
+    gemm = [n for n in kernels if n.startswith("tc_") and not n.startswith("tc_router")]
+    gemm_ms = sum(sum(m["kern_ms"][n]) / len(m["kern_ms"][n]) for n in gemm)
+    gemm_flops = sum(kc[n]["flops"] for n in gemm)
+    out = {"workload": f"{w.name} at T={T} tokens (Tk={T * w.k}, {T * w.k // w.E} rows per expert on average)",
+           "ms_per_step": round(m["ms_per_step"], 4),
+           "TFLOP/s": round(flops / (m["ms_per_step"] * 1e-3) / 1e12, 2),
+           "tensor_frac_step": round(flops / (m["ms_per_step"] * 1e-3) / (peak * 1e12), 4),
+           "expert_gemms": {"ms": round(gemm_ms, 4), "TFLOP/s": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 2),
+                            "tensor_frac": round(gemm_flops / (gemm_ms * 1e-3) / (peak * 1e12), 4)},
+           "kernels": {n: kernels[n] for n in gemm},
+           "peak": f"MEASURED_PEAKS.json {fkey} = {peak}", "steps": steps}
+    del b
+    return out
+
+
 def run_ours(args, w):
     import torch
 
@@ -362,7 +675,7 @@ def run_ours(args, w):
     from mixture_experts_layer_pft_gb300 import binding, build, layer, workloads
 
     build.build()
-    lib = binding.lib()
+    binding.lib()
     T = w.T
     inp = workloads.make_inputs(w, device, token_seed=None if world == 1 else w.seed + 7919 * rank)
     b = layer.LayerBuffers(T, w.h, w.E, w.k, w.f, w.torch_dtype(), device, backward=w.backward,
@@ -370,113 +683,16 @@ def run_ours(args, w):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)  # 2x the 129 MB L2
     stream = torch.cuda.current_stream()
 
-    def run_stages(ev, timer=None, spans=None):
-        """One step with an event before each stage call and one after the last.  With a
-        kernel timer, spans[i] = (first, last) ring index of the launches call i made."""
-        calls = [
-            lambda: binding.moe_route(inp["x"], inp["Wg"], inp["bias"], w.k, b.logits, b.probs,
-                                      b.topk_idx, b.topk_w, b.ws),
-            lambda: binding.moe_pft_build(b.topk_idx, w.E, b.num_ids, b.offsets, b.token_ids,
-                                          b.expert_ids, b.slot_of, b.ws),
-            # fused: no dispatch call; the gate/up GEMM gathers its token rows from x
-            (lambda: None) if b.fused else
-            (lambda: binding.moe_dispatch(inp["x"], b.token_ids, w.k, b.xbuf, b.ws)),
-            (lambda: binding.moe_expert_ffn_fused(b.xbuf, inp["x"], b.token_ids, b.slot_of, b.topk_w, b.offsets,
-                                                  inp["W1"], inp["W3"], inp["W2"], b.ybuf, b.h1, b.h3, b.a,
-                                                  b.y, b.ws)) if b.fold_combine else
-            (lambda: binding.moe_expert_ffn_gather(inp["x"], b.token_ids, b.offsets, inp["W1"], inp["W3"],
-                                                   inp["W2"], b.ybuf, b.h1, b.h3, b.a, b.ws)) if b.fused else
-            (lambda: binding.moe_expert_ffn(b.xbuf, b.offsets, inp["W1"], inp["W3"], inp["W2"],
-                                            b.ybuf, b.h1, b.h3, b.a, b.ws)),
-            # fold_combine: the down projection already wrote y
-            (lambda: None) if b.fold_combine else
-            (lambda: binding.moe_combine(b.ybuf, b.slot_of, b.topk_w, b.y, b.ws)),
-        ]
-        if w.backward:
-            calls += [
-                lambda: binding.moe_combine_bwd(inp["dy"], b.ybuf, b.slot_of, b.topk_w, b.dybuf,
-                                                b.d_topk_w, b.ws),
-                (lambda: binding.moe_expert_ffn_bwd_gather(b.dybuf, inp["x"], b.token_ids, b.h1, b.h3, b.a,
-                                                           b.offsets, inp["W1"], inp["W3"], inp["W2"],
-                                                           b.dxbuf, b.dW1, b.dW3, b.dW2, b.ws)) if b.fused else
-                (lambda: binding.moe_expert_ffn_bwd(b.dybuf, b.xbuf, b.h1, b.h3, b.a, b.offsets,
-                                                    inp["W1"], inp["W3"], inp["W2"], b.dxbuf,
-                                                    b.dW1, b.dW3, b.dW2, b.ws)),
-                lambda: binding.moe_route_bwd(inp["x"], inp["Wg"], b.probs, b.topk_idx, b.d_topk_w,
-                                              b.d_logits, b.dWg, b.dx_router, b.ws),
-                lambda: binding.moe_dispatch_bwd(b.dxbuf, b.slot_of, b.dx_router, w.k, b.dx, b.ws),
-            ]
-        for i, c in enumerate(calls):
-            if ev is not None:
-                ev[i].record(stream)
-            n0 = timer.count() if timer else 0
-            c()
-            if timer is not None:
-                spans.append((n0, timer.count()))
-        if ev is not None:
-            ev[len(calls)].record(stream)
-
-    nst = len(STAGES) if w.backward else 5
-    for _ in range(args.warmup):
-        run_stages(None)
-    torch.cuda.synchronize()
-    assert binding.moe_check_status(b.ws) == 0, "device status set during warm-up"
-
-    # ---------------------------------------------------------------- timed region: whole steps
-    # Each step is the captured layer step (CUDA graph replay; --no-graph: one host call per
-    # stage), bracketed by one event pair; L2 is flushed between steps, outside the events.
-    if args.no_graph:
-        graph = None
-        per_step = None
-    else:
-        graph = layer.CapturedStep(lambda: run_stages(None))
-        per_step = graph.launches
-    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-    clocks = ClockSampler(device.index)
-    clocks.start()
-    n_launch0 = lib.moe_kernel_launches()
-    barrier(world)
-    torch.cuda.synchronize()
-    for s in range(args.steps):
-        flush.zero_()
-        step_ev[s][0].record(stream)
-        if graph is not None:
-            graph.replay()
-        else:
-            run_stages(None)
-        step_ev[s][1].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    launches = (per_step * args.steps if graph is not None
-                else lib.moe_kernel_launches() - n_launch0)
-    clk = clocks.stop()
-    assert binding.moe_check_status(b.ws) == 0, "device status set during the timed region"
-    step_ms = [a.elapsed_time(e) for a, e in step_ev]
-    total_ms = max_over_ranks(sum(step_ms), world, device)
-
-    # ---------------------------------------------------------------- breakdown pass
-    # The same steps again, with an event before each stage call and after each kernel launch:
-    # per-stage and per-kernel times (the roofline's kernel duration) come from here.
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(args.steps)]
-    timer = binding.KernelTimer(64 * args.steps)
-    spans = [[] for _ in range(args.steps)]
-    with timer:
-        torch.cuda.synchronize()
-        for s in range(args.steps):
-            flush.zero_()
-            run_stages(events[s], timer, spans[s])
-        torch.cuda.synchronize()
-    assert binding.moe_check_status(b.ws) == 0, "device status set during the breakdown pass"
-    stage_ms = {STAGES[i]: [events[s][i].elapsed_time(events[s][i + 1]) for s in range(args.steps)]
-                for i in range(nst)}
-    ms_per_step = total_ms / args.steps
+    # ---------------------------------------------------------------- timed region + breakdown pass
+    m = measure_layer(w, T, inp, b, args.steps, args.warmup, flush, world, device, args.no_graph,
+                      ClockSampler(device.index))
+    ms_per_step = m["ms_per_step"]
     flops = model_flops(w, T)
     value = world * flops / (ms_per_step * 1e-3) / 1e12
 
     counts = stage_counts(w, T)
     stages = {}
-    for n, ms in stage_ms.items():
+    for n, ms in m["stage_ms"].items():
         avg = sum(ms) / len(ms)
         c = counts[n]
         if (b.fused and n == "dispatch") or (b.fold_combine and n == "combine"):
@@ -485,32 +701,13 @@ def run_ours(args, w):
         stages[n] = {"ms": round(avg, 4), "GB/s": round(c["bytes"] / (avg * 1e-3) / 1e9, 1)}
         if c["flops"] and n.startswith(("expert", "route")):
             stages[n]["TFLOP/s"] = round(c["flops"] / (avg * 1e-3) / 1e12, 2)
-
-    # ---------------------------------------------------------------- per-kernel times (event ring)
-    e_active = int((b.num_ids > 0).sum().item())
-    kern_ms = {}  # kernel name -> list of durations (ms)
-    kern_src = {}
-    for s in range(args.steps):
-        for i, (a0, a1) in enumerate(spans[s]):
-            names, src = kernel_names(STAGES[i], a1 - a0, w)
-            prev = events[s][i]
-            for j, q in enumerate(range(a0, a1)):
-                ev = timer.event(q)
-                kern_ms.setdefault(names[j], []).append(prev.elapsed_time(ev))
-                kern_src[names[j]] = src
-                prev = ev
-    kernels = {}
-    kc = kernel_counts(w, T, e_active, binding)
-    for n, ms in kern_ms.items():
-        avg = sum(ms) / len(ms)
-        c = kc.get(n, {"flops": 0, "bytes": 0})
-        kernels[n] = {"us": round(1e3 * avg, 2), "GB/s": round(c["bytes"] / (avg * 1e-3) / 1e9, 1)}
-        if c["flops"]:
-            kernels[n]["TFLOP/s"] = round(c["flops"] / (avg * 1e-3) / 1e12, 2)
+    kernels, kc = kernel_table(w, T, m)
+    kern_ms, kern_src = m["kern_ms"], m["kern_src"]
 
     # ---------------------------------------------------------------- roofline of the dominant kernel
     peaks, peak_src = read_peaks()
-    dom = max(kern_ms, key=lambda n: sum(kern_ms[n]) / len(kern_ms[n]))
+    known = [n for n in kern_ms if n in kc]
+    dom = max(known, key=lambda n: sum(kern_ms[n]) / len(kern_ms[n]))
     dom_ms = sum(kern_ms[dom]) / len(kern_ms[dom])
     c = kc[dom]
     region_ms = ms_per_step * args.steps
@@ -569,16 +766,28 @@ def run_ours(args, w):
         bo = hy.numel() * hy.element_size() + (hdx.numel() * hdx.element_size() if w.backward else 0)
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms}
+        del hgraph
 
     # ---------------------------------------------------------------- CPU oracle baseline (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         Ts = oracle_sample_tokens(w)
-        ts = time_oracle(w, Ts, 1)
+        ts, n_exp = time_oracle(w, Ts, 1, inp)
         cpu = {"value": model_flops(w, Ts) / ts[0] / 1e12, "unit": "TFLOPS", "cores": cpu_cores(),
                "kind": "oracle",
-               "sample": f"one {'forward+backward' if w.backward else 'forward'} of {Ts} of {w.T} tokens "
-                         f"(all {w.E} experts' weights), fp64 numpy/OpenBLAS, {ts[0]:.1f} s"}
+               "sample": f"one {'forward+backward' if w.backward else 'forward'} of a seeded {Ts} of {w.T} "
+                         f"tokens and the {n_exp} experts they reach (the benchmark's own inputs), fp64 "
+                         f"numpy/OpenBLAS, {ts[0]:.1f} s; value = sample FLOPs / time"}
+
+    # ---------------------------------------------------------------- scaled PFT build and the T = 16384 run
+    pft_scaled = None if args.no_pft_scaled else measure_pft_scaled(binding, flush, peaks)
+    supplementary = None
+    is_large = (w.h, w.E, w.k, w.f, w.dtype) == (7168, 256, 8, 2048, "bf16")
+    if is_large and not args.no_supplementary:
+        del b
+        torch.cuda.empty_cache()
+        supplementary = measure_supplementary(w, inp, peaks, flush, world, device, steps=min(args.steps, 10),
+                                              warmup=3)
 
     if rank == 0:
         line = {
@@ -587,16 +796,17 @@ def run_ours(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic (seeded N(0,1) tokens, random-init weights)",
             "tokens_per_s": world * T / (ms_per_step * 1e-3),
-            "dispatch_GBps": None if b.fused else stages["dispatch"]["GB/s"],
-            "combine_GBps": None if b.fold_combine else stages["combine"]["GB/s"],
+            "dispatch_GBps": None if args.fused else stages["dispatch"]["GB/s"],
+            "combine_GBps": None if args.fold_combine else stages["combine"]["GB/s"],
             "config": {"workload": workload_desc(w), "tokens_per_gpu": T,
                        "l2": "flushed between timed steps (256 MB write, outside the step events)",
                        "step": ("one host call per stage" if args.no_graph else
-                                f"CUDA graph replay of the captured layer step ({per_step} library kernels)"),
+                                f"CUDA graph replay of the captured layer step ({m['per_step_launches']} "
+                                f"library kernels)"),
                        "breakdown": "stages and kernels timed in a second pass with an event after each launch",
                        "dispatch": ("folded into the gate/up and dW1/dW3 GEMMs (rows gathered from x)"
-                                    if b.fused else "its own kernel writing the padding-free buffer"),
-                       "combine": ("folded into the down projection's epilogue" if b.fold_combine
+                                    if args.fused else "its own kernel writing the padding-free buffer"),
+                       "combine": ("folded into the down projection's epilogue" if args.fold_combine
                                    else "its own kernel over ybuf"),
                        "parallelism": f"replicas x{world} (independent tokens, no data-path collective)"},
             "stages": stages,
@@ -604,8 +814,10 @@ def run_ours(args, w):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": int(launches),
-            "clocks": clk,
+            "pft_scaled": pft_scaled,
+            "supplementary": supplementary,
+            "gpu_launches": m["launches"],
+            "clocks": m["clocks"],
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -630,6 +842,10 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="time steps as one host call per stage instead of a CUDA graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pft-scaled", action="store_true",
+                    help="skip the PFT build at T = 2^20, k = 8, E = 256")
+    ap.add_argument("--no-supplementary", action="store_true",
+                    help="skip the Large layer shape at T = 16384 (run with the Large workload only)")
     ap.add_argument("--ref-budget-tflop", type=float, default=0.1,
                     help="reference arm: algorithmic TFLOP per step of the oracle sample")
     args = ap.parse_args(argv)

@@ -116,3 +116,35 @@ def random_tensor(shape, seed: int, dtype=torch.float32, device="cpu", std: floa
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     return _normal(gen, shape, std, device, dtype)
+
+
+def make_token_sample(w: Workload, T: int, device="cpu"):
+    """x, W_g, bias and dy for T tokens of workload ``w`` with no expert weights: the seeded
+    recipe's router weight and token draws (x, then W_g, from the workload's seed; dy from a
+    second generator seeded with seed + 1), for the oracle's timing samples, which fetch expert
+    weights only for the experts their tokens reach (``make_expert_sample``)."""
+    dt = w.torch_dtype()
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed)
+    x = _normal(gen, (T, w.h), 1.0, device, dt)
+    Wg = _normal(gen, (w.h, w.E), 1.0 / math.sqrt(w.h), device, torch.float32)
+    dgen = torch.Generator(device=device)
+    dgen.manual_seed(w.seed + 1)
+    dy = _normal(dgen, (T, w.h), 1.0, device, dt)
+    bias = skew_bias(w.E, device) if w.skew else None
+    return {"x": x, "Wg": Wg, "bias": bias, "dy": dy}
+
+
+def make_expert_sample(w: Workload, experts, device="cpu"):
+    """{e: (W1[e], W3[e], W2[e])} for the listed experts, each drawn from its own generator
+    (seeded from the workload's seed and e) with the recipe's distributions: timing samples for
+    the oracle, not the values make_inputs draws."""
+    dt = w.torch_dtype()
+    out = {}
+    for e in experts:
+        gen = torch.Generator(device=device)
+        gen.manual_seed(1_000_003 * (w.seed + 1) + int(e))
+        out[int(e)] = (_normal(gen, (w.h, w.f), 1.0 / math.sqrt(w.h), device, dt),
+                       _normal(gen, (w.h, w.f), 1.0 / math.sqrt(w.h), device, dt),
+                       _normal(gen, (w.f, w.h), 1.0 / math.sqrt(w.f), device, dt))
+    return out
