@@ -659,6 +659,71 @@ def measure_supplementary(w, inp, peaks, flush, world, device, steps, warmup, T=
     return out
 
 
+def measure_gshard(flush, device, cfg=1, reps=20):
+    """The capacity-buffer (GShard-style) forward beside the padding-free one on workload ``cfg``
+    (X-MoE Small: the pages' ablation compares gating, dispatch and combine there), C = the largest
+    expert load so that both compute the same layer.  Each stage is timed on its own, L2 flushed
+    before it, averaged over ``reps``."""
+    import torch
+
+    from mixture_experts_layer_pft_gb300 import binding, layer, workloads
+
+    w = workloads.WORKLOADS[cfg]
+    inp = workloads.make_inputs(w, device)
+    pb = layer.LayerBuffers(w.T, w.h, w.E, w.k, w.f, w.torch_dtype(), device, backward=False)
+    layer.forward(inp, pb)
+    torch.cuda.synchronize()
+    C = int(pb.num_ids.max().item())
+    gb = layer.GShardBuffers(w.T, w.h, w.E, w.k, w.f, C, w.torch_dtype(), device)
+    layer.gshard_forward(inp, gb)
+    torch.cuda.synchronize()
+    g_calls = layer.gshard_forward(inp, gb, stages=True)
+    route = lambda: binding.moe_route(inp["x"], inp["Wg"], inp["bias"], w.k, pb.logits, pb.probs,  # noqa: E731
+                                      pb.topk_idx, pb.topk_w, pb.ws)
+    pft = {
+        "gating": lambda: (route(), binding.moe_pft_build(pb.topk_idx, w.E, pb.num_ids, pb.offsets, pb.token_ids,
+                                                          pb.expert_ids, pb.slot_of, pb.ws)),
+        "dispatch": lambda: binding.moe_dispatch(inp["x"], pb.token_ids, w.k, pb.xbuf, pb.ws),
+        "experts": lambda: binding.moe_expert_ffn(pb.xbuf, pb.offsets, inp["W1"], inp["W3"], inp["W2"], pb.ybuf,
+                                                  pb.h1, pb.h3, pb.a, pb.ws),
+        "combine": lambda: binding.moe_combine(pb.ybuf, pb.slot_of, pb.topk_w, pb.y, pb.ws),
+    }
+    gsh = dict(zip(("gating", "dispatch", "experts", "combine"), g_calls))
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        fn()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return 1e3 * sum(ms) / len(ms)
+
+    out = {"workload": workload_desc(w) + " (forward)", "capacity_C": C, "stages_us": {}}
+    for n in ("gating", "dispatch", "experts", "combine"):
+        tp, tg = timed(pft[n]), timed(gsh[n])
+        out["stages_us"][n] = {"pft": round(tp, 2), "capacity_buffer": round(tg, 2),
+                               "speedup": round(tg / tp, 2)}
+    tp = sum(v["pft"] for v in out["stages_us"].values())
+    tg = sum(v["capacity_buffer"] for v in out["stages_us"].values())
+    out["forward_us"] = {"pft": round(tp, 2), "capacity_buffer": round(tg, 2), "speedup": round(tg / tp, 2)}
+    s = 2 if w.dtype == "bf16" else 4
+    out["buffer_bytes"] = {"pft_token_buffers": 2 * w.Tk * w.h * s,
+                           "capacity_buffers": 2 * w.E * C * w.h * s + w.T * w.E * C * (s + 4)}
+    diff = (gb.y.float() - pb.y.float()).norm() / pb.y.float().norm()
+    out["rel_l2_y_vs_pft"] = float(diff)
+    assert binding.moe_check_status(gb.ws_gshard) == 0 and binding.moe_check_status(pb.ws) == 0
+    out["note"] = ("the pages' X-MoE ablation (Small, AMD MI250X) reports 5.7x / 35.7x / 8.1x for gating / "
+                   "dispatch / combine; these are the same stages on one GB300")
+    del gb, pb
+    return out
+
+
 def run_ours(args, w):
     import torch
 
@@ -781,6 +846,9 @@ def run_ours(args, w):
 
     # ---------------------------------------------------------------- scaled PFT build and the T = 16384 run
     pft_scaled = None if args.no_pft_scaled else measure_pft_scaled(binding, flush, peaks)
+    gshard = None
+    if not args.no_gshard:
+        gshard = measure_gshard(flush, device)
     supplementary = None
     is_large = (w.h, w.E, w.k, w.f, w.dtype) == (7168, 256, 8, 2048, "bf16")
     if is_large and not args.no_supplementary:
@@ -816,6 +884,7 @@ def run_ours(args, w):
             "e2e": e2e,
             "pft_scaled": pft_scaled,
             "supplementary": supplementary,
+            "gshard": gshard,
             "gpu_launches": m["launches"],
             "clocks": m["clocks"],
         }
@@ -844,6 +913,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pft-scaled", action="store_true",
                     help="skip the PFT build at T = 2^20, k = 8, E = 256")
+    ap.add_argument("--no-gshard", action="store_true",
+                    help="skip the capacity-buffer (GShard-style) stages timed beside the PFT ones")
     ap.add_argument("--no-supplementary", action="store_true",
                     help="skip the Large layer shape at T = 16384 (run with the Large workload only)")
     ap.add_argument("--ref-budget-tflop", type=float, default=0.1,

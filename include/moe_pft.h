@@ -77,7 +77,8 @@ enum moe_op {
   MOE_OP_EXPERT_FFN_BWD = 6,
   MOE_OP_COMBINE = 7,
   MOE_OP_COMBINE_BWD = 8,
-  MOE_OP_ALL = 9 /* the largest of the above: one workspace for the whole layer */
+  MOE_OP_ALL = 9, /* the largest of the above: one workspace for the whole layer */
+  MOE_OP_GSHARD = 10 /* the capacity-buffer comparison path (moe_gshard_*) */
 };
 
 /* Workspace bytes `op` needs at these sizes (always >= 256, a multiple of 256). */
@@ -310,6 +311,44 @@ int moe_combine(const void* ybuf, const int32_t* slot_of, const float* topk_w, i
 int moe_combine_bwd(const void* dy, const void* ybuf, const int32_t* slot_of,
                     const float* topk_w, int T, int k, int h, int dtype, void* dybuf,
                     float* d_topk_w, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The capacity-buffer (GShard-style) data path, the comparison system the padding-free buffers
+ * replace -- X-MoE review §3 "Core formulas" (GShard-style dispatching keeps an E x C x H buffer,
+ * C a fixed capacity, against the PFT's B x H) and §3 "Training pipeline" step 2 (the PFT gate
+ * builds no dispatch_mask); §5 "Ablation" times gating, dispatch and combine against it.  With C
+ * the largest expert load nothing is dropped and the layer equals the padding-free one: the
+ * experts run on the E*C padded rows (moe_expert_ffn with offsets e*C), and
+ * moe_gshard_combine's y equals moe_combine's up to the order of the fp32 sums.
+ *
+ * moe_gshard_gate: from a top-k selection (topk_idx [T,k] int32, topk_w [T,k] fp32, as moe_route
+ * writes them), token t's slot c in expert e is the number of tokens before t that chose e; each
+ * (t, j) with c < C sets dispatch_mask[t,e,c] = 1 and combine_w[t,e,c] = topk_w[t,j]; slots at or
+ * beyond C are dropped.  dispatch_mask: [T,E,C] dtype; combine_w: [T,E,C] fp32 (both overwritten,
+ * zeros elsewhere); loads: [E] int32, the tokens that chose each expert (dropped ones included).
+ * An id outside [0,E), or an expert listed twice in a row, sets MOE_STATUS_BAD_INDEX and is
+ * skipped.  Workspace: moe_workspace_size(MOE_OP_GSHARD, T, h, E, k, f, dtype).
+ */
+int moe_gshard_gate(const int32_t* topk_idx, const float* topk_w, int T, int E, int k, int C, int dtype,
+                    void* dispatch_mask, float* combine_w, int32_t* loads, void* ws, size_t ws_bytes,
+                    void* stream);
+
+/*
+ * moe_gshard_dispatch: xe[e,c,:] = sum_t dispatch_mask[t,e,c] * x[t,:] for the one token per
+ * padded row a gate mask holds (a row with no token is written as zeros; a column with more than
+ * one non-zero sets MOE_STATUS_BAD_INDEX and keeps the first).  x: [T,h]; dispatch_mask:
+ * [T,E,C]; xe: [E,C,h]; all dtype.  A mask of 1 copies the row bit for bit.
+ */
+int moe_gshard_dispatch(const void* x, const void* dispatch_mask, int T, int E, int C, int h, int dtype,
+                        void* xe, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_gshard_combine: y[t,:] = sum_{e,c} combine_w[t,e,c] * ye[e,c,:], summed in fp32 in
+ * ascending (e, c) order over the non-zero weights (at most 256 per token; more set
+ * MOE_STATUS_BAD_INDEX), rounded once.  combine_w: [T,E,C] fp32; ye: [E,C,h] dtype; y: [T,h] dtype.
+ */
+int moe_gshard_combine(const float* combine_w, const void* ye, int T, int E, int C, int h, int dtype, void* y,
+                       void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -22,7 +22,7 @@ MOE_F32, MOE_BF16 = 0, 1
 MOE_STATUS_BAD_INDEX, MOE_STATUS_TIMEOUT = 1, 2
 MOE_ROUTE_FROM_LOGITS, MOE_ROUTE_SIGMOID, MOE_ROUTE_RENORM = 1, 2, 4
 (MOE_OP_ROUTE, MOE_OP_ROUTE_BWD, MOE_OP_PFT_BUILD, MOE_OP_DISPATCH, MOE_OP_DISPATCH_BWD,
- MOE_OP_EXPERT_FFN, MOE_OP_EXPERT_FFN_BWD, MOE_OP_COMBINE, MOE_OP_COMBINE_BWD, MOE_OP_ALL) = range(10)
+ MOE_OP_EXPERT_FFN, MOE_OP_EXPERT_FFN_BWD, MOE_OP_COMBINE, MOE_OP_COMBINE_BWD, MOE_OP_ALL, MOE_OP_GSHARD) = range(11)
 
 # C signatures: (name, restype, argtypes).  P = pointer, I = int, Z = size_t.
 _P, _I, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -53,6 +53,9 @@ SIGNATURES = {
     "moe_expert_ffn_fused": (_I, [_P, _P, _P, _I, _I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P,
                                   _P, _P, _Z, _P]),
     "moe_combine": (_I, [_P, _P, _P, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    "moe_gshard_gate": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "moe_gshard_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
+    "moe_gshard_combine": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]),
     "moe_combine_bwd": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
 }
 
@@ -285,3 +288,26 @@ def moe_combine_bwd(dy, ybuf, slot_of, topk_w, dybuf, d_topk_w, ws):
     k = topk_w.shape[1]
     _call("moe_combine_bwd", _p(dy), _p(ybuf), _p(slot_of), _p(topk_w), T, k, h, _dtype_code(dy),
           _p(dybuf), _p(d_topk_w), _p(ws), ws.numel(), _stream())
+
+
+def moe_gshard_gate(topk_idx, topk_w, E, C, dispatch_mask, combine_w, loads, ws):
+    """Capacity-buffer gate: dispatch_mask [T,E,C] (activation dtype) and combine_w [T,E,C] fp32."""
+    T, k = topk_idx.shape
+    _call("moe_gshard_gate", _p(topk_idx), _p(topk_w), T, E, k, C, _dtype_code(dispatch_mask),
+          _p(dispatch_mask), _p(combine_w), _p(loads), _p(ws), ws.numel(), _stream())
+
+
+def moe_gshard_dispatch(x, dispatch_mask, xe, ws):
+    """xe [E,C,h] = the contraction of dispatch_mask [T,E,C] with x [T,h] over the tokens."""
+    T, E, C = dispatch_mask.shape
+    h = x.shape[1]
+    _call("moe_gshard_dispatch", _p(x), _p(dispatch_mask), T, E, C, h, _dtype_code(x), _p(xe), _p(ws),
+          ws.numel(), _stream())
+
+
+def moe_gshard_combine(combine_w, ye, y, ws):
+    """y [T,h] = the contraction of combine_w [T,E,C] with ye [E,C,h] over (e, c)."""
+    T, E, C = combine_w.shape
+    h = ye.shape[2]
+    _call("moe_gshard_combine", _p(combine_w), _p(ye), T, E, C, h, _dtype_code(ye), _p(y), _p(ws), ws.numel(),
+          _stream())

@@ -166,6 +166,8 @@ size_t moe_workspace_size(int op, int T, int h, int E, int k, int f, int dtype) 
       return hdr + round256(pft_scratch_bytes(std::max(Tk, 1LL), std::max(E, 1)));
     case MOE_OP_EXPERT_FFN_BWD:
       return hdr + 2 * round256((size_t)Tk * std::max(f, 0) * esize(dtype));
+    case MOE_OP_GSHARD:
+      return hdr + round256((size_t)Tk * sizeof(int));
     case MOE_OP_ALL: {
       size_t m = 0;
       for (int o = 0; o < MOE_OP_ALL; ++o) m = std::max(m, moe_workspace_size(o, T, h, E, k, f, dtype));
@@ -482,6 +484,49 @@ int moe_combine_bwd(const void* dy, const void* ybuf, const int32_t* slot_of,
   launch_combine_bwd(dtype, dy, ybuf, slot_of, topk_w, T, k, h, dybuf, d_topk_w, status_of(ws),
                      (cudaStream_t)stream);
   return check_launch("moe_combine_bwd");
+}
+
+int moe_gshard_gate(const int32_t* topk_idx, const float* topk_w, int T, int E, int k, int C, int dtype,
+                    void* dispatch_mask, float* combine_w, int32_t* loads, void* ws, size_t ws_bytes,
+                    void* stream) {
+  REQUIRE(T >= 1 && E >= 1 && E <= 1024 && k >= 1 && k <= E && C >= 1, MOE_ERR_INVALID_ARG,
+          "moe_gshard_gate: need T >= 1, 1 <= k <= E <= 1024, C >= 1");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_gshard_gate: bad dtype");
+  REQUIRE((long long)T * k <= (1LL << 30), MOE_ERR_UNSUPPORTED, "moe_gshard_gate: T*k above 2^30");
+  REQUIRE(ws != nullptr && aligned16(ws) &&
+              ws_bytes >= moe_workspace_size(MOE_OP_GSHARD, T, 0, E, k, 0, dtype),
+          MOE_ERR_WORKSPACE, "moe_gshard_gate: workspace too small");
+  REQUIRE_PTR(topk_idx); REQUIRE_PTR(topk_w); REQUIRE_PTR(dispatch_mask); REQUIRE_PTR(combine_w);
+  REQUIRE_PTR(loads);
+  int* slot = reinterpret_cast<int*>(static_cast<char*>(ws) + sizeof(WsHeader));
+  launch_gshard_gate(dtype, topk_idx, topk_w, T, E, k, C, dispatch_mask, combine_w, loads, slot, status_of(ws),
+                     (cudaStream_t)stream);
+  return check_launch("moe_gshard_gate");
+}
+
+int moe_gshard_dispatch(const void* x, const void* dispatch_mask, int T, int E, int C, int h, int dtype,
+                        void* xe, void* ws, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 1 && E >= 1 && C >= 1 && h >= 8, MOE_ERR_INVALID_ARG,
+          "moe_gshard_dispatch: need T >= 1, E >= 1, C >= 1, h >= 8");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_gshard_dispatch: bad dtype");
+  REQUIRE(h % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_gshard_dispatch: h must be a multiple of 8");
+  REQUIRE(ws != nullptr && ws_bytes >= sizeof(WsHeader), MOE_ERR_WORKSPACE, "moe_gshard_dispatch: workspace too small");
+  REQUIRE_PTR(x); REQUIRE_PTR(dispatch_mask); REQUIRE_PTR(xe);
+  launch_gshard_dispatch(dtype, x, dispatch_mask, T, E, C, h, xe, status_of(ws), (cudaStream_t)stream);
+  return check_launch("moe_gshard_dispatch");
+}
+
+int moe_gshard_combine(const float* combine_w, const void* ye, int T, int E, int C, int h, int dtype, void* y,
+                       void* ws, size_t ws_bytes, void* stream) {
+  REQUIRE(T >= 1 && E >= 1 && C >= 1 && h >= 8, MOE_ERR_INVALID_ARG,
+          "moe_gshard_combine: need T >= 1, E >= 1, C >= 1, h >= 8");
+  REQUIRE(dtype_ok(dtype), MOE_ERR_INVALID_ARG, "moe_gshard_combine: bad dtype");
+  REQUIRE(h % 8 == 0, MOE_ERR_UNSUPPORTED, "moe_gshard_combine: h must be a multiple of 8");
+  REQUIRE((long long)E * C < (1LL << 31), MOE_ERR_UNSUPPORTED, "moe_gshard_combine: E*C at or above 2^31");
+  REQUIRE(ws != nullptr && ws_bytes >= sizeof(WsHeader), MOE_ERR_WORKSPACE, "moe_gshard_combine: workspace too small");
+  REQUIRE_PTR(combine_w); REQUIRE_PTR(ye); REQUIRE_PTR(y);
+  launch_gshard_combine(dtype, combine_w, ye, T, E, C, h, y, status_of(ws), (cudaStream_t)stream);
+  return check_launch("moe_gshard_combine");
 }
 
 }  // extern "C"

@@ -38,6 +38,14 @@ void launch_route_dlogits(const float* probs, const int* topk_idx, const float* 
                           int E, int k, bool sigmoid, bool renorm, float* d_logits, void* dl_planes,
                           int* status, cudaStream_t st);
 
+// gshard.cu -- the capacity-buffer (GShard-style) comparison path
+void launch_gshard_gate(int dtype, const int* idx, const float* w, int T, int E, int k, int C, void* mask,
+                        float* cw, int* loads, int* slot, int* status, cudaStream_t st);
+void launch_gshard_dispatch(int dtype, const void* x, const void* mask, int T, int E, int C, int h, void* xe,
+                            int* status, cudaStream_t st);
+void launch_gshard_combine(int dtype, const float* cw, const void* ye, int T, int E, int C, int h, void* y,
+                           int* status, cudaStream_t st);
+
 // pft.cu
 int pft_num_chunks(long long Tk);
 int pft_chunk_size(long long Tk);

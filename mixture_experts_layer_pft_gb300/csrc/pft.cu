@@ -2,17 +2,20 @@
 //
 // Flattened entry i = t*k + j carries expert e_i = topk_idx[t][j].  For a fixed expert the
 // entries are distinct tokens, so ascending i is ascending t and a STABLE counting sort on e
-// gives the unique (expert, token) order.  Two launches, no spin-waits:
-//   1. pft_hist: each CTA counts its chunk of entries per expert (shared-memory atomics) and
-//      writes the chunk's histogram row.  The last CTA to finish (a ticket from an atomic
-//      counter in the workspace header) sums the rows into num_ids, scans them into
-//      offsets, turns every histogram entry into that chunk's base position for the expert,
-//      and resets the counter for the next call.
-//   2. pft_scatter: each CTA walks its chunk again in rounds of one entry per thread.  Inside
-//      a warp, __match_any_sync groups the lanes with the same expert; a lane's rank is the
-//      number of matching lanes below it.  Per-warp counts in shared memory give the rank
-//      offset contributed by earlier warps of the round.  The position is
-//      base[e] + earlier warps + rank; token_ids, expert_ids and slot_of are written there.
+// gives the unique (expert, token) order.  The entries are cut into G contiguous ranges, one per
+// CTA, and three launches sort them with no spin-waits:
+//   1. pft_count: each CTA counts its range per expert (warp-aggregated shared-memory adds) and
+//      writes one column of the expert-major table hist[e][c].
+//   2. pft_scan: one CTA per expert turns its row of the table into the exclusive prefix over
+//      the ranges (the expert's rows that earlier ranges hold) and writes the expert's total to
+//      num_ids; the last CTA to finish (a ticket from an atomic counter in the workspace header)
+//      scans num_ids into offsets and resets the counter for the next call.
+//   3. pft_scatter: each CTA walks its range in tiles of 4096 entries.  A warp owns 256
+//      consecutive entries of a tile; __match_any_sync groups its lanes by expert, per-warp counts
+//      in shared memory give every entry its rank among the same expert's entries of the tile, in
+//      index order.  slot_of is written in index order; token_ids and expert_ids go through a
+//      tile-local sorted copy in shared memory and are written as runs of consecutive rows per
+//      expert, so the scattered writes coalesce.
 #include "common.cuh"
 #include "internal.h"
 
@@ -20,139 +23,225 @@ namespace moe {
 
 namespace {
 
-constexpr int kHistBlock = 256;
-constexpr int kScatBlock = 512;
-constexpr int kScatWarps = kScatBlock / kWarp;
-constexpr int kMaxE = 1024;
+constexpr int kPBlock = 512;                 // threads of the count and scatter CTAs
+constexpr int kPWarps = kPBlock / kWarp;     // 16
+constexpr int kTile = 4096;                  // entries of one scatter tile
+constexpr int kPerWarp = kTile / kPWarps;    // 256 consecutive entries per warp
+constexpr int kRounds = kPerWarp / kWarp;    // 8 rounds of 32
+constexpr int kMaxRanges = 608;              // 4 CTAs on each of 152 SMs (fixed: sizes the workspace)
+constexpr int kScanBlock = 256;
 
-__global__ void __launch_bounds__(kHistBlock) pft_hist_kernel(
-    const int* __restrict__ idx, long long Tk, int E, int chunk, int nchunks,
-    int* __restrict__ hist, int* __restrict__ num_ids, int* __restrict__ offsets, WsHeader* hdr) {
-  __shared__ int cnt[kMaxE];
-  __shared__ int is_last;
+// ---------------------------------------------------------------------------- 1. count
+__global__ void __launch_bounds__(kPBlock) pft_count_kernel(const int* __restrict__ idx, long long Tk, int E,
+                                                            long long range, int G, int* __restrict__ hist,
+                                                            int* status) {
+  extern __shared__ int cnt[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
-  const long long beg = (long long)blockIdx.x * chunk;
-  const long long end = min(beg + chunk, Tk);
+  const long long beg = (long long)blockIdx.x * range;
+  const long long end = min(beg + range, Tk);
+  const int lane = threadIdx.x % kWarp;
   bool bad = false;
-  for (long long i = beg + threadIdx.x; i < end; i += blockDim.x) {
-    const int e = __ldg(idx + i);
-    if ((unsigned)e < (unsigned)E) atomicAdd(&cnt[e], 1);
-    else bad = true;
-  }
-  if (bad) flag_status(&hdr->status, MOE_STATUS_BAD_INDEX);
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)blockIdx.x * E + e] = cnt[e];
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(&hdr->pft_done, 1u) == (unsigned)(nchunks - 1);
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-  // totals per expert (thread e walks the chunk rows; reads bypass L1)
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int tot = 0;
-    for (int c = 0; c < nchunks; ++c) tot += __ldcg(hist + (size_t)c * E + e);
-    cnt[e] = tot;
-    num_ids[e] = tot;
-  }
-  __syncthreads();
-  // exclusive scan of cnt[0..E) by warp 0 (E <= 1024: 32 entries per lane)
-  if (threadIdx.x < kWarp) {
-    const int lane = threadIdx.x;
-    const int per = (E + kWarp - 1) / kWarp;
-    const int b0 = lane * per, b1 = min(b0 + per, E);
-    int local = 0;
-    for (int e = b0; e < b1; ++e) local += cnt[e];
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < kWarp; o <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += n;
-    }
-    int run = incl - local;
-    for (int e = b0; e < b1; ++e) {
-      const int c = cnt[e];
-      cnt[e] = run;  // now the exclusive offset
-      offsets[e] = run;
-      run += c;
-    }
-    if (lane == kWarp - 1) offsets[E] = incl;
-  }
-  __syncthreads();
-  // histogram entry (c, e) -> base position of chunk c's entries for expert e
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = cnt[e];
-    for (int c = 0; c < nchunks; ++c) {
-      const size_t q = (size_t)c * E + e;
-      const int h = __ldcg(hist + q);
-      hist[q] = run;
-      run += h;
-    }
-  }
-  if (threadIdx.x == 0) hdr->pft_done = 0u;
-}
-
-__global__ void __launch_bounds__(kScatBlock) pft_scatter_kernel(
-    const int* __restrict__ idx, long long Tk, int k, int E, int chunk,
-    const int* __restrict__ base_g, int* __restrict__ token_ids, int* __restrict__ expert_ids,
-    int* __restrict__ slot_of) {
-  extern __shared__ int sm[];
-  int* base = sm;               // [E]
-  int* wcnt = sm + E;           // [kScatWarps][E]
-  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] = __ldcg(base_g + (size_t)blockIdx.x * E + e);
-  for (int q = threadIdx.x; q < kScatWarps * E; q += blockDim.x) wcnt[q] = 0;
-  __syncthreads();
-  const long long beg = (long long)blockIdx.x * chunk;
-  const long long end = min(beg + chunk, Tk);
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (long long r0 = beg; r0 < end; r0 += kScatBlock) {
-    const long long i = r0 + threadIdx.x;
+  // whole warps step through the range together so that __match_any_sync sees full warps
+  for (long long i0 = beg + (threadIdx.x - lane); i0 < end; i0 += blockDim.x) {
+    const long long i = i0 + lane;
     int e = -1;
     if (i < end) {
       e = __ldg(idx + i);
-      if ((unsigned)e >= (unsigned)E) {
-        slot_of[i] = -1;  // flagged by pft_hist
-        e = -1;
-      }
+      if ((unsigned)e >= (unsigned)E) { bad = true; e = -1; }
     }
     const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int rank = __popc(peers & lt_mask);
-    const bool leader = rank == 0;
-    if (leader && e >= 0) wcnt[warp * E + e] = __popc(peers);
-    __syncthreads();
-    if (e >= 0) {
-      int pos = base[e] + rank;
-      for (int w = 0; w < warp; ++w) pos += wcnt[w * E + e];
-      token_ids[pos] = (int)(i / k);
-      expert_ids[pos] = e;
-      slot_of[i] = pos;
-    }
-    __syncthreads();
-    for (int x = threadIdx.x; x < E; x += blockDim.x) {
-      int add = 0;
-      for (int w = 0; w < kScatWarps; ++w) add += wcnt[w * E + x];
-      base[x] += add;
-    }
-    __syncthreads();
-    if (leader && e >= 0) wcnt[warp * E + e] = 0;
-    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[e], __popc(peers));
   }
+  if (bad) flag_status(status, MOE_STATUS_BAD_INDEX);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)e * G + blockIdx.x] = cnt[e];
+}
+
+// ---------------------------------------------------------------------------- 2. scan
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
+  const int lane = threadIdx.x % kWarp, warp = threadIdx.x / kWarp;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < kWarp; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == kWarp - 1) warp_tot[warp] = incl;
+  __syncthreads();
+  int before = 0, all = 0;
+  for (int w = 0; w < (int)(blockDim.x / kWarp); ++w) {
+    const int t = warp_tot[w];
+    if (w < warp) before += t;
+    all += t;
+  }
+  __syncthreads();
+  *total = all;
+  return before + incl - v;
+}
+
+__global__ void __launch_bounds__(kScanBlock) pft_scan_kernel(int* __restrict__ hist, int G, int E,
+                                                              int* __restrict__ num_ids, int* __restrict__ offsets,
+                                                              WsHeader* hdr) {
+  __shared__ int warp_tot[kScanBlock / kWarp];
+  __shared__ int is_last;
+  const int e = blockIdx.x;
+  int* row = hist + (size_t)e * G;
+  int run = 0;
+  for (int c0 = 0; c0 < G; c0 += kScanBlock) {
+    const int c = c0 + threadIdx.x;
+    const int v = c < G ? __ldcg(row + c) : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, warp_tot, &tot);
+    if (c < G) row[c] = run + ex;
+    run += tot;
+  }
+  if (threadIdx.x == 0) num_ids[e] = run;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(&hdr->pft_done, 1u) == (unsigned)(E - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  // the last CTA: offsets = exclusive scan of num_ids (E <= 1024: four per thread)
+  int carry = 0;
+  for (int e0 = 0; e0 < E; e0 += kScanBlock) {
+    const int q = e0 + threadIdx.x;
+    const int v = q < E ? __ldcg(num_ids + q) : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, warp_tot, &tot);
+    if (q < E) offsets[q] = carry + ex;
+    carry += tot;
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = carry;
+    hdr->pft_done = 0u;
+  }
+}
+
+// ---------------------------------------------------------------------------- 3. scatter
+// Shared memory: base[E] (next global row of each expert for this CTA), wcnt[kPWarps][E] (per-warp
+// counts, then per-warp starts within the tile's bucket), tstart[E] (bucket starts in the tile's
+// sorted copy), tcnt[E], stok[kTile], sexp[kTile] (uint16), warp_tot[kPWarps].
+__global__ void __launch_bounds__(kPBlock) pft_scatter_kernel(const int* __restrict__ idx, long long Tk, int k,
+                                                              int E, long long range, int G,
+                                                              const int* __restrict__ hist,
+                                                              const int* __restrict__ offsets,
+                                                              int* __restrict__ token_ids, int* __restrict__ expert_ids,
+                                                              int* __restrict__ slot_of) {
+  extern __shared__ int sm[];
+  int* base = sm;
+  int* wcnt = base + E;
+  int* tstart = wcnt + kPWarps * E;
+  int* tcnt = tstart + E;
+  int* stok = tcnt + E;
+  unsigned short* sexp = reinterpret_cast<unsigned short*>(stok + kTile);
+  __shared__ int warp_tot[kPWarps];
+  const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    base[e] = __ldg(offsets + e) + __ldcg(hist + (size_t)e * G + blockIdx.x);
+  const long long beg = (long long)blockIdx.x * range;
+  const long long end = min(beg + range, Tk);
+  for (long long t0 = beg; t0 < end; t0 += kTile) {
+    // (a) this warp's 256 consecutive entries, 8 per lane in rounds of 32; per-warp counts
+    for (int q = threadIdx.x; q < kPWarps * E; q += blockDim.x) wcnt[q] = 0;
+    __syncthreads();
+    const long long w0 = t0 + (long long)warp * kPerWarp;
+    int ev[kRounds];
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const long long i = w0 + r * kWarp + lane;
+      int e = -1;
+      if (i < end) {
+        e = __ldg(idx + i);
+        if ((unsigned)e >= (unsigned)E) {
+          slot_of[i] = -1;  // reported by pft_count
+          e = -1;
+        }
+      }
+      ev[r] = e;
+    }
+    int* wc = wcnt + warp * E;
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const unsigned peers = __match_any_sync(0xffffffffu, ev[r]);
+      if (ev[r] >= 0 && lane == __ffs(peers) - 1) wc[ev[r]] += __popc(peers);
+      __syncwarp();
+    }
+    __syncthreads();
+    // (b) per expert: each warp's start inside the tile's bucket, the bucket size
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int run = 0;
+      for (int w = 0; w < kPWarps; ++w) {
+        const int c = wcnt[w * E + e];
+        wcnt[w * E + e] = run;
+        run += c;
+      }
+      tcnt[e] = run;
+    }
+    __syncthreads();
+    // bucket starts of the tile's sorted copy: exclusive scan of tcnt over the experts
+    int carry = 0;
+    for (int e0 = 0; e0 < E; e0 += kPBlock) {
+      const int q = e0 + threadIdx.x;
+      const int v = q < E ? tcnt[q] : 0;
+      int tot;
+      const int ex = block_exclusive_scan(v, warp_tot, &tot);
+      if (q < E) tstart[q] = carry + ex;
+      carry += tot;
+    }
+    __syncthreads();
+    // (c) ranks in index order: slot_of directly, token and expert into the sorted copy
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int e = ev[r];
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      int pos = 0;
+      if (e >= 0) pos = wc[e] + __popc(peers & lt_mask);
+      __syncwarp();
+      if (e >= 0 && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
+      __syncwarp();
+      if (e >= 0) {
+        const long long i = w0 + r * kWarp + lane;
+        slot_of[i] = base[e] + pos;
+        const int q = tstart[e] + pos;
+        stok[q] = (int)(i / k);
+        sexp[q] = (unsigned short)e;
+      }
+    }
+    __syncthreads();
+    // (d) write the sorted copy: consecutive entries of one expert go to consecutive rows
+    const int n = carry;  // valid entries of the tile
+    for (int q = threadIdx.x; q < n; q += blockDim.x) {
+      const int e = sexp[q];
+      const int row = base[e] + (q - tstart[e]);
+      if ((unsigned)row < (unsigned)Tk) {  // always true when the counts agree; guards the writes
+        token_ids[row] = stok[q];
+        expert_ids[row] = e;
+      }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) base[e] += tcnt[e];
+    __syncthreads();
+  }
+}
+
+size_t scatter_smem(int E) {
+  return (size_t)(E + kPWarps * E + 2 * E + kTile) * sizeof(int) + (size_t)kTile * sizeof(unsigned short);
 }
 
 }  // namespace
 
-int pft_chunk_size(long long Tk) {
-  // at least 1024 entries per CTA; larger chunks keep the grid near four waves of CTAs
-  long long c = (Tk + 607) / 608;
-  c = ((c + kScatBlock - 1) / kScatBlock) * kScatBlock;
-  return (int)(c < 1024 ? 1024 : c);
+// Ranges (CTAs) for Tk entries: at least 1024 entries each, at most kMaxRanges of them.
+int pft_num_chunks(long long Tk) {
+  const long long g = (Tk + 1023) / 1024;
+  return (int)(g < 1 ? 1 : (g > kMaxRanges ? kMaxRanges : g));
 }
 
-int pft_num_chunks(long long Tk) {
-  const long long c = pft_chunk_size(Tk);
-  return (int)((Tk + c - 1) / c);
+int pft_chunk_size(long long Tk) {
+  const long long g = pft_num_chunks(Tk);
+  return (int)((Tk + g - 1) / g);
 }
 
 size_t pft_scratch_bytes(long long Tk, int E) {
@@ -162,18 +251,19 @@ size_t pft_scratch_bytes(long long Tk, int E) {
 void launch_pft_build(const int* topk_idx, int T, int E, int k, int* num_ids, int* offsets,
                       int* token_ids, int* expert_ids, int* slot_of, void* ws, cudaStream_t st) {
   const long long Tk = (long long)T * k;
-  const int chunk = pft_chunk_size(Tk);
-  const int nchunks = pft_num_chunks(Tk);
+  const int G = pft_num_chunks(Tk);
+  const long long range = pft_chunk_size(Tk);
   WsHeader* hdr = static_cast<WsHeader*>(ws);
   int* hist = reinterpret_cast<int*>(static_cast<char*>(ws) + sizeof(WsHeader));
-  pft_hist_kernel<<<nchunks, kHistBlock, 0, st>>>(topk_idx, Tk, E, chunk, nchunks, hist, num_ids,
-                                                  offsets, hdr);
+  pft_count_kernel<<<G, kPBlock, (size_t)E * sizeof(int), st>>>(topk_idx, Tk, E, range, G, hist, &hdr->status);
   count_launch(st);
-  const size_t smem = (size_t)(1 + kScatWarps) * E * sizeof(int);
+  pft_scan_kernel<<<E, kScanBlock, 0, st>>>(hist, G, E, num_ids, offsets, hdr);
+  count_launch(st);
+  const size_t smem = scatter_smem(E);
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(pft_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  pft_scatter_kernel<<<nchunks, kScatBlock, smem, st>>>(topk_idx, Tk, k, E, chunk, hist, token_ids,
-                                                        expert_ids, slot_of);
+  pft_scatter_kernel<<<G, kPBlock, smem, st>>>(topk_idx, Tk, k, E, range, G, hist, offsets, token_ids, expert_ids,
+                                                slot_of);
   count_launch(st);
 }
 

@@ -171,3 +171,50 @@ class CapturedStep:
 
     def replay(self):
         self.graph.replay()
+
+
+class GShardBuffers:
+    """Device buffers of the capacity-buffer (GShard-style) forward at capacity C: the masks
+    [T,E,C], the padded expert buffers [E*C, ...] and the padded segment offsets e*C.  The gate's
+    probabilities and top-k come from the same moe_route as the padding-free layer."""
+
+    def __init__(self, T: int, h: int, E: int, k: int, f: int, C: int, dtype: torch.dtype, device="cuda"):
+        self.T, self.h, self.E, self.k, self.f, self.C, self.dtype = T, h, E, k, f, C, dtype
+        f32, i32 = torch.float32, torch.int32
+        d = dict(device=device)
+        self.logits = torch.empty(T, E, dtype=f32, **d)
+        self.probs = torch.empty(T, E, dtype=f32, **d)
+        self.topk_idx = torch.empty(T, k, dtype=i32, **d)
+        self.topk_w = torch.empty(T, k, dtype=f32, **d)
+        self.dispatch_mask = torch.empty(T, E, C, dtype=dtype, **d)
+        self.combine_w = torch.empty(T, E, C, dtype=f32, **d)
+        self.loads = torch.empty(E, dtype=i32, **d)
+        self.offsets = (torch.arange(E + 1, dtype=i32, **d) * C).contiguous()
+        self.xe = torch.empty(E, C, h, dtype=dtype, **d)
+        self.h1 = torch.empty(E * C, f, dtype=dtype, **d)
+        self.h3 = torch.empty(E * C, f, dtype=dtype, **d)
+        self.a = torch.empty(E * C, f, dtype=dtype, **d)
+        self.ye = torch.empty(E, C, h, dtype=dtype, **d)
+        self.y = torch.empty(T, h, dtype=dtype, **d)
+        self.ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, dtype, device)
+        self.ws_gshard = B.new_workspace(B.MOE_OP_GSHARD, T, h, E, k, f, dtype, device)
+
+
+def gshard_forward(inp: dict, g: GShardBuffers, stages=None):
+    """Gate -> masks -> padded dispatch -> experts on every padded row -> combine.  With
+    ``stages`` (a list of callables) the four stage calls are returned instead of run."""
+    calls = [
+        lambda: (B.moe_route(inp["x"], inp["Wg"], inp.get("bias"), g.k, g.logits, g.probs, g.topk_idx, g.topk_w,
+                             g.ws),
+                 B.moe_gshard_gate(g.topk_idx, g.topk_w, g.E, g.C, g.dispatch_mask, g.combine_w, g.loads,
+                                   g.ws_gshard)),
+        lambda: B.moe_gshard_dispatch(inp["x"], g.dispatch_mask, g.xe, g.ws_gshard),
+        lambda: B.moe_expert_ffn(g.xe.view(g.E * g.C, g.h), g.offsets, inp["W1"], inp["W3"], inp["W2"],
+                                 g.ye.view(g.E * g.C, g.h), g.h1, g.h3, g.a, g.ws),
+        lambda: B.moe_gshard_combine(g.combine_w, g.ye, g.y, g.ws_gshard),
+    ]
+    if stages is not None:
+        return calls
+    for c in calls:
+        c()
+    return g.y

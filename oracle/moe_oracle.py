@@ -33,6 +33,13 @@ What it computes, stage by stage, and where each stage comes from:
   y[t] = sum_j w[t,j] · ybuf[slot_of[t*k+j]], j ascending.
 * Backward -- the pages describe none; each stage's backward is the textbook adjoint of
   its forward (chain rule, softmax Jacobian, SwiGLU derivative).
+* Capacity-buffer baseline -- X-MoE review, §3 "Core formulas" (GShard-style dispatching
+  holds an E x C x H buffer, C a fixed capacity) and §3 "Training pipeline" step 2 (the PFT
+  gate avoids building a dispatch_mask).  Reading adopted: the gate turns the same top-k
+  selection into dispatch_mask [T,E,C] and combine_weights [T,E,C]; a token's slot c in
+  expert e's C rows is the number of earlier tokens that chose e; slots at or beyond C are
+  dropped; dispatch is the contraction xe[e,c] = sum_t mask[t,e,c] x[t] and combine is
+  y[t] = sum_{e,c} combine_weights[t,e,c] ye[e,c]; the experts run on all E*C padded rows.
 
 Precision policy (``dtype``):
 
@@ -48,7 +55,7 @@ Parity pins (tests marked "not gpu" check each of them): top-k against a brute-f
 selection and constructed ties; softmax against the two-expert closed form; the PFT
 arrays against a brute-force recount and the inverse-permutation identity; dispatch and
 combine against identity experts and adjoint identities; the expert FFN against a
-hand-derived SwiGLU case and an independent GShard-style capacity-buffer formulation;
+hand-derived SwiGLU case and the capacity-buffer formulation below (equal to the PFT layer);
 every gradient against central finite differences in fp64; bf16 rounding against
 hand-derived bit patterns and torch's own conversion.  No function here is unpinned.
 """
@@ -387,3 +394,61 @@ def layer_backward(fwd, x, Wg, W1, W3, W2, dy, dtype="f32"):
     out.update(rb)
     return out
 
+
+
+# ----------------------------------------------------------------------------- capacity-buffer baseline
+
+
+def gshard_capacity_gate(topk_idx, topk_w, E, C):
+    """dispatch_mask, combine_weights [T,E,C] and per-expert loads from a top-k selection.
+
+    The token-by-expert choice matrix is scanned down the tokens: token t's slot in expert e is
+    the number of tokens before t that chose e.  Each (t, j) with slot c < C sets
+    dispatch_mask[t,e,c] = 1 and combine_weights[t,e,c] = topk_w[t,j]; a slot at or beyond the
+    capacity is dropped.  loads[e] counts every token that chose e, dropped or not."""
+    idx = np.asarray(topk_idx, np.int64)
+    w = np.asarray(topk_w, np.float64)
+    T, k = idx.shape
+    chose = np.zeros((T, E))
+    for j in range(k):
+        chose[np.arange(T), idx[:, j]] = 1.0
+    slot = np.cumsum(chose, axis=0) - chose  # tokens before t that chose e
+    mask = np.zeros((T, E, C))
+    cw = np.zeros((T, E, C))
+    for t in range(T):
+        for j in range(k):
+            e = idx[t, j]
+            c = int(slot[t, e])
+            if c < C:
+                mask[t, e, c] = 1.0
+                cw[t, e, c] = w[t, j]
+    return {"dispatch_mask": mask, "combine_weights": cw, "loads": chose.sum(axis=0).astype(np.int64)}
+
+
+def gshard_dispatch(dispatch_mask, x):
+    """xe[e,c,:] = sum_t dispatch_mask[t,e,c] * x[t,:]: the padded [E,C,h] expert buffer."""
+    return np.einsum("tec,th->ech", np.asarray(dispatch_mask, np.float64), np.asarray(x, np.float64))
+
+
+def gshard_combine(combine_weights, ye, dtype="f32"):
+    """y[t,:] = sum_{e,c} combine_weights[t,e,c] * ye[e,c,:], rounded once."""
+    y = np.einsum("tec,ech->th", np.asarray(combine_weights, np.float64), np.asarray(ye, np.float64))
+    return store(y, dtype)
+
+
+def gshard_layer_forward(x, Wg, W1, W3, W2, k, C=None, bias=None, dtype="f32"):
+    """The capacity-buffer forward: gate -> masks -> padded dispatch -> experts on all E*C rows
+    -> combine.  C defaults to the largest expert load, so no token is dropped."""
+    E = W1.shape[0]
+    r = route(x, Wg, k, bias, dtype)
+    if C is None:
+        C = int(np.bincount(r["topk_idx"].ravel(), minlength=E).max())
+    g = gshard_capacity_gate(r["topk_idx"], r["topk_w"], E, C)
+    xe = gshard_dispatch(g["dispatch_mask"], x)
+    h = xe.shape[2]
+    ffn = expert_ffn(xe.reshape(E * C, h), np.arange(E + 1) * C, W1, W3, W2, dtype)
+    ye = ffn["ybuf"].reshape(E, C, h)
+    out = dict(r)
+    out.update(g)
+    out.update({"C": C, "xe": xe, "ye": ye, "y": gshard_combine(g["combine_weights"], ye, dtype)})
+    return out

@@ -11,6 +11,8 @@ Those tokens are checked for validity and left out of the element-wise compariso
 experts whose token set depends on them.
 """
 
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import pytest
 import torch
@@ -114,7 +116,26 @@ def oracle_token_rows(x_s, Wg, bias, W1, W3, W2, k, dn, dy_s=None):
     r = O.route(x_s, Wg, k, bias, dn)
     pft = O.pft_build(r["topk_idx"], E)
     xbuf = O.dispatch(x_s, pft["token_ids"])
-    ffn = O.expert_ffn(xbuf, pft["offsets"], W1, W3, W2, dn)
+    off = pft["offsets"]
+    experts = np.nonzero(np.diff(off))[0]
+
+    def one(t, e):
+        return LazyExperts(t.t[e:e + 1]) if isinstance(t, LazyExperts) else t[e:e + 1]
+
+    # the oracle's expert stages one expert segment at a time (each expert's rows depend on that
+    # expert alone), several experts at once on the host's cores
+    def fwd(e):
+        return e, O.expert_ffn(xbuf[off[e]:off[e + 1]], np.array([0, off[e + 1] - off[e]]), one(W1, e), one(W3, e),
+                               one(W2, e), dn)
+
+    Tk_s, h = xbuf.shape
+    f = W1.shape[2]
+    ffn = {"h1": np.zeros((Tk_s, f)), "h3": np.zeros((Tk_s, f)), "a": np.zeros((Tk_s, f)),
+           "ybuf": np.zeros((Tk_s, h))}
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        for e, res in ex.map(fwd, experts):
+            for n in ffn:
+                ffn[n][off[e]:off[e + 1]] = res[n]
     out = dict(r)
     out.update(pft)
     out.update(ffn)
@@ -123,16 +144,17 @@ def oracle_token_rows(x_s, Wg, bias, W1, W3, W2, k, dn, dy_s=None):
     if dy_s is None:
         return out
     dybuf, d_w = O.combine_bwd(dy_s, ffn["ybuf"], pft["slot_of"], r["topk_w"], dn)
-    off = pft["offsets"]
-    Tk_s, h = xbuf.shape
-    f = ffn["h1"].shape[1]
     dxbuf, dh1, dh3 = np.zeros((Tk_s, h)), np.zeros((Tk_s, f)), np.zeros((Tk_s, f))
-    for e in np.nonzero(np.diff(off))[0]:
+
+    def bwd(e):
         sl = slice(off[e], off[e + 1])
-        one = np.array([0, off[e + 1] - off[e]])
-        We = [LazyExperts(t.t[e:e + 1]) if isinstance(t, LazyExperts) else t[e:e + 1] for t in (W1, W3, W2)]
-        eb = O.expert_ffn_bwd(dybuf[sl], xbuf[sl], ffn["h1"][sl], ffn["h3"][sl], ffn["a"][sl], one, *We, dn)
-        dxbuf[sl], dh1[sl], dh3[sl] = eb["dxbuf"], eb["dh1"], eb["dh3"]
+        return e, O.expert_ffn_bwd(dybuf[sl], xbuf[sl], ffn["h1"][sl], ffn["h3"][sl], ffn["a"][sl],
+                                   np.array([0, off[e + 1] - off[e]]), one(W1, e), one(W3, e), one(W2, e), dn)
+
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        for e, eb in ex.map(bwd, experts):
+            sl = slice(off[e], off[e + 1])
+            dxbuf[sl], dh1[sl], dh3[sl] = eb["dxbuf"], eb["dh1"], eb["dh3"]
     rb = O.route_bwd(x_s, Wg, r["probs"], r["topk_idx"], d_w, dn)
     out.update({"dybuf": dybuf, "d_topk_w": d_w, "dxbuf": dxbuf, "dh1": dh1, "dh3": dh3,
                 "d_logits": rb["d_logits"], "dx_router": rb["dx_router"],

@@ -235,40 +235,69 @@ def test_swiglu_closed_form_case():
     np.testing.assert_allclose(out["ybuf"][0], a[0] * W2[0, 0] + a[1] * W2[0, 1], rtol=1e-14)
 
 
-def _gshard_capacity_forward(x, idx, w, W1, W3, W2):
-    """GShard-style layer: dispatch_mask [T,E,C] with C = the largest expert load, an
-    einsum dispatch into a padded [E,C,h] buffer, the experts on every padded row, and an
-    einsum combine.  It shares only the per-expert FFN with the PFT path."""
-    T, k = idx.shape
-    E = W1.shape[0]
-    chose = np.zeros((T, E))
-    for t in range(T):
-        for j in range(k):
-            chose[t, idx[t, j]] = 1.0
-    loc = np.cumsum(chose, axis=0) - 1.0
-    C = int(chose.sum(axis=0).max())
-    mask = np.zeros((T, E, C)); cw = np.zeros((T, E, C))
-    for t in range(T):
-        for j in range(k):
-            e = idx[t, j]; c = int(loc[t, e])
-            mask[t, e, c] = 1.0
-            cw[t, e, c] = w[t, j]
-    xe = np.einsum("tec,th->ech", mask, x)
-    ye = np.zeros_like(xe)
-    for e in range(E):
-        ye[e] = O.expert_ffn(xe[e], np.array([0, C]), W1[e:e + 1], W3[e:e + 1], W2[e:e + 1], "f64")["ybuf"]
-    return np.einsum("tec,ech->th", cw, ye)
-
-
 @pytest.mark.parametrize("T,h,E,k,f,skew", [(24, 6, 4, 2, 5, False), (40, 8, 8, 3, 4, True)])
 def test_pft_layer_equals_gshard_capacity_layer(T, h, E, k, f, skew):
+    """X-MoE's claim: the padding-free layer is a lossless change of data structure, so the
+    capacity-buffer layer with C = the largest load gives the same outputs."""
     g = rng(T + E)
     x = g.standard_normal((T, h)); Wg = g.standard_normal((h, E)) / math.sqrt(h)
     W1 = g.standard_normal((E, h, f)); W3 = g.standard_normal((E, h, f)); W2 = g.standard_normal((E, f, h))
     bias = -1.6 * np.log(np.arange(E) + 1.0) if skew else None
     fw = O.layer_forward(x, Wg, W1, W3, W2, k, bias, "f64")
-    ref = _gshard_capacity_forward(x, fw["topk_idx"], fw["topk_w"], W1, W3, W2)
-    np.testing.assert_allclose(fw["y"], ref, rtol=1e-12, atol=1e-12)
+    gs = O.gshard_layer_forward(x, Wg, W1, W3, W2, k, None, bias, "f64")
+    np.testing.assert_allclose(gs["y"], fw["y"], rtol=1e-12, atol=1e-12)
+    # the padded buffer holds the PFT buffer's rows at the same positions within each expert
+    for e in range(E):
+        n = fw["num_ids"][e]
+        np.testing.assert_array_equal(gs["xe"][e, :n], fw["xbuf"][fw["offsets"][e]:fw["offsets"][e + 1]])
+        assert (gs["xe"][e, n:] == 0).all()
+    assert gs["C"] == fw["num_ids"].max()
+
+
+def test_gshard_gate_by_brute_force_and_its_invariants():
+    """Masks against a plain recount (slot = earlier tokens of the same expert), the drop rule
+    at a capacity below the largest load, and the sums the masks must keep."""
+    T, E, k = 30, 5, 2
+    g = rng(11)
+    idx = np.stack([g.permutation(E)[:k] for _ in range(T)]).astype(np.int32)
+    w = g.uniform(0.1, 1.0, (T, k))
+    loads = np.bincount(idx.ravel(), minlength=E)
+    for C in (int(loads.max()), int(loads.max()) - 3):
+        m = O.gshard_capacity_gate(idx, w, E, C)
+        np.testing.assert_array_equal(m["loads"], loads)
+        kept = 0
+        for t in range(T):
+            for j in range(k):
+                e = idx[t, j]
+                c = sum(1 for u in range(t) if e in idx[u])
+                if c < C:
+                    assert m["dispatch_mask"][t, e, c] == 1.0 and m["combine_weights"][t, e, c] == w[t, j]
+                    kept += 1
+        assert m["dispatch_mask"].sum() == kept
+        assert (m["dispatch_mask"].sum(axis=0) <= 1).all()  # one token per padded row
+        if C == loads.max():
+            assert kept == T * k
+            np.testing.assert_allclose(m["combine_weights"].sum(axis=(1, 2)), w.sum(axis=1), rtol=1e-15)
+        else:
+            assert kept < T * k
+
+
+def test_gshard_dispatch_and_combine_are_the_contractions():
+    """One-hot masks make the contractions a gather and a weighted sum of picked rows."""
+    T, E, C, h = 7, 3, 4, 5
+    g = rng(12)
+    x = g.standard_normal((T, h)); ye = g.standard_normal((E, C, h))
+    mask = np.zeros((T, E, C)); cw = np.zeros((T, E, C))
+    mask[2, 1, 0] = 1.0; mask[5, 1, 1] = 1.0; mask[0, 2, 3] = 1.0
+    cw[2, 1, 0] = 0.25; cw[2, 0, 2] = 0.5; cw[6, 2, 1] = -2.0
+    xe = O.gshard_dispatch(mask, x)
+    np.testing.assert_array_equal(xe[1, 0], x[2]); np.testing.assert_array_equal(xe[1, 1], x[5])
+    np.testing.assert_array_equal(xe[2, 3], x[0])
+    assert np.count_nonzero(np.abs(xe).sum(axis=2)) == 3
+    y = O.gshard_combine(cw, ye, "f64")
+    np.testing.assert_allclose(y[2], 0.25 * ye[1, 0] + 0.5 * ye[0, 2], rtol=1e-15)
+    np.testing.assert_allclose(y[6], -2.0 * ye[2, 1], rtol=1e-15)
+    assert (y[[0, 1, 3, 4, 5]] == 0).all()
 
 
 def test_identical_experts_scale_one_dense_ffn():
