@@ -913,6 +913,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pft-scaled", action="store_true",
                     help="skip the PFT build at T = 2^20, k = 8, E = 256")
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count T")
+    ap.add_argument("--experts", type=int, default=0, help="override the workload's expert count E")
     ap.add_argument("--no-gshard", action="store_true",
                     help="skip the capacity-buffer (GShard-style) stages timed beside the PFT ones")
     ap.add_argument("--no-supplementary", action="store_true",
@@ -925,6 +927,13 @@ def main(argv=None):
     from mixture_experts_layer_pft_gb300 import workloads
 
     w = workloads.WORKLOADS[args.config]
+    if args.tokens or args.experts:
+        # a slice of the workload with the same expert shape (profiling captures stay small)
+        import dataclasses
+
+        T = args.tokens or w.T
+        E = args.experts or w.E
+        w = dataclasses.replace(w, T=T, E=E, name=f"{w.name}-slice-T{T}-E{E}")
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)
