@@ -59,10 +59,12 @@ __global__ void __launch_bounds__(kBlock) dispatch_kernel(const T* __restrict__ 
       const int v = vb + lt + u * tpr;
       if (v < nvec) r[u] = __ldg(src + v);
     }
+    // streaming stores (evict first): the buffer is written once, while the rows of x it copies
+    // are read k times and should stay in L2
 #pragma unroll
     for (int u = 0; u < kMaxVecPerThread; ++u) {
       const int v = vb + lt + u * tpr;
-      if (v < nvec) dst[v] = r[u];
+      if (v < nvec) __stcs(reinterpret_cast<int4*>(dst + v), *reinterpret_cast<const int4*>(&r[u]));
     }
   }
 }

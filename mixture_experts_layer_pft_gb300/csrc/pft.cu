@@ -4,16 +4,16 @@
 // entries are distinct tokens, so ascending i is ascending t and a STABLE counting sort on e
 // gives the unique (expert, token) order.  The entries are cut into G contiguous ranges, one per
 // CTA, and three launches sort them with no spin-waits:
-//   1. pft_count: each CTA counts its range per expert (warp-aggregated shared-memory adds) and
-//      writes one column of the expert-major table hist[e][c].
+//   1. pft_count: each CTA counts its range per expert (shared-memory atomic adds, eight loads in
+//      flight per thread) and writes one column of the expert-major table hist[e][c].
 //   2. pft_scan: one CTA per expert turns its row of the table into the exclusive prefix over
 //      the ranges (the expert's rows that earlier ranges hold) and writes the expert's total to
 //      num_ids; the last CTA to finish (a ticket from an atomic counter in the workspace header)
 //      scans num_ids into offsets and resets the counter for the next call.
 //   3. pft_scatter: each CTA walks its range in tiles of 4096 entries.  A warp owns 256
-//      consecutive entries of a tile; __match_any_sync groups its lanes by expert, per-warp counts
-//      in shared memory give every entry its rank among the same expert's entries of the tile, in
-//      index order.  slot_of is written in index order; token_ids and expert_ids go through a
+//      consecutive entries of a tile; per-warp counts in shared memory, and the lanes that share an
+//      expert in each round of 32 (ballots over the bits of the id), give every entry its rank
+//      among the same expert's entries of the tile, in index order.  slot_of is written in index order; token_ids and expert_ids go through a
 //      tile-local sorted copy in shared memory and are written as runs of consecutive rows per
 //      expert, so the scattered writes coalesce.
 #include "common.cuh"
@@ -40,18 +40,24 @@ __global__ void __launch_bounds__(kPBlock) pft_count_kernel(const int* __restric
   __syncthreads();
   const long long beg = (long long)blockIdx.x * range;
   const long long end = min(beg + range, Tk);
-  const int lane = threadIdx.x % kWarp;
   bool bad = false;
-  // whole warps step through the range together so that __match_any_sync sees full warps
-  for (long long i0 = beg + (threadIdx.x - lane); i0 < end; i0 += blockDim.x) {
-    const long long i = i0 + lane;
-    int e = -1;
-    if (i < end) {
-      e = __ldg(idx + i);
-      if ((unsigned)e >= (unsigned)E) { bad = true; e = -1; }
+  // eight loads in flight per thread (coalesced across the block), then the shared-memory adds
+  constexpr int U = 8;
+  for (long long i0 = beg + threadIdx.x; i0 < end; i0 += (long long)U * blockDim.x) {
+    int ev[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = i0 + (long long)u * blockDim.x;
+      ev[u] = i < end ? __ldg(idx + i) : -1;
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(peers) - 1) atomicAdd(&cnt[e], __popc(peers));
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long i = i0 + (long long)u * blockDim.x;
+      if (i < end) {
+        if ((unsigned)ev[u] < (unsigned)E) atomicAdd(&cnt[ev[u]], 1);
+        else bad = true;
+      }
+    }
   }
   if (bad) flag_status(status, MOE_STATUS_BAD_INDEX);
   __syncthreads();
@@ -120,11 +126,27 @@ __global__ void __launch_bounds__(kScanBlock) pft_scan_kernel(int* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------- 3. scatter
+// Lanes of the warp holding the same expert id as this lane: the AND over the id's bits of
+// the ballot of that bit (or of its complement), restricted to lanes with a valid id.  nbits
+// (warp-uniform) bits cover every id below E.  Lanes with e < 0 get an unused mask.
+__device__ __forceinline__ unsigned same_expert_lanes(int e, int nbits) {
+  unsigned m = __ballot_sync(0xffffffffu, e >= 0);
+#pragma unroll
+  for (int b = 0; b < 10; ++b) {
+    if (b < nbits) {
+      const bool bit = ((e >> b) & 1) != 0;
+      const unsigned bb = __ballot_sync(0xffffffffu, bit);
+      m &= bit ? bb : ~bb;
+    }
+  }
+  return m;
+}
+
 // Shared memory: base[E] (next global row of each expert for this CTA), wcnt[kPWarps][E] (per-warp
 // counts, then per-warp starts within the tile's bucket), tstart[E] (bucket starts in the tile's
 // sorted copy), tcnt[E], stok[kTile], sexp[kTile] (uint16), warp_tot[kPWarps].
 __global__ void __launch_bounds__(kPBlock) pft_scatter_kernel(const int* __restrict__ idx, long long Tk, int k,
-                                                              int E, long long range, int G,
+                                                              int E, int nbits, long long range, int G,
                                                               const int* __restrict__ hist,
                                                               const int* __restrict__ offsets,
                                                               int* __restrict__ token_ids, int* __restrict__ expert_ids,
@@ -164,11 +186,8 @@ __global__ void __launch_bounds__(kPBlock) pft_scatter_kernel(const int* __restr
     }
     int* wc = wcnt + warp * E;
 #pragma unroll
-    for (int r = 0; r < kRounds; ++r) {
-      const unsigned peers = __match_any_sync(0xffffffffu, ev[r]);
-      if (ev[r] >= 0 && lane == __ffs(peers) - 1) wc[ev[r]] += __popc(peers);
-      __syncwarp();
-    }
+    for (int r = 0; r < kRounds; ++r)
+      if (ev[r] >= 0) atomicAdd(&wc[ev[r]], 1);  // this warp's row only
     __syncthreads();
     // (b) per expert: each warp's start inside the tile's bucket, the bucket size
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -192,23 +211,31 @@ __global__ void __launch_bounds__(kPBlock) pft_scatter_kernel(const int* __restr
       carry += tot;
     }
     __syncthreads();
-    // (c) ranks in index order: slot_of directly, token and expert into the sorted copy
+    // (c) ranks in index order: slot_of directly, token and expert into the sorted copy.  The
+    // token of entry i = w0 + 32 r + lane is t = i / k, stepped from round to round.
+    const int i_first = (int)(w0 - beg) + lane;  // entry index relative to the range start
+    int t_cur = (int)((beg + i_first) / k), j_cur = (int)((beg + i_first) % k);
+    const int dt = kWarp / k, dj = kWarp % k;
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
       const int e = ev[r];
-      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const unsigned peers = same_expert_lanes(e, nbits);
+      const unsigned below = peers & lt_mask;
       int pos = 0;
-      if (e >= 0) pos = wc[e] + __popc(peers & lt_mask);
+      if (e >= 0) pos = wc[e] + __popc(below);
       __syncwarp();
-      if (e >= 0 && lane == __ffs(peers) - 1) wc[e] += __popc(peers);
+      if (e >= 0 && below == 0u) wc[e] = pos + __popc(peers);  // the group's first lane
       __syncwarp();
       if (e >= 0) {
         const long long i = w0 + r * kWarp + lane;
         slot_of[i] = base[e] + pos;
         const int q = tstart[e] + pos;
-        stok[q] = (int)(i / k);
+        stok[q] = t_cur;
         sexp[q] = (unsigned short)e;
       }
+      t_cur += dt;
+      j_cur += dj;
+      if (j_cur >= k) { j_cur -= k; ++t_cur; }
     }
     __syncthreads();
     // (d) write the sorted copy: consecutive entries of one expert go to consecutive rows
@@ -262,8 +289,10 @@ void launch_pft_build(const int* topk_idx, int T, int E, int k, int* num_ids, in
   const size_t smem = scatter_smem(E);
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(pft_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  pft_scatter_kernel<<<G, kPBlock, smem, st>>>(topk_idx, Tk, k, E, range, G, hist, offsets, token_ids, expert_ids,
-                                                slot_of);
+  int nbits = 0;  // bits that hold every id below E
+  while ((1 << nbits) < E) ++nbits;
+  pft_scatter_kernel<<<G, kPBlock, smem, st>>>(topk_idx, Tk, k, E, nbits, range, G, hist, offsets, token_ids,
+                                                expert_ids, slot_of);
   count_launch(st);
 }
 
