@@ -33,15 +33,6 @@ RowGeom row_geom(int nvec, int maxvec = kMaxVecPerThread) {
   return {tpr, kBlock / tpr};
 }
 
-// 16-byte read-only load that asks L2 to keep the line (evict-last policy `pol`).
-__device__ __forceinline__ uint4 ld_keep_in_l2(const uint4* p, uint64_t pol) {
-  uint4 r;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p), "l"(pol));
-  return r;
-}
-
 // ---------------------------------------------------------------------------- dispatch
 // xbuf[p,:] = x[token_ids[p],:]
 template <typename T>
@@ -61,15 +52,12 @@ __global__ void __launch_bounds__(kBlock) dispatch_kernel(const T* __restrict__ 
     return;
   }
   const uint4* src = reinterpret_cast<const uint4*>(x) + (size_t)t * nvec;
-  // each row of x is read k times, from k places in the buffer: keep it in L2
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   for (int vb = 0; vb < nvec; vb += tpr * kMaxVecPerThread) {
     uint4 r[kMaxVecPerThread];
 #pragma unroll
     for (int u = 0; u < kMaxVecPerThread; ++u) {
       const int v = vb + lt + u * tpr;
-      if (v < nvec) r[u] = ld_keep_in_l2(src + v, pol);
+      if (v < nvec) r[u] = __ldg(src + v);
     }
     // streaming stores (evict first): the buffer is written once, while the rows of x it copies
     // are read k times and should stay in L2
