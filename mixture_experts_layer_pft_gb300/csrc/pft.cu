@@ -126,36 +126,38 @@ __global__ void __launch_bounds__(kScanBlock) pft_scan_kernel(int* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------- 3. scatter
-// Lanes of the warp holding the same expert id as this lane: the AND over the id's bits of
-// the ballot of that bit (or of its complement), restricted to lanes with a valid id.  nbits
-// (warp-uniform) bits cover every id below E.  Lanes with e < 0 get an unused mask.
-__device__ __forceinline__ unsigned same_expert_lanes(int e, int nbits) {
+// Lanes of the warp holding the same expert id as this lane: the AND over the id's NB bits of
+// the ballot of that bit (or of its complement), restricted to lanes with a valid id (NB bits
+// cover every id below E).  Lanes with e < 0 get an unused mask.
+template <int NB>
+__device__ __forceinline__ unsigned same_expert_lanes(int e) {
   unsigned m = __ballot_sync(0xffffffffu, e >= 0);
 #pragma unroll
-  for (int b = 0; b < 10; ++b) {
-    if (b < nbits) {
-      const bool bit = ((e >> b) & 1) != 0;
-      const unsigned bb = __ballot_sync(0xffffffffu, bit);
-      m &= bit ? bb : ~bb;
-    }
+  for (int b = 0; b < NB; ++b) {
+    const bool bit = ((e >> b) & 1) != 0;
+    const unsigned bb = __ballot_sync(0xffffffffu, bit);
+    m &= bit ? bb : ~bb;
   }
   return m;
 }
 
-// Shared memory: base[E] (next global row of each expert for this CTA), wcnt[kPWarps][E] (per-warp
-// counts, then per-warp starts within the tile's bucket), tstart[E] (bucket starts in the tile's
-// sorted copy), tcnt[E], stok[kTile], sexp[kTile] (uint16), warp_tot[kPWarps].
-__global__ void __launch_bounds__(kPBlock) pft_scatter_kernel(const int* __restrict__ idx, long long Tk, int k,
-                                                              int E, int nbits, long long range, int G,
-                                                              const int* __restrict__ hist,
-                                                              const int* __restrict__ offsets,
-                                                              int* __restrict__ token_ids, int* __restrict__ expert_ids,
-                                                              int* __restrict__ slot_of) {
+constexpr int kWStride = kPWarps + 1;  // per-expert row of the per-warp count table (padded)
+
+// Shared memory: base[E] (next global row of each expert for this CTA), wcnt[E][kWStride]
+// (per-warp counts, then each warp's start inside the tile's bucket), delta[E] (global row minus
+// position in the tile's sorted copy), tcnt[E], stok[kTile], sexp[kTile] (uint16).
+template <int NB>
+__global__ void __launch_bounds__(kPBlock, 2) pft_scatter_kernel(const int* __restrict__ idx, int Tk, int k, int E,
+                                                                 int range, int G, const int* __restrict__ hist,
+                                                                 const int* __restrict__ offsets,
+                                                                 int* __restrict__ token_ids,
+                                                                 int* __restrict__ expert_ids,
+                                                                 int* __restrict__ slot_of) {
   extern __shared__ int sm[];
   int* base = sm;
   int* wcnt = base + E;
-  int* tstart = wcnt + kPWarps * E;
-  int* tcnt = tstart + E;
+  int* delta = wcnt + kWStride * E;
+  int* tcnt = delta + E;
   int* stok = tcnt + E;
   unsigned short* sexp = reinterpret_cast<unsigned short*>(stok + kTile);
   __shared__ int warp_tot[kPWarps];
@@ -163,17 +165,18 @@ __global__ void __launch_bounds__(kPBlock) pft_scatter_kernel(const int* __restr
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     base[e] = __ldg(offsets + e) + __ldcg(hist + (size_t)e * G + blockIdx.x);
-  const long long beg = (long long)blockIdx.x * range;
-  const long long end = min(beg + range, Tk);
-  for (long long t0 = beg; t0 < end; t0 += kTile) {
+  const int beg = blockIdx.x * range;
+  const int end = min(beg + range, Tk);
+  const int dt = kWarp / k, dj = kWarp % k;
+  for (int t0 = beg; t0 < end; t0 += kTile) {
     // (a) this warp's 256 consecutive entries, 8 per lane in rounds of 32; per-warp counts
-    for (int q = threadIdx.x; q < kPWarps * E; q += blockDim.x) wcnt[q] = 0;
+    for (int q = threadIdx.x; q < kWStride * E; q += blockDim.x) wcnt[q] = 0;
     __syncthreads();
-    const long long w0 = t0 + (long long)warp * kPerWarp;
+    const int w0 = t0 + warp * kPerWarp;
     int ev[kRounds];
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
-      const long long i = w0 + r * kWarp + lane;
+      const int i = w0 + r * kWarp + lane;
       int e = -1;
       if (i < end) {
         e = __ldg(idx + i);
@@ -184,17 +187,18 @@ __global__ void __launch_bounds__(kPBlock) pft_scatter_kernel(const int* __restr
       }
       ev[r] = e;
     }
-    int* wc = wcnt + warp * E;
 #pragma unroll
     for (int r = 0; r < kRounds; ++r)
-      if (ev[r] >= 0) atomicAdd(&wc[ev[r]], 1);  // this warp's row only
+      if (ev[r] >= 0) atomicAdd(&wcnt[ev[r] * kWStride + warp], 1);
     __syncthreads();
     // (b) per expert: each warp's start inside the tile's bucket, the bucket size
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      int* row = wcnt + e * kWStride;
       int run = 0;
+#pragma unroll
       for (int w = 0; w < kPWarps; ++w) {
-        const int c = wcnt[w * E + e];
-        wcnt[w * E + e] = run;
+        const int c = row[w];
+        row[w] = run;
         run += c;
       }
       tcnt[e] = run;
@@ -207,29 +211,27 @@ __global__ void __launch_bounds__(kPBlock) pft_scatter_kernel(const int* __restr
       const int v = q < E ? tcnt[q] : 0;
       int tot;
       const int ex = block_exclusive_scan(v, warp_tot, &tot);
-      if (q < E) tstart[q] = carry + ex;
+      if (q < E) delta[q] = base[q] - (carry + ex);
       carry += tot;
     }
     __syncthreads();
     // (c) ranks in index order: slot_of directly, token and expert into the sorted copy.  The
     // token of entry i = w0 + 32 r + lane is t = i / k, stepped from round to round.
-    const int i_first = (int)(w0 - beg) + lane;  // entry index relative to the range start
-    int t_cur = (int)((beg + i_first) / k), j_cur = (int)((beg + i_first) % k);
-    const int dt = kWarp / k, dj = kWarp % k;
+    int t_cur = (w0 + lane) / k, j_cur = (w0 + lane) % k;
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
       const int e = ev[r];
-      const unsigned peers = same_expert_lanes(e, nbits);
+      const unsigned peers = same_expert_lanes<NB>(e);
       const unsigned below = peers & lt_mask;
       int pos = 0;
-      if (e >= 0) pos = wc[e] + __popc(below);
+      if (e >= 0) pos = wcnt[e * kWStride + warp] + __popc(below);
       __syncwarp();
-      if (e >= 0 && below == 0u) wc[e] = pos + __popc(peers);  // the group's first lane
+      if (e >= 0 && below == 0u) wcnt[e * kWStride + warp] = pos + __popc(peers);  // the group's first lane
       __syncwarp();
       if (e >= 0) {
-        const long long i = w0 + r * kWarp + lane;
-        slot_of[i] = base[e] + pos;
-        const int q = tstart[e] + pos;
+        const int row = base[e] + pos;
+        slot_of[w0 + r * kWarp + lane] = row;
+        const int q = row - delta[e];
         stok[q] = t_cur;
         sexp[q] = (unsigned short)e;
       }
@@ -239,10 +241,9 @@ __global__ void __launch_bounds__(kPBlock) pft_scatter_kernel(const int* __restr
     }
     __syncthreads();
     // (d) write the sorted copy: consecutive entries of one expert go to consecutive rows
-    const int n = carry;  // valid entries of the tile
-    for (int q = threadIdx.x; q < n; q += blockDim.x) {
+    for (int q = threadIdx.x; q < carry; q += blockDim.x) {
       const int e = sexp[q];
-      const int row = base[e] + (q - tstart[e]);
+      const int row = q + delta[e];
       if ((unsigned)row < (unsigned)Tk) {  // always true when the counts agree; guards the writes
         token_ids[row] = stok[q];
         expert_ids[row] = e;
@@ -255,7 +256,17 @@ __global__ void __launch_bounds__(kPBlock) pft_scatter_kernel(const int* __restr
 }
 
 size_t scatter_smem(int E) {
-  return (size_t)(E + kPWarps * E + 2 * E + kTile) * sizeof(int) + (size_t)kTile * sizeof(unsigned short);
+  return (size_t)(E + kWStride * E + 2 * E + kTile) * sizeof(int) + (size_t)kTile * sizeof(unsigned short);
+}
+
+template <int NB>
+void launch_scatter(const int* idx, int Tk, int k, int E, int range, int G, const int* hist, const int* offsets,
+                    int* token_ids, int* expert_ids, int* slot_of, cudaStream_t st) {
+  const size_t smem = scatter_smem(E);
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(pft_scatter_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  pft_scatter_kernel<NB><<<G, kPBlock, smem, st>>>(idx, Tk, k, E, range, G, hist, offsets, token_ids, expert_ids,
+                                                   slot_of);
 }
 
 }  // namespace
@@ -286,13 +297,13 @@ void launch_pft_build(const int* topk_idx, int T, int E, int k, int* num_ids, in
   count_launch(st);
   pft_scan_kernel<<<E, kScanBlock, 0, st>>>(hist, G, E, num_ids, offsets, hdr);
   count_launch(st);
-  const size_t smem = scatter_smem(E);
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(pft_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  int nbits = 0;  // bits that hold every id below E
-  while ((1 << nbits) < E) ++nbits;
-  pft_scatter_kernel<<<G, kPBlock, smem, st>>>(topk_idx, Tk, k, E, nbits, range, G, hist, offsets, token_ids,
-                                                expert_ids, slot_of);
+  // bits that hold every id below E (at most 10: E <= 1024)
+  const int Tk32 = (int)Tk, range32 = (int)range;
+  if (E <= 64) launch_scatter<6>(topk_idx, Tk32, k, E, range32, G, hist, offsets, token_ids, expert_ids, slot_of, st);
+  else if (E <= 128) launch_scatter<7>(topk_idx, Tk32, k, E, range32, G, hist, offsets, token_ids, expert_ids, slot_of, st);
+  else if (E <= 256) launch_scatter<8>(topk_idx, Tk32, k, E, range32, G, hist, offsets, token_ids, expert_ids, slot_of, st);
+  else if (E <= 512) launch_scatter<9>(topk_idx, Tk32, k, E, range32, G, hist, offsets, token_ids, expert_ids, slot_of, st);
+  else launch_scatter<10>(topk_idx, Tk32, k, E, range32, G, hist, offsets, token_ids, expert_ids, slot_of, st);
   count_launch(st);
 }
 
