@@ -10,7 +10,7 @@
 //      the ranges (the expert's rows that earlier ranges hold) and writes the expert's total to
 //      num_ids; the last CTA to finish (a ticket from an atomic counter in the workspace header)
 //      scans num_ids into offsets and resets the counter for the next call.
-//   3. pft_scatter: each CTA walks its range in tiles of 4096 entries.  A warp owns 256
+//   3. pft_scatter: each CTA walks its range in tiles of 2048 entries.  A warp owns 256
 //      consecutive entries of a tile; per-warp counts in shared memory, and the lanes that share an
 //      expert in each round of 32 (ballots over the bits of the id), give every entry its rank
 //      among the same expert's entries of the tile, in index order.  slot_of is written in index order; token_ids and expert_ids go through a
@@ -23,9 +23,10 @@ namespace moe {
 
 namespace {
 
-constexpr int kPBlock = 512;                 // threads of the count and scatter CTAs
-constexpr int kPWarps = kPBlock / kWarp;     // 16
-constexpr int kTile = 4096;                  // entries of one scatter tile
+constexpr int kPBlock = 512;                 // threads of the count CTAs
+constexpr int kSBlock = 256;                 // threads of the scatter CTAs
+constexpr int kPWarps = kSBlock / kWarp;     // 8 warps per scatter CTA
+constexpr int kTile = 2048;                  // entries of one scatter tile
 constexpr int kPerWarp = kTile / kPWarps;    // 256 consecutive entries per warp
 constexpr int kRounds = kPerWarp / kWarp;    // 8 rounds of 32
 constexpr int kMaxRanges = 608;              // 4 CTAs on each of 152 SMs (fixed: sizes the workspace)
@@ -147,7 +148,7 @@ constexpr int kWStride = kPWarps + 1;  // per-expert row of the per-warp count t
 // (per-warp counts, then each warp's start inside the tile's bucket), delta[E] (global row minus
 // position in the tile's sorted copy), tcnt[E], stok[kTile], sexp[kTile] (uint16).
 template <int NB>
-__global__ void __launch_bounds__(kPBlock, 2) pft_scatter_kernel(const int* __restrict__ idx, int Tk, int k, int E,
+__global__ void __launch_bounds__(kSBlock, 4) pft_scatter_kernel(const int* __restrict__ idx, int Tk, int k, int E,
                                                                  int range, int G, const int* __restrict__ hist,
                                                                  const int* __restrict__ offsets,
                                                                  int* __restrict__ token_ids,
@@ -165,28 +166,34 @@ __global__ void __launch_bounds__(kPBlock, 2) pft_scatter_kernel(const int* __re
   const unsigned lt_mask = (1u << lane) - 1u;
   for (int e = threadIdx.x; e < E; e += blockDim.x)
     base[e] = __ldg(offsets + e) + __ldcg(hist + (size_t)e * G + blockIdx.x);
+  __syncthreads();
   const int beg = blockIdx.x * range;
   const int end = min(beg + range, Tk);
   const int dt = kWarp / k, dj = kWarp % k;
+  // this warp's 256 consecutive entries of a tile, 8 per lane in rounds of 32 (the next tile's
+  // ids are loaded while the current one is written out)
+  int nx[kRounds];
+#pragma unroll
+  for (int r = 0; r < kRounds; ++r) {
+    const int i = beg + warp * kPerWarp + r * kWarp + lane;
+    nx[r] = i < end ? __ldg(idx + i) : -1;
+  }
   for (int t0 = beg; t0 < end; t0 += kTile) {
-    // (a) this warp's 256 consecutive entries, 8 per lane in rounds of 32; per-warp counts
+    // (a) per-warp counts of the tile
     for (int q = threadIdx.x; q < kWStride * E; q += blockDim.x) wcnt[q] = 0;
-    __syncthreads();
     const int w0 = t0 + warp * kPerWarp;
     int ev[kRounds];
 #pragma unroll
     for (int r = 0; r < kRounds; ++r) {
       const int i = w0 + r * kWarp + lane;
-      int e = -1;
-      if (i < end) {
-        e = __ldg(idx + i);
-        if ((unsigned)e >= (unsigned)E) {
-          slot_of[i] = -1;  // reported by pft_count
-          e = -1;
-        }
+      int e = nx[r];
+      if (i < end && (unsigned)e >= (unsigned)E) {
+        slot_of[i] = -1;  // reported by pft_count
+        e = -1;
       }
-      ev[r] = e;
+      ev[r] = i < end ? e : -1;
     }
+    __syncthreads();
 #pragma unroll
     for (int r = 0; r < kRounds; ++r)
       if (ev[r] >= 0) atomicAdd(&wcnt[ev[r] * kWStride + warp], 1);
@@ -206,7 +213,7 @@ __global__ void __launch_bounds__(kPBlock, 2) pft_scatter_kernel(const int* __re
     __syncthreads();
     // bucket starts of the tile's sorted copy: exclusive scan of tcnt over the experts
     int carry = 0;
-    for (int e0 = 0; e0 < E; e0 += kPBlock) {
+    for (int e0 = 0; e0 < E; e0 += kSBlock) {
       const int q = e0 + threadIdx.x;
       const int v = q < E ? tcnt[q] : 0;
       int tot;
@@ -239,6 +246,11 @@ __global__ void __launch_bounds__(kPBlock, 2) pft_scatter_kernel(const int* __re
       j_cur += dj;
       if (j_cur >= k) { j_cur -= k; ++t_cur; }
     }
+#pragma unroll
+    for (int r = 0; r < kRounds; ++r) {
+      const int i = w0 + kTile + r * kWarp + lane;
+      nx[r] = i < end ? __ldg(idx + i) : -1;
+    }
     __syncthreads();
     // (d) write the sorted copy: consecutive entries of one expert go to consecutive rows
     for (int q = threadIdx.x; q < carry; q += blockDim.x) {
@@ -265,7 +277,7 @@ void launch_scatter(const int* idx, int Tk, int k, int E, int range, int G, cons
   const size_t smem = scatter_smem(E);
   if (smem > 48 * 1024)
     cudaFuncSetAttribute(pft_scatter_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  pft_scatter_kernel<NB><<<G, kPBlock, smem, st>>>(idx, Tk, k, E, range, G, hist, offsets, token_ids, expert_ids,
+  pft_scatter_kernel<NB><<<G, kSBlock, smem, st>>>(idx, Tk, k, E, range, G, hist, offsets, token_ids, expert_ids,
                                                    slot_of);
 }
 
