@@ -371,7 +371,9 @@ def kernel_names(stage, n, w):
                      CSRC + "gemm_simt.cu")
     table = {
         "route": route,
-        "pft_build": (["pft_hist", "pft_scatter"], CSRC + "pft.cu"),
+        # few ranges: the count kernel's last CTA also scans; otherwise a scan kernel between
+        "pft_build": ((["pft_count_scan", "pft_scatter"] if n == 2 else ["pft_count", "pft_scan", "pft_scatter"]),
+                      CSRC + "pft.cu"),
         "dispatch": (["dispatch"], CSRC + "gather.cu"),
         "expert_ffn": ((["tc_GATEUP", "tc_DOWN"], CSRC + "gemm_tc.cu") if tc
                        else ((["simt_gateup", "simt_down"] if n == 2 else ["simt_h1", "simt_h3_swiglu", "simt_down"]),
@@ -401,7 +403,9 @@ def kernel_counts(w, T, e_active):
         "router_gemm": {"flops": 2 * T * h * E, "bytes": T * h * s + h * E * 4 + T * E * 4},
         "router_splitk_reduce": {"flops": 0, "bytes": 2 * T * E * 4},
         "softmax_topk": {"flops": 0, "bytes": 2 * T * E * 4 + 8 * Tk},
-        "pft_hist": {"flops": 0, "bytes": 4 * Tk},
+        "pft_count": {"flops": 0, "bytes": 4 * Tk},
+        "pft_count_scan": {"flops": 0, "bytes": 4 * Tk + 8 * E},
+        "pft_scan": {"flops": 0, "bytes": 8 * E},
         "pft_scatter": {"flops": 0, "bytes": 16 * Tk},
         "dispatch": {"flops": 0, "bytes": T * h * s + Tk * h * s + 4 * Tk},
         "tc_GATEUP": {"flops": 4 * Tk * h * f, "bytes": 2 * e_active * Wb + Tk * h * s + 3 * Tk * f * s},
@@ -608,7 +612,7 @@ def measure_pft_scaled(binding, flush, peaks, steps=20, T=1 << 20, k=8, E=256, s
     assert binding.moe_check_status(ws) == 0, "device status set by the scaled PFT build"
     us = 1e3 * sum(a.elapsed_time(e) for a, e in ev) / steps
     kus = {}
-    names = ["pft_hist", "pft_scatter"]
+    names = ["pft_count", "pft_scan", "pft_scatter"]
     for s, (n0, n1) in enumerate(per_kernel):
         prev = ev[s][0]
         for j, q in enumerate(range(n0, n1)):

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_pft.so")
 
-SOURCES = ["api.cu", "gather.cu", "route.cu", "pft.cu", "pft_noalloc.cu", "gemm_simt.cu", "gemm_tc.cu", "router_tc.cu", "gshard.cu"]
+SOURCES = ["api.cu", "gather.cu", "route.cu", "pft.cu", "pft_noalloc.cu", "gemm_simt.cu", "gemm_tc.cu", "router_tc.cu", "gshard.cu", "gemm_f32tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", INCLUDE, "-I", CSRC]

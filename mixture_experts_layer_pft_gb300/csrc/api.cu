@@ -164,6 +164,9 @@ size_t moe_workspace_size(int op, int T, int h, int E, int k, int f, int dtype) 
     }
     case MOE_OP_PFT_BUILD:
       return hdr + round256(pft_scratch_bytes(std::max(Tk, 1LL), std::max(E, 1)));
+    case MOE_OP_EXPERT_FFN:
+      // the fp32 forward on the tensor cores keeps bf16 planes of its operands in the workspace
+      return hdr + (Tk > 0 && f32tc_supported(dtype, h, f, E) ? f32tc_scratch(Tk, E, h, f) : 0);
     case MOE_OP_EXPERT_FFN_BWD:
       return hdr + 2 * round256((size_t)Tk * std::max(f, 0) * esize(dtype));
     case MOE_OP_GSHARD:
@@ -342,6 +345,13 @@ int expert_ffn_impl(const char* fn, TokenRows xr, const int32_t* offsets, const 
   REQUIRE_PTR(ybuf); REQUIRE_PTR(h1); REQUIRE_PTR(h3); REQUIRE_PTR(a);
   if (use_tensor_cores(dtype, h, f)) {
     if (tc_expert_ffn(xr, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, status_of(ws), st, fold) != 0)
+      return tc_failure(fn);
+  } else if (f32tc_supported(dtype, h, f, E)) {
+    REQUIRE(aligned16(ws), MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace not 16-byte aligned");
+    if (f32tc_expert_ffn(static_cast<const float*>(xr.xbuf), offsets, static_cast<const float*>(W1),
+                         static_cast<const float*>(W3), static_cast<const float*>(W2), Tk, E, h, f,
+                         static_cast<float*>(ybuf), static_cast<float*>(h1), static_cast<float*>(h3),
+                         static_cast<float*>(a), static_cast<char*>(ws) + sizeof(WsHeader), status_of(ws), st) != 0)
       return tc_failure(fn);
   } else {
     simt_expert_ffn(dtype, xr.xbuf, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, st);

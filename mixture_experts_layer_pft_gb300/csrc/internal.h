@@ -84,6 +84,15 @@ int tc_router_logits(const void* x, const float* Wg, const float* bias, int T, i
 int tc_router_bwd(const void* x, const float* Wg, const float* d_logits, int T, int h, int E, float* dWg,
                   float* dx_router, void* scratch, bool dl_planes_ready, int* status, cudaStream_t st);
 
+// gemm_f32tc.cu -- the fp32 expert forward on tcgen05 over exact three-plane bf16 splits (h and f
+// multiples of 128).  The scratch (token planes of xbuf and a, one weight tensor's planes) follows
+// the workspace header.
+bool f32tc_supported(int dtype, int h, int f, int E);
+size_t f32tc_scratch(long long Tk, int E, int h, int f);
+int f32tc_expert_ffn(const float* xbuf, const int* offsets, const float* W1, const float* W3, const float* W2,
+                     int Tk, int E, int h, int f, float* ybuf, float* h1, float* h3, float* a, void* scratch,
+                     int* status, cudaStream_t st);
+
 // gemm_tc.cu -- tcgen05/TMEM/TMA grouped GEMMs (bf16; h and f multiples of 128)
 bool tc_supported(int dtype, int h, int f);
 // Token rows of the padding-free buffer: either xbuf itself ([Tk,h]), or, with xbuf null, row p

@@ -3,7 +3,8 @@
 // Flattened entry i = t*k + j carries expert e_i = topk_idx[t][j].  For a fixed expert the
 // entries are distinct tokens, so ascending i is ascending t and a STABLE counting sort on e
 // gives the unique (expert, token) order.  The entries are cut into G contiguous ranges, one per
-// CTA, and three launches sort them with no spin-waits:
+// CTA, and three launches sort them with no spin-waits (two when G <= 64: the count kernel's last
+// CTA does the scan):
 //   1. pft_count: each CTA counts its range per expert (shared-memory atomic adds, eight loads in
 //      flight per thread) and writes one column of the expert-major table hist[e][c].
 //   2. pft_scan: one CTA per expert turns its row of the table into the exclusive prefix over
@@ -33,10 +34,19 @@ constexpr int kMaxRanges = 608;              // 4 CTAs on each of 152 SMs (fixed
 constexpr int kScanBlock = 256;
 
 // ---------------------------------------------------------------------------- 1. count
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* total);
+__device__ void scan_ranges_and_experts(int* hist, int G, int E, int* num_ids, int* offsets, int* warp_tot);
+
+// With fused_scan (few ranges) the last CTA to finish (a ticket from the workspace header's
+// counter) also does pft_scan's work, so that small builds take two launches.
 __global__ void __launch_bounds__(kPBlock) pft_count_kernel(const int* __restrict__ idx, long long Tk, int E,
                                                             long long range, int G, int* __restrict__ hist,
-                                                            int* status) {
+                                                            WsHeader* hdr, bool fused_scan, int* __restrict__ num_ids,
+                                                            int* __restrict__ offsets) {
   extern __shared__ int cnt[];  // [E]
+  __shared__ int warp_tot[kPBlock / kWarp];
+  __shared__ int is_last;
+  int* status = &hdr->status;
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
   const long long beg = (long long)blockIdx.x * range;
@@ -63,6 +73,15 @@ __global__ void __launch_bounds__(kPBlock) pft_count_kernel(const int* __restric
   if (bad) flag_status(status, MOE_STATUS_BAD_INDEX);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(size_t)e * G + blockIdx.x] = cnt[e];
+  if (!fused_scan) return;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(&hdr->pft_done, 1u) == (unsigned)(G - 1);
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  scan_ranges_and_experts(hist, G, E, num_ids, offsets, warp_tot);
+  if (threadIdx.x == 0) hdr->pft_done = 0u;
 }
 
 // ---------------------------------------------------------------------------- 2. scan
@@ -85,6 +104,32 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int* t
   __syncthreads();
   *total = all;
   return before + incl - v;
+}
+
+// One CTA: each expert's row of the table turned into its exclusive prefix over the ranges (a
+// thread per expert walks its G <= 64 entries), the totals into num_ids, their scan into offsets.
+__device__ void scan_ranges_and_experts(int* hist, int G, int E, int* num_ids, int* offsets, int* warp_tot) {
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int* row = hist + (size_t)e * G;
+    int run = 0;
+    for (int c = 0; c < G; ++c) {
+      const int v = __ldcg(row + c);
+      row[c] = run;
+      run += v;
+    }
+    num_ids[e] = run;
+  }
+  __syncthreads();
+  int carry = 0;
+  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+    const int q = e0 + threadIdx.x;
+    const int v = q < E ? num_ids[q] : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, warp_tot, &tot);
+    if (q < E) offsets[q] = carry + ex;
+    carry += tot;
+  }
+  if (threadIdx.x == 0) offsets[E] = carry;
 }
 
 __global__ void __launch_bounds__(kScanBlock) pft_scan_kernel(int* __restrict__ hist, int G, int E,
@@ -305,10 +350,14 @@ void launch_pft_build(const int* topk_idx, int T, int E, int k, int* num_ids, in
   const long long range = pft_chunk_size(Tk);
   WsHeader* hdr = static_cast<WsHeader*>(ws);
   int* hist = reinterpret_cast<int*>(static_cast<char*>(ws) + sizeof(WsHeader));
-  pft_count_kernel<<<G, kPBlock, (size_t)E * sizeof(int), st>>>(topk_idx, Tk, E, range, G, hist, &hdr->status);
+  const bool fused_scan = G <= 64;  // few ranges: the count kernel's last CTA scans them
+  pft_count_kernel<<<G, kPBlock, (size_t)E * sizeof(int), st>>>(topk_idx, Tk, E, range, G, hist, hdr, fused_scan,
+                                                                 num_ids, offsets);
   count_launch(st);
-  pft_scan_kernel<<<E, kScanBlock, 0, st>>>(hist, G, E, num_ids, offsets, hdr);
-  count_launch(st);
+  if (!fused_scan) {
+    pft_scan_kernel<<<E, kScanBlock, 0, st>>>(hist, G, E, num_ids, offsets, hdr);
+    count_launch(st);
+  }
   // bits that hold every id below E (at most 10: E <= 1024)
   const int Tk32 = (int)Tk, range32 = (int)range;
   if (E <= 64) launch_scatter<6>(topk_idx, Tk32, k, E, range32, G, hist, offsets, token_ids, expert_ids, slot_of, st);

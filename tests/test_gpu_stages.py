@@ -389,6 +389,10 @@ EXPERT_SHAPES = [
     (600, 256, 4, 2, 256, torch.bfloat16, False),   # > 160 rows per expert: 256-row gate/up chunks
     (520, 384, 4, 2, 128, torch.bfloat16, True),    # 256-row chunks over Zipf-sized segments
     (400, 512, 80, 2, 512, torch.bfloat16, False),  # 160 paired units: the last 8 split into M tiles
+    # fp32 on the tensor cores over exact bf16 planes (h and f multiples of 128)
+    (700, 256, 12, 3, 256, torch.float32, True),    # Zipf segments, several 128-token chunks
+    (300, 512, 8, 2, 384, torch.float32, False),    # K = 512 and 384: two and 1.5 drains of 256
+    (64, 1024, 4, 1, 128, torch.float32, False),    # K = 1024 (four drains), one chunk per expert
 ]
 
 
@@ -415,6 +419,34 @@ def test_tensor_core_engine_matches_simt_engine(B, monkeypatch, T, h, E, k, f, s
     assert B.moe_check_status(ws) == 0
     for n in outs["tc"]:
         assert rel_l2(np64(outs["tc"][n]), np64(outs["simt"][n])) <= TOL["bf16"], n
+
+
+@pytest.mark.parametrize("T,h,E,k,f,skew", [(640, 256, 8, 2, 256, False), (900, 384, 16, 4, 128, True),
+                                             (2048, 2048, 32, 2, 2048, True)])
+def test_fp32_tensor_core_forward_matches_the_fma_engine(B, monkeypatch, T, h, E, k, f, skew):
+    """The fp32 forward over exact bf16 planes on the tensor cores against the FP32 FMA engine and
+    the oracle: both within the fp32 tolerance, expert segment by expert segment."""
+    p, d = expert_inputs(T, h, E, k, f, torch.float32, 90 + T, skew)
+    Tk = T * k
+    outs = {}
+    for engine in ("tc", "simt"):
+        if engine == "simt":
+            monkeypatch.setenv("MOE_PFT_GEMM", "simt")
+        z = lambda *s: torch.empty(*s, dtype=torch.float32, device="cuda")  # noqa: E731
+        ybuf, h1, h3, a = z(Tk, h), z(Tk, f), z(Tk, f), z(Tk, f)
+        ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, torch.float32)
+        B.moe_expert_ffn(d["xbuf"], d["offsets"], d["W1"], d["W3"], d["W2"], ybuf, h1, h3, a, ws)
+        assert B.moe_check_status(ws) == 0
+        outs[engine] = {"ybuf": np64(ybuf), "h1": np64(h1), "h3": np64(h3), "a": np64(a)}
+        monkeypatch.delenv("MOE_PFT_GEMM", raising=False)
+    want = O.expert_ffn(np64(d["xbuf"]), p["offsets"], np64(d["W1"]), np64(d["W3"]), np64(d["W2"]), "f32")
+    off = p["offsets"]
+    for n in ("ybuf", "h1", "h3", "a"):
+        for e in range(E):
+            if off[e + 1] > off[e]:
+                sl = slice(off[e], off[e + 1])
+                assert rel_l2(outs["tc"][n][sl], want[n][sl]) <= TOL["f32"], (n, e)
+                assert rel_l2(outs["tc"][n][sl], outs["simt"][n][sl]) <= TOL["f32"], (n, e)
 
 
 @pytest.mark.parametrize("h,f", [(256, 384), (384, 256)])

@@ -155,6 +155,31 @@ def test_router_gemms_time_out_and_recover(B):
     _run_twice_with_a_timeout_between(B, ws, bwd, [d_logits, dWg, dxr], 2)
 
 
+def test_fp32_tensor_core_gemm_times_out_and_recovers(B):
+    """The fp32 forward over bf16 planes: its first GEMM withheld, then all three."""
+    from mixture_experts_layer_pft_gb300.workloads import random_logits, random_tensor
+
+    T, h, E, k, f = 256, 256, 4, 2, 256
+    idx = torch.topk(random_logits(T, E, 65, "cuda"), k, dim=1).indices
+    counts = torch.bincount(idx.flatten(), minlength=E)
+    offsets = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
+    offsets[1:] = torch.cumsum(counts, 0).to(torch.int32)
+    Tk = T * k
+    xbuf = random_tensor((Tk, h), 66, torch.float32, "cuda")
+    W1 = random_tensor((E, h, f), 67, torch.float32, "cuda", std=h ** -0.5)
+    W3 = random_tensor((E, h, f), 68, torch.float32, "cuda", std=h ** -0.5)
+    W2 = random_tensor((E, f, h), 69, torch.float32, "cuda", std=f ** -0.5)
+    z = lambda *s: torch.empty(*s, dtype=torch.float32, device="cuda")  # noqa: E731
+    ybuf, h1, h3, a = z(Tk, h), z(Tk, f), z(Tk, f), z(Tk, f)
+    ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, torch.float32)
+
+    def call():
+        B.moe_expert_ffn(xbuf, offsets, W1, W3, W2, ybuf, h1, h3, a, ws)
+
+    _run_twice_with_a_timeout_between(B, ws, call, [ybuf, h1, h3, a], 1)
+    _run_twice_with_a_timeout_between(B, ws, call, [ybuf, h1, h3, a], 3)
+
+
 def test_hook_is_off_by_default_and_cancels(B):
     """A cancelled request leaves the next launch alone."""
     T, h, E, k, f = 256, 256, 4, 2, 128
