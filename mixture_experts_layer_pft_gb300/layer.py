@@ -196,7 +196,10 @@ class GShardBuffers:
         self.a = torch.empty(E * C, f, dtype=dtype, **d)
         self.ye = torch.empty(E, C, h, dtype=dtype, **d)
         self.y = torch.empty(T, h, dtype=dtype, **d)
-        self.ws = B.new_workspace(B.MOE_OP_ALL, T, h, E, k, f, dtype, device)
+        # the experts run on E*C padded rows, more than the T*k of the padding-free layer
+        nbytes = max(B.workspace_size(B.MOE_OP_ALL, T, h, E, k, f, dtype),
+                     B.workspace_size(B.MOE_OP_EXPERT_FFN, E * C, h, E, 1, f, dtype))
+        self.ws = torch.zeros(nbytes, dtype=torch.uint8, device=device)
         self.ws_gshard = B.new_workspace(B.MOE_OP_GSHARD, T, h, E, k, f, dtype, device)
 
 
