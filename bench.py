@@ -357,6 +357,7 @@ def kernel_names(stage, n, w):
     simt_only = os.environ.get("MOE_PFT_GEMM") == "simt"
     tc = w.dtype == "bf16" and w.h % 128 == 0 and w.f % 128 == 0 and not simt_only
     tc_router = w.dtype == "bf16" and w.h % 64 == 0 and w.E % 16 == 0 and w.E >= 64 and not simt_only
+    f32tc = w.dtype == "f32" and w.h % 128 == 0 and w.f % 128 == 0 and not simt_only
     if tc_router:
         route = (["router_split_w", "tc_router_fwd", "softmax_topk"], CSRC + "router_tc.cu")
         # route_dlogits also writes d_logits' bf16 planes; the top-k kernel finishes a K-split logits GEMM
@@ -376,6 +377,8 @@ def kernel_names(stage, n, w):
                       CSRC + "pft.cu"),
         "dispatch": (["dispatch"], CSRC + "gather.cu"),
         "expert_ffn": ((["tc_GATEUP", "tc_DOWN"], CSRC + "gemm_tc.cu") if tc
+                       else (["f32_split_x", "f32_split_w1", "f32tc_H1", "f32_split_w3", "f32tc_H3A",
+                              "f32_split_w2", "f32tc_Y"], CSRC + "gemm_f32tc.cu") if f32tc
                        else ((["simt_gateup", "simt_down"] if n == 2 else ["simt_h1", "simt_h3_swiglu", "simt_down"]),
                              CSRC + "gemm_simt.cu")),
         "combine": (["combine"], CSRC + "gather.cu"),
@@ -428,6 +431,15 @@ def kernel_counts(w, T, e_active):
         "router_dx": {"flops": 2 * T * h * E, "bytes": T * E * 4 + h * E * 4 + T * h * 4},
         "dispatch_bwd": {"flops": 0, "bytes": Tk * h * s + T * h * s + T * h * 4 + 4 * Tk},
     }
+    # fp32 expert forward on the tensor cores: exact three-plane bf16 splits, then one GEMM per
+    # product (the FLOPs are the fp32 GEMM's; the tensor cores do six plane products for each)
+    d["f32_split_x"] = {"flops": 0, "bytes": Tk * h * 4 + 3 * Tk * h * 2}
+    for n in ("f32_split_w1", "f32_split_w3", "f32_split_w2"):
+        d[n] = {"flops": 0, "bytes": e_active * h * f * (4 + 6)}
+    d["f32tc_H1"] = {"flops": 2 * Tk * h * f, "bytes": 3 * e_active * h * f * 2 + 3 * Tk * h * 2 + Tk * f * 4}
+    d["f32tc_H3A"] = {"flops": 2 * Tk * h * f,
+                      "bytes": 3 * e_active * h * f * 2 + 3 * Tk * h * 2 + Tk * f * 4 * 3 + 3 * Tk * f * 2}
+    d["f32tc_Y"] = {"flops": 2 * Tk * h * f, "bytes": 3 * e_active * h * f * 2 + 3 * Tk * f * 2 + Tk * h * 4}
     d["simt_h1"] = {"flops": 2 * Tk * h * f, "bytes": e_active * Wb + Tk * h * s + Tk * f * s}
     d["simt_h3_swiglu"] = {"flops": 2 * Tk * h * f, "bytes": e_active * Wb + Tk * h * s + 3 * Tk * f * s}
     for a, bname in (("simt_gateup", "tc_GATEUP"), ("simt_down", "tc_DOWN"), ("simt_dA", "tc_DA"),
@@ -781,7 +793,13 @@ def run_ours(args, w):
     c = kc[dom]
     region_ms = ms_per_step * args.steps
     fkey = "bf16_tflops_sustained" if region_ms > 2000 else "bf16_tflops"
-    if dom.startswith("simt") or dom in ("router_gemm", "router_dwg", "router_dx"):
+    if dom.startswith("f32tc_"):
+        # six exact bf16 plane products per fp32 product: the tensor work is 6x the GEMM's FLOPs
+        roof = {"bound": "tensor", "achieved": 6 * c["flops"] / (dom_ms * 1e-3) / 1e12,
+                "peak": float(peaks[fkey]), "unit": "TFLOP/s"}
+        which = (f"MEASURED_PEAKS.json {fkey} ({'of measured' if peak_src == 'measured' else 'of fallback'}); "
+                 "achieved counts the six bf16 plane products of each fp32 product")
+    elif dom.startswith("simt") or dom in ("router_gemm", "router_dwg", "router_dx"):
         roof = {"bound": "alu", "achieved": c["flops"] / (dom_ms * 1e-3) / 1e12,
                 "peak": FP32_ALU_TFLOPS_NOMINAL, "unit": "TFLOP/s"}
         which = "derived FP32 FMA peak: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (nominal)"

@@ -290,21 +290,34 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
       // element (token n, weight column m) of the output; lanes hold consecutive m, so each store
       // instruction writes 32 consecutive floats of one token row
       const int m = w.m0 + q * 32 + lane;
+      if (MODE == H3A) {
+        // h1 in groups of 16 columns, all loads issued before the group's stores
 #pragma unroll
-      for (int n = 0; n < FBN; ++n) {
-        if (n < w.rows) {
-          const size_t o = (size_t)(w.row0 + n) * p.M + m;
-          const float v = run[n];
-          if (MODE == H3A) {
-            const float z1 = __ldg(p.h1 + o);
-            const float av = z1 * sigmoidf_(z1) * v;
-            p.out[o] = v;
-            p.a[o] = av;
-            split3_value(av, p.a_planes + o, p.a_planes + p.Tk * p.M + o, p.a_planes + 2 * p.Tk * p.M + o);
-          } else {
-            p.out[o] = v;
+        for (int g = 0; g < FBN / 16; ++g) {
+          if (16 * g >= w.rows) break;
+          float z1[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = 16 * g + i;
+            z1[i] = n < w.rows ? __ldg(p.h1 + (size_t)(w.row0 + n) * p.M + m) : 0.f;
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int n = 16 * g + i;
+            if (n < w.rows) {
+              const size_t o = (size_t)(w.row0 + n) * p.M + m;
+              const float v = run[n];
+              const float av = z1[i] * sigmoidf_(z1[i]) * v;
+              p.out[o] = v;
+              p.a[o] = av;
+              split3_value(av, p.a_planes + o, p.a_planes + p.Tk * p.M + o, p.a_planes + 2 * p.Tk * p.M + o);
+            }
           }
         }
+      } else {
+#pragma unroll
+        for (int n = 0; n < FBN; ++n)
+          if (n < w.rows) p.out[(size_t)(w.row0 + n) * p.M + m] = run[n];
       }
     }
   }
