@@ -356,14 +356,16 @@ def kernel_names(stage, n, w):
     """Names (and source file) of the n launches one stage call makes, in launch order."""
     simt_only = os.environ.get("MOE_PFT_GEMM") == "simt"
     tc = w.dtype == "bf16" and w.h % 128 == 0 and w.f % 128 == 0 and not simt_only
-    tc_router = w.dtype == "bf16" and w.h % 64 == 0 and w.E % 16 == 0 and w.E >= 64 and not simt_only
+    tc_router = w.h % 64 == 0 and w.E % 16 == 0 and w.E >= 64 and not simt_only
     f32tc = w.dtype == "f32" and w.h % 128 == 0 and w.f % 128 == 0 and not simt_only
     if tc_router:
-        route = (["router_split_w", "tc_router_fwd", "softmax_topk"], CSRC + "router_tc.cu")
+        # fp32 activations: x is split into bf16 planes too, before each of its two GEMMs
+        xs = ["router_split_x"] if w.dtype == "f32" else []
+        route = (["router_split_w"] + xs + ["tc_router_fwd", "softmax_topk"], CSRC + "router_tc.cu")
         # route_dlogits also writes d_logits' bf16 planes; the top-k kernel finishes a K-split logits GEMM
-        route_bwd = ((["route_dlogits", "tc_router_dwg", "router_split_w", "tc_router_dx"] if n == 4
-                      else ["route_dlogits", "tc_router_dwg", "router_dwg_splitk_reduce", "router_split_w",
-                            "tc_router_dx"]), CSRC + "router_tc.cu")
+        route_bwd = ((["route_dlogits"] + xs + ["tc_router_dwg", "router_split_w", "tc_router_dx"] if n == 4 + len(xs)
+                      else ["route_dlogits"] + xs + ["tc_router_dwg", "router_dwg_splitk_reduce", "router_split_w",
+                                                     "tc_router_dx"]), CSRC + "router_tc.cu")
     else:
         route = (["router_gemm", "softmax_topk"] if n == 2 else ["router_gemm", "router_splitk_reduce", "softmax_topk"],
                  CSRC + "gemm_simt.cu")
@@ -423,6 +425,7 @@ def kernel_counts(w, T, e_active):
         # tensor-core router: exact three-plane bf16 splits of the fp32 operands, then the GEMMs
         "router_split_w": {"flops": 0, "bytes": h * E * 4 + 3 * h * E * 2},
         "router_split_dl": {"flops": 0, "bytes": T * E * 4 + 3 * T * E * 2},
+        "router_split_x": {"flops": 0, "bytes": T * h * 4 + 3 * T * h * 2},
         "tc_router_fwd": {"flops": 2 * T * h * E, "bytes": T * h * s + 3 * h * E * 2 + T * E * 4},
         "tc_router_dwg": {"flops": 2 * T * h * E, "bytes": T * h * s + 3 * T * E * 2 + h * E * 4},
         "tc_router_dx": {"flops": 2 * T * h * E, "bytes": 3 * T * E * 2 + 3 * h * E * 2 + T * h * 4},

@@ -46,7 +46,9 @@ int tc_failure(const char* what) {
 }
 
 // Shapes the tensor-core router takes (the workspace is sized for them whatever the engine).
-bool router_tc_shape(int dtype, int h, int E) { return dtype == MOE_BF16 && h % 64 == 0 && E % 16 == 0 && E >= 64; }
+bool router_tc_shape(int dtype, int h, int E) {
+  return (dtype == MOE_BF16 || dtype == MOE_F32) && h % 64 == 0 && E % 16 == 0 && E >= 64;
+}
 
 bool use_tensor_cores(int dtype, int h, int f) {
   const char* env = getenv("MOE_PFT_GEMM");
@@ -153,13 +155,13 @@ size_t moe_workspace_size(int op, int T, int h, int E, int k, int f, int dtype) 
     case MOE_OP_ROUTE: {
       const int sp = (T > 0 && h > 0 && E > 0) ? router_splits(T, E, h) : 1;
       size_t b = sp > 1 ? round256((size_t)sp * T * E * sizeof(float)) : 0;
-      if (T > 0 && router_tc_shape(dtype, h, E)) b = std::max(b, tc_router_scratch(0, T, h, E));
+      if (T > 0 && router_tc_shape(dtype, h, E)) b = std::max(b, tc_router_scratch(0, T, h, E, dtype));
       return hdr + b;
     }
     case MOE_OP_ROUTE_BWD: {
       const int sp = (T > 0 && h > 0 && E > 0) ? router_splits(h, E, T) : 1;
       size_t b = sp > 1 ? round256((size_t)sp * h * E * sizeof(float)) : 0;
-      if (T > 0 && router_tc_shape(dtype, h, E)) b = std::max(b, tc_router_scratch(1, T, h, E));
+      if (T > 0 && router_tc_shape(dtype, h, E)) b = std::max(b, tc_router_scratch(1, T, h, E, dtype));
       return hdr + b;
     }
     case MOE_OP_PFT_BUILD:
@@ -223,7 +225,7 @@ int moe_route(const void* x, const float* Wg, const float* bias, int T, int h, i
     char* scratch = static_cast<char*>(ws) + sizeof(WsHeader);
     if (tc_router_supported(dtype, h, E)) {
       REQUIRE(aligned16(x) && aligned16(logits), MOE_ERR_INVALID_ARG, "moe_route: x or logits not aligned");
-      if (tc_router_logits(x, Wg, bias, T, h, E, logits, scratch, &partial, &slices, status_of(ws), st) != 0)
+      if (tc_router_logits(x, Wg, bias, T, h, E, dtype, logits, scratch, &partial, &slices, status_of(ws), st) != 0)
         return tc_failure("moe_route");
     } else {
       simt_router_logits(dtype, x, Wg, bias, T, h, E, logits, reinterpret_cast<float*>(scratch), st);
@@ -265,7 +267,7 @@ int moe_route_bwd(const void* x, const float* Wg, const float* probs, const int3
   launch_route_dlogits(probs, topk_idx, d_topk_w, T, E, k, (flags & MOE_ROUTE_SIGMOID) != 0,
                        (flags & MOE_ROUTE_RENORM) != 0, d_logits, tc ? scratch : nullptr, status_of(ws), st);
   if (tc) {
-    if (tc_router_bwd(x, Wg, d_logits, T, h, E, dWg, dx_router, scratch, true, status_of(ws), st) != 0)
+    if (tc_router_bwd(x, Wg, d_logits, T, h, E, dtype, dWg, dx_router, scratch, true, status_of(ws), st) != 0)
       return tc_failure("moe_route_bwd");
   } else {
     simt_router_dwg(dtype, x, d_logits, T, h, E, dWg, reinterpret_cast<float*>(scratch), st);

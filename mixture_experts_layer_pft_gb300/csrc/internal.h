@@ -72,17 +72,18 @@ void simt_expert_ffn_bwd(int dtype, const void* dybuf, const void* xbuf, const v
                          const void* W3, const void* W2, int Tk, int E, int h, int f, void* dxbuf,
                          void* dW1, void* dW3, void* dW2, void* dh1, void* dh3, cudaStream_t st);
 
-// router_tc.cu -- router GEMMs on tcgen05 over exact three-plane bf16 splits (bf16 activations,
-// h a multiple of 64, E of 16).  The scratch follows the workspace header, 256-byte aligned.
+// router_tc.cu -- router GEMMs on tcgen05 over exact three-plane bf16 splits (bf16 or fp32
+// activations, h a multiple of 64, E of 16).  The scratch follows the workspace header, 256-byte aligned.
 bool tc_router_supported(int dtype, int h, int E);
-size_t tc_router_scratch(int op, int T, int h, int E);  // op 0: forward, 1: backward
+size_t tc_router_scratch(int op, int T, int h, int E, int dtype);  // op 0: forward, 1: backward
 // The forward leaves several K slices' partials for launch_softmax_topk to add (*partial_out,
 // *slices_out; nullptr and 1 when the logits were written directly).  The backward splits
 // d_logits itself unless route_dlogits already wrote its planes at the start of `scratch`.
-int tc_router_logits(const void* x, const float* Wg, const float* bias, int T, int h, int E, float* logits,
-                     void* scratch, const float** partial_out, int* slices_out, int* status, cudaStream_t st);
-int tc_router_bwd(const void* x, const float* Wg, const float* d_logits, int T, int h, int E, float* dWg,
-                  float* dx_router, void* scratch, bool dl_planes_ready, int* status, cudaStream_t st);
+int tc_router_logits(const void* x, const float* Wg, const float* bias, int T, int h, int E, int dtype,
+                     float* logits, void* scratch, const float** partial_out, int* slices_out, int* status,
+                     cudaStream_t st);
+int tc_router_bwd(const void* x, const float* Wg, const float* d_logits, int T, int h, int E, int dtype,
+                  float* dWg, float* dx_router, void* scratch, bool dl_planes_ready, int* status, cudaStream_t st);
 
 // gemm_f32tc.cu -- the fp32 expert forward on tcgen05 over exact three-plane bf16 splits (h and f
 // multiples of 128).  The scratch (token planes of xbuf and a, one weight tensor's planes) follows

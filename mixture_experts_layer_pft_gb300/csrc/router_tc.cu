@@ -1,11 +1,12 @@
 // Router GEMMs on the tensor cores with fp32-faithful sums (sm_103a: tcgen05 + TMEM + TMA).
 //
 // Gating is an fp32 computation: logits = x Wg (+ bias), and in the backward dWg = x^T dL and
-// dx = dL Wg^T, with x in bf16 and Wg, dL in fp32.  Every fp32 operand is first split exactly into
+// dx = dL Wg^T, with x in bf16 or fp32 and Wg, dL in fp32.  Every fp32 operand is first split exactly into
 // three bf16 planes, v = v0 + v1 + v2 with v0 = bf16(v), v1 = bf16(v - v0), v2 = v - v0 - v1, so
 // that every product of two planes is exact in fp32 and the operand products the layer needs are
 // sums of plane products:
-//   x w      = x w0 + x w1 + x w2                             (x is bf16: one plane)
+//   x w      = x w0 + x w1 + x w2                             (bf16 x: one plane; fp32 x is split
+//                                                              too and takes the six-term sum below)
 //   a b      = a0 b0 + a0 b1 + a1 b0 + a0 b2 + a1 b1 + a2 b0   (both fp32; the dropped terms
 //                                                              a1 b2, a2 b1, a2 b2 are below 2^-32
 //                                                              of the product)
@@ -18,6 +19,7 @@
 //   FWD    logits [T x E]     x [T, h] bf16 (K-major)             Wg planes [h, E] (MN-major)
 //   DWG    dWg [h x E]        x [T, h] bf16 (MN-major), K = T     dL planes [T, E] (MN-major)
 //   DX     dx [T x h]         dL planes [T, E] (K-major), K = E   Wg planes [h, E] (K-major)
+//   FWD3, DWG3: FWD and DWG with three planes of fp32 x
 //
 // One persistent CTA per SM walks units (slice z of K, M tile, N tile of 128): warp 0 issues the
 // TMA loads, warp 1 owns TMEM (two buffers of the accumulator pair) and issues the MMAs, warps 2-5
@@ -46,12 +48,14 @@ constexpr int kChunkSteps = 4;  // stages per drain: 256 of K
 constexpr int kRThreads = 192;  // producer, MMA, four epilogue warps
 constexpr uint32_t kPlane = 16384;  // bytes of one 128 x 64 bf16 plane tile
 
-enum RMode { FWD = 0, DWG = 1, DX = 2 };
+// FWD3 and DWG3 are FWD and DWG for fp32 activations: x is split into three planes too, and
+// every product is the six-term plane sum that DX uses.
+enum RMode { FWD = 0, DWG = 1, DX = 2, FWD3 = 3, DWG3 = 4 };
 
 template <int MODE> struct RCfg {
-  static constexpr int NA = (MODE == DX) ? 3 : 1;  // A planes
+  static constexpr int NA = (MODE == DX || MODE == FWD3 || MODE == DWG3) ? 3 : 1;  // A planes
   static constexpr int NB = 3;                     // B planes
-  static constexpr bool A_MN = (MODE == DWG);
+  static constexpr bool A_MN = (MODE == DWG || MODE == DWG3);
   static constexpr bool B_MN = (MODE != DX);
   static constexpr uint32_t STAGE_BYTES = (NA + NB) * kPlane;
   static constexpr int STAGES = 196608 / STAGE_BYTES;
@@ -152,8 +156,8 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
 #pragma unroll
           for (int i = 0; i < C::NA; ++i) {
             if (C::A_MN) {  // x [T, h]: rows are K, columns are M
-              tma_load_2d(a_sm, &p.mapA[0], &full_bar[s], w.m0, k0);
-              tma_load_2d(a_sm + 8192, &p.mapA[0], &full_bar[s], w.m0 + 64, k0);
+              tma_load_2d(a_sm + i * kPlane, &p.mapA[i], &full_bar[s], w.m0, k0);
+              tma_load_2d(a_sm + i * kPlane + 8192, &p.mapA[i], &full_bar[s], w.m0 + 64, k0);
             } else {  // rows are M, columns are K: one 64 x 128 box
               tma_load_2d(a_sm + i * kPlane, &p.mapA[i], &full_bar[s], k0, w.m0);
             }
@@ -213,7 +217,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
                 const int ia = (C::NA == 3) ? qa[t] : pa[t];
                 const int ib = (C::NA == 3) ? qb[t] : pb[t];
                 uint64_t ad, bd;
-                if (C::A_MN) ad = sdesc(a_sm + kk * 2048, 8192, 1024);
+                if (C::A_MN) ad = sdesc(a_sm + ia * kPlane + kk * 2048, 8192, 1024);
                 else ad = sdesc(a_sm + ia * kPlane + kk * 32, 16, 1024);
                 if (C::B_MN) bd = sdesc(b_sm + ib * kPlane + kk * 2048, 8192, 1024);
                 else bd = sdesc(b_sm + ib * kPlane + kk * 32, 16, 1024);
@@ -274,7 +278,7 @@ __global__ void __launch_bounds__(kRThreads, 1) router_tc_kernel(const __grid_co
       if (!ok) break;
       const int row = w.m0 + q * 32 + lane;
       if (row < p.M) {
-        const bool add_bias = (MODE == FWD) && p.z == 1 && p.bias != nullptr;
+        const bool add_bias = (MODE == FWD || MODE == FWD3) && p.z == 1 && p.bias != nullptr;
         float* dst = p.out + ((size_t)w.z * p.M + row) * (size_t)p.N + w.n0;
 #pragma unroll
         for (int g = 0; g < RBN / 4; ++g) {
@@ -361,35 +365,49 @@ size_t r256(size_t b) { return (b + 255) & ~size_t(255); }
 
 }  // namespace
 
-// bf16 activations, h a multiple of 64, 64 <= E <= 1024 a multiple of 16 (MMA N); MOE_PFT_GEMM=simt forces the
-// fp32 FFMA path.
+// bf16 or fp32 activations (fp32 ones are split into planes too), h a multiple of 64, 64 <= E <= 1024 a
+// multiple of 16 (MMA N); MOE_PFT_GEMM=simt forces the fp32 FFMA path.
 bool tc_router_supported(int dtype, int h, int E) {
   const char* env = getenv("MOE_PFT_GEMM");
   if (env && strcmp(env, "simt") == 0) return false;
-  return dtype == MOE_BF16 && h % 64 == 0 && E % 16 == 0 && E >= 64 && E <= 1024 && tc_encode_available();
+  return (dtype == MOE_BF16 || dtype == MOE_F32) && h % 64 == 0 && E % 16 == 0 && E >= 64 && E <= 1024 &&
+         tc_encode_available();
 }
 
-// Scratch bytes after the workspace header: op 0 = forward, 1 = backward.
-size_t tc_router_scratch(int op, int T, int h, int E) {
+// Scratch bytes after the workspace header: op 0 = forward, 1 = backward.  fp32 activations add
+// the three planes of x.
+size_t tc_router_scratch(int op, int T, int h, int E, int dtype) {
   const size_t planes_w = r256((size_t)3 * h * E * 2);
   const size_t planes_d = r256((size_t)3 * T * E * 2);
+  const size_t planes_x = dtype == MOE_F32 ? r256((size_t)3 * T * h * 2) : 0;
   int ks, z;
-  if (op == 0) {  // forward: Wg planes, partials [z][T][E]
+  if (op == 0) {  // forward: Wg planes, x planes, partials [z][T][E]
     pick_slices(((T + RBM - 1) / RBM) * ((E + RBN - 1) / RBN), h, &ks, &z);
-    return planes_w + (z > 1 ? r256((size_t)z * T * E * 4) : 0);
+    return planes_w + planes_x + (z > 1 ? r256((size_t)z * T * E * 4) : 0);
   }
-  // backward: dL planes, Wg planes, partials [z][h][E]
+  // backward: dL planes, Wg planes, x planes, partials [z][h][E]
   pick_slices(((h + RBM - 1) / RBM) * ((E + RBN - 1) / RBN), T, &ks, &z);
-  return planes_d + planes_w + (z > 1 ? r256((size_t)z * h * E * 4) : 0);
+  return planes_d + planes_w + planes_x + (z > 1 ? r256((size_t)z * h * E * 4) : 0);
 }
 
-int tc_router_logits(const void* x, const float* Wg, const float* bias, int T, int h, int E, float* logits,
-                     void* scratch, const float** partial_out, int* slices_out, int* status, cudaStream_t st) {
-  __nv_bfloat16* wp = static_cast<__nv_bfloat16*>(scratch);
-  float* partial = reinterpret_cast<float*>(static_cast<char*>(scratch) + r256((size_t)3 * h * E * 2));
+int tc_router_logits(const void* x, const float* Wg, const float* bias, int T, int h, int E, int dtype,
+                     float* logits, void* scratch, const float** partial_out, int* slices_out, int* status,
+                     cudaStream_t st) {
+  const bool f32 = dtype == MOE_F32;
+  char* sp = static_cast<char*>(scratch);
+  __nv_bfloat16* wp = reinterpret_cast<__nv_bfloat16*>(sp);
+  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(sp + r256((size_t)3 * h * E * 2));
+  float* partial = reinterpret_cast<float*>(sp + r256((size_t)3 * h * E * 2) +
+                                            (f32 ? r256((size_t)3 * T * h * 2) : 0));
   launch_split3(Wg, (long long)h * E, wp, st);
+  if (f32) launch_split3(static_cast<const float*>(x), (long long)T * h, xp, st);
   RouterParams p = rblank(status);
-  bool ok = tc_make_map(&p.mapA[0], x, T, h, 64, 128);
+  bool ok = true;
+  if (f32) {
+    for (int i = 0; i < 3; ++i) ok = ok && tc_make_map(&p.mapA[i], xp + (size_t)i * T * h, T, h, 64, 128);
+  } else {
+    ok = tc_make_map(&p.mapA[0], x, T, h, 64, 128);
+  }
   for (int j = 0; j < 3; ++j) ok = ok && tc_make_map(&p.mapB[j], wp + (size_t)j * h * E, h, E, 64, 64);
   if (!ok) return -1;
   p.M = T; p.N = E; p.K = h;
@@ -397,29 +415,38 @@ int tc_router_logits(const void* x, const float* Wg, const float* bias, int T, i
   pick_slices(p.mt * p.nt, h, &p.kslice, &p.z);
   p.out = p.z > 1 ? partial : logits;
   p.bias = bias;
-  if (rlaunch<FWD>(p, st)) return -1;
+  if (f32 ? rlaunch<FWD3>(p, st) : rlaunch<FWD>(p, st)) return -1;
   // several K slices: the caller adds the partials (with the bias) where it reads the logits
   *partial_out = p.z > 1 ? partial : nullptr;
   *slices_out = p.z;
   return 0;
 }
 
-int tc_router_bwd(const void* x, const float* Wg, const float* d_logits, int T, int h, int E, float* dWg,
-                  float* dx_router, void* scratch, bool dl_planes_ready, int* status, cudaStream_t st) {
-  __nv_bfloat16* dp = static_cast<__nv_bfloat16*>(scratch);
-  __nv_bfloat16* wp = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(scratch) + r256((size_t)3 * T * E * 2));
-  float* partial = reinterpret_cast<float*>(reinterpret_cast<char*>(wp) + r256((size_t)3 * h * E * 2));
+int tc_router_bwd(const void* x, const float* Wg, const float* d_logits, int T, int h, int E, int dtype,
+                  float* dWg, float* dx_router, void* scratch, bool dl_planes_ready, int* status, cudaStream_t st) {
+  const bool f32 = dtype == MOE_F32;
+  char* sp = static_cast<char*>(scratch);
+  __nv_bfloat16* dp = reinterpret_cast<__nv_bfloat16*>(sp);
+  __nv_bfloat16* wp = reinterpret_cast<__nv_bfloat16*>(sp + r256((size_t)3 * T * E * 2));
+  __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(reinterpret_cast<char*>(wp) + r256((size_t)3 * h * E * 2));
+  float* partial = reinterpret_cast<float*>(reinterpret_cast<char*>(xp) + (f32 ? r256((size_t)3 * T * h * 2) : 0));
   if (!dl_planes_ready) launch_split3(d_logits, (long long)T * E, dp, st);
+  if (f32) launch_split3(static_cast<const float*>(x), (long long)T * h, xp, st);
   // dWg = x^T dL: M = h, N = E, K = T
   RouterParams g = rblank(status);
-  bool ok = tc_make_map(&g.mapA[0], x, T, h, 64, 64);
+  bool ok = true;
+  if (f32) {
+    for (int i = 0; i < 3; ++i) ok = ok && tc_make_map(&g.mapA[i], xp + (size_t)i * T * h, T, h, 64, 64);
+  } else {
+    ok = tc_make_map(&g.mapA[0], x, T, h, 64, 64);
+  }
   for (int j = 0; j < 3; ++j) ok = ok && tc_make_map(&g.mapB[j], dp + (size_t)j * T * E, T, E, 64, 64);
   if (!ok) return -1;
   g.M = h; g.N = E; g.K = T;
   g.mt = (h + RBM - 1) / RBM; g.nt = (E + RBN - 1) / RBN;
   pick_slices(g.mt * g.nt, T, &g.kslice, &g.z);
   g.out = g.z > 1 ? partial : dWg;
-  if (rlaunch<DWG>(g, st)) return -1;
+  if (f32 ? rlaunch<DWG3>(g, st) : rlaunch<DWG>(g, st)) return -1;
   if (g.z > 1) launch_splitk_reduce(partial, g.z, (long long)h * E, E, nullptr, dWg, st);
   if (dx_router == nullptr) return 0;
   // dx = dL Wg^T: M = T, N = h, K = E

@@ -111,14 +111,14 @@ def test_route_bwd(B, dt, T, h, E, k):
     assert B.moe_check_status(ws) == 0
 
 
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("T,h,E", [(300, 7168, 256), (4096, 2048, 64), (1000, 5120, 128), (257, 2048, 80),
-                                   (100, 256, 1024)])
-def test_router_gemms_at_full_widths(B, T, h, E):
-    """bf16 activations with an fp32 router at the pages' widths (long sums over h = 7168 and
-    T = 4096): logits, dWg and dx stay within the fp32 tolerance of the exact sums."""
+                                   (100, 256, 1024), (16384, 2048, 128)])
+def test_router_gemms_at_full_widths(B, dt, T, h, E):
+    """bf16 or fp32 activations with an fp32 router at the pages' widths (long sums over h = 7168
+    and T up to 16384): logits, dWg and dx stay within the fp32 tolerance of the exact sums."""
     from mixture_experts_layer_pft_gb300.workloads import random_tensor
 
-    dt = torch.bfloat16
     k = 2
     x = random_tensor((T, h), 21, dt, "cuda")
     Wg = random_tensor((h, E), 22, torch.float32, "cuda", std=h ** -0.5)
@@ -142,13 +142,13 @@ def test_router_gemms_at_full_widths(B, T, h, E):
     assert B.moe_check_status(ws) == 0
 
 
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("T,h,E", [(300, 2048, 64), (77, 512, 256)])
-def test_tensor_core_router_matches_fp32_fma_router(B, monkeypatch, T, h, E):
+def test_tensor_core_router_matches_fp32_fma_router(B, monkeypatch, dt, T, h, E):
     """The tensor-core router (exact bf16 planes, short truncated chains) and the fp32 FMA router
     agree to fp32 accuracy on the same inputs."""
     from mixture_experts_layer_pft_gb300.workloads import random_tensor
 
-    dt = torch.bfloat16
     k = 4
     x = random_tensor((T, h), 31, dt, "cuda")
     Wg = random_tensor((h, E), 32, torch.float32, "cuda", std=h ** -0.5)
