@@ -22,8 +22,9 @@
 // H3A's epilogue reads h1 back and writes h3, a = silu(h1) h3 and the three planes of a.
 //
 // Warp roles (one CTA per SM): warp 0 issues the TMA loads (three A and three B planes per stage),
-// warp 1 owns TMEM (two buffers of the accumulator pair) and issues the MMAs, warps 2-5 drain one
-// TMEM lane quarter each and hold their row's 128 running sums.  Every wait is bounded.
+// warp 1 owns TMEM (two buffers of the accumulator pair) and issues the MMAs, warps 2-9 drain the
+// accumulators, two warps per TMEM lane quarter each holding its row's 64 running sums of half the
+// token columns.  Every wait is bounded.
 #include <string.h>
 
 #include "common.cuh"
@@ -40,7 +41,9 @@ constexpr int FBM = 128;       // MMA M: rows of the weight dimension per unit
 constexpr int FBN = 128;       // tokens per chunk (MMA N up to 128)
 constexpr int FBK = 64;        // K per stage (one 128-byte swizzle row of bf16)
 constexpr int kFSteps = 4;     // stages per drain: 256 of K
-constexpr int kFThreads = 192;  // producer, MMA, four epilogue warps
+constexpr int kFEpiWarps = 8;   // two per TMEM lane quarter, each draining half the columns
+constexpr int kFCols = FBN / 2;  // columns per epilogue warp
+constexpr int kFThreads = 64 + 32 * kFEpiWarps;  // producer, MMA, eight epilogue warps
 constexpr uint32_t kFBox = 8192;   // one 64 x 64 bf16 box
 constexpr uint32_t kFPlaneA = 2 * kFBox;  // 128 weight columns x 64 K rows
 constexpr uint32_t kFPlaneB = 2 * kFBox;  // 128 token rows x 64 K
@@ -143,7 +146,7 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kFStages; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], 4); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&tfull_bar[b], 1); mbar_init(&tempty_bar[b], kFEpiWarps); }
     mbar_init(&drain_bar, 1);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -253,15 +256,16 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
     }
     __syncwarp();
   } else {
-    // ================================================================ epilogue (warps 2..5)
-    const int q = warp & 3;  // TMEM lane quarter
+    // ================================================================ epilogue (warps 2..9)
+    const int q = warp & 3;              // TMEM lane quarter
+    const int cb = ((warp - 2) >> 2) * kFCols;  // this warp's first column
     int cc = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const FUnit w = fdecode(u, s_pref, s_off, p.E, mt);
-      float run[FBN];
+      float run[kFCols];
 #pragma unroll
-      for (int i = 0; i < FBN; ++i) run[i] = 0.f;
+      for (int i = 0; i < kFCols; ++i) run[i] = 0.f;
       for (int c0 = 0; c0 < nsteps; c0 += kFSteps, ++cc) {
         const int b = cc & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(&tfull_bar[b], (uint32_t)(cc >> 1) & 1u, &s_abort, p.status,
@@ -270,10 +274,10 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
           break;
         }
         tc_fence_after();
-        const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 2 * FBN);
+        const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * 2 * FBN + cb);
 #pragma unroll
-        for (int g = 0; g < FBN / 16; ++g) {
-          if (16 * g < w.nmma) {
+        for (int g = 0; g < kFCols / 16; ++g) {
+          if (cb + 16 * g < w.nmma) {
             float vm[16], vc[16];
             tmem_ld16(t0 + 16 * g, vm);
             tmem_ld16(t0 + FBN + 16 * g, vc);
@@ -293,20 +297,20 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
       if (MODE == H3A) {
         // h1 in groups of 16 columns, all loads issued before the group's stores
 #pragma unroll
-        for (int g = 0; g < FBN / 16; ++g) {
-          if (16 * g >= w.rows) break;
+        for (int g = 0; g < kFCols / 16; ++g) {
+          if (cb + 16 * g >= w.rows) break;
           float z1[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int n = 16 * g + i;
+            const int n = cb + 16 * g + i;
             z1[i] = n < w.rows ? __ldg(p.h1 + (size_t)(w.row0 + n) * p.M + m) : 0.f;
           }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int n = 16 * g + i;
+            const int n = cb + 16 * g + i;
             if (n < w.rows) {
               const size_t o = (size_t)(w.row0 + n) * p.M + m;
-              const float v = run[n];
+              const float v = run[16 * g + i];
               const float av = z1[i] * sigmoidf_(z1[i]) * v;
               p.out[o] = v;
               p.a[o] = av;
@@ -316,8 +320,8 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
         }
       } else {
 #pragma unroll
-        for (int n = 0; n < FBN; ++n)
-          if (n < w.rows) p.out[(size_t)(w.row0 + n) * p.M + m] = run[n];
+        for (int i = 0; i < kFCols; ++i)
+          if (cb + i < w.rows) p.out[(size_t)(w.row0 + cb + i) * p.M + m] = run[i];
       }
     }
   }
