@@ -335,21 +335,30 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
 }
 
 // Three-plane split of the experts' weight matrices, skipping experts without rows: expert
-// blockIdx.y, dst[p][e][i] = plane p of src[e][i] for its `per` elements.
+// blockIdx.y, dst[p][e][i] = plane p of src[e][i] for its `per` elements (a multiple of 8), eight
+// elements a thread with 16-byte loads and plane stores.
 __global__ void __launch_bounds__(256) split3_experts_kernel(const float* __restrict__ src, const int* __restrict__ offsets,
                                                              long long per, long long n, __nv_bfloat16* __restrict__ dst) {
   const int e = blockIdx.y;
   if (__ldg(offsets + e + 1) == __ldg(offsets + e)) return;  // no rows: its planes are never read
-  const float* s = src + (size_t)e * per;
   const size_t o = (size_t)e * per;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < per; i += (long long)gridDim.x * blockDim.x)
-    split3_value(__ldg(s + i), dst + o + i, dst + n + o + i, dst + 2 * n + o + i);
+  const float4* s = reinterpret_cast<const float4*>(src + o);
+  uint4* d0 = reinterpret_cast<uint4*>(dst + o);
+  uint4* d1 = reinterpret_cast<uint4*>(dst + n + o);
+  uint4* d2 = reinterpret_cast<uint4*>(dst + 2 * n + o);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < per / 8; i += (long long)gridDim.x * blockDim.x)
+    split3_vec8(__ldg(s + 2 * i), __ldg(s + 2 * i + 1), d0 + i, d1 + i, d2 + i);
 }
 
+// The same for n contiguous values (n a multiple of 8): dst[p][i] = plane p of src[i].
 __global__ void __launch_bounds__(256) split3_rows_kernel(const float* __restrict__ src, long long n,
                                                           __nv_bfloat16* __restrict__ dst) {
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x)
-    split3_value(__ldg(src + i), dst + i, dst + n + i, dst + 2 * n + i);
+  const float4* s = reinterpret_cast<const float4*>(src);
+  uint4* d0 = reinterpret_cast<uint4*>(dst);
+  uint4* d1 = reinterpret_cast<uint4*>(dst + n);
+  uint4* d2 = reinterpret_cast<uint4*>(dst + 2 * n);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n / 8; i += (long long)gridDim.x * blockDim.x)
+    split3_vec8(__ldg(s + 2 * i), __ldg(s + 2 * i + 1), d0 + i, d1 + i, d2 + i);
 }
 
 template <int MODE>

@@ -314,9 +314,25 @@ __global__ void __launch_bounds__(256) split3_kernel(const float* __restrict__ s
   }
 }
 
+// n a multiple of 8: eight values a thread, 16-byte loads and plane stores.
+__global__ void __launch_bounds__(256) split3_vec_kernel(const float* __restrict__ src, long long n,
+                                                         __nv_bfloat16* __restrict__ dst) {
+  const float4* s = reinterpret_cast<const float4*>(src);
+  uint4* d0 = reinterpret_cast<uint4*>(dst);
+  uint4* d1 = reinterpret_cast<uint4*>(dst + n);
+  uint4* d2 = reinterpret_cast<uint4*>(dst + 2 * n);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n / 8; i += (long long)gridDim.x * blockDim.x)
+    split3_vec8(__ldg(s + 2 * i), __ldg(s + 2 * i + 1), d0 + i, d1 + i, d2 + i);
+}
+
 void launch_split3(const float* src, long long n, __nv_bfloat16* dst, cudaStream_t st) {
-  const int blocks = (int)std::min<long long>((n + 255) / 256, 8 * num_sms());
-  split3_kernel<<<blocks, 256, 0, st>>>(src, n, dst);
+  if (n % 8 == 0) {  // every plane starts 16-byte aligned (the planes are n values apart)
+    const int blocks = (int)std::min<long long>((n / 8 + 255) / 256, 8 * num_sms());
+    split3_vec_kernel<<<blocks, 256, 0, st>>>(src, n, dst);
+  } else {
+    const int blocks = (int)std::min<long long>((n + 255) / 256, 8 * num_sms());
+    split3_kernel<<<blocks, 256, 0, st>>>(src, n, dst);
+  }
   count_launch(st);
 }
 
