@@ -655,23 +655,19 @@ __global__ void __launch_bounds__(Cfg<MODE>::THREADS, 1) tc_gemm_kernel(const __
 #pragma unroll
         for (int j = 0; j < NCH; ++j) {
           const int c0 = C::CW * (cg + G * j);
-          // both outputs' 32 columns in flight before one wait: the drain holds up the next
-          // unit's MMAs, so its TMEM round trips are on the critical path
-          float vv[NOUT][32];
-          if (!zero && c0 < w.ncols) {
 #pragma unroll
-            for (int a = 0; a < NOUT; ++a) tmem_ld32(t0u + a * C::BN + c0, vv[a]);
-            tmem_wait_ld();
-          } else {
+          for (int a = 0; a < NOUT; ++a) {
+            float vv[32];
+            if (!zero && c0 < w.ncols) {
+              tmem_ld32(t0u + a * C::BN + c0, vv);
+              tmem_wait_ld();
+            } else {
 #pragma unroll
-            for (int a = 0; a < NOUT; ++a)
+              for (int i = 0; i < 32; ++i) vv[i] = 0.f;
+            }
 #pragma unroll
-              for (int i = 0; i < 32; ++i) vv[a][i] = 0.f;
+            for (int i = 0; i < 16; ++i) pk[a][j][i] = pack_bf16x2(vv[2 * i], vv[2 * i + 1]);
           }
-#pragma unroll
-          for (int a = 0; a < NOUT; ++a)
-#pragma unroll
-            for (int i = 0; i < 16; ++i) pk[a][j][i] = pack_bf16x2(vv[a][2 * i], vv[a][2 * i + 1]);
         }
         tc_fence_before();
         __syncwarp();
