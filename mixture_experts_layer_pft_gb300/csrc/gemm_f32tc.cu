@@ -29,6 +29,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "planes.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {

@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "planes.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
