@@ -379,8 +379,8 @@ def kernel_names(stage, n, w):
                       CSRC + "pft.cu"),
         "dispatch": (["dispatch"], CSRC + "gather.cu"),
         "expert_ffn": ((["tc_GATEUP", "tc_DOWN"], CSRC + "gemm_tc.cu") if tc
-                       else (["f32_split_x", "f32_split_w1", "f32tc_H1", "f32_split_w3", "f32tc_H3A",
-                              "f32_split_w2", "f32tc_Y"], CSRC + "gemm_f32tc.cu") if f32tc
+                       else (["f32_split_x", "f32_split_w1", "f32tc_H1", "f32tc_H3A", "f32tc_Y"],
+                             CSRC + "gemm_f32tc.cu") if f32tc
                        else ((["simt_gateup", "simt_down"] if n == 2 else ["simt_h1", "simt_h3_swiglu", "simt_down"]),
                              CSRC + "gemm_simt.cu")),
         "combine": (["combine"], CSRC + "gather.cu"),
@@ -437,11 +437,14 @@ def kernel_counts(w, T, e_active):
     # fp32 expert forward on the tensor cores: exact three-plane bf16 splits, then one GEMM per
     # product (the FLOPs are the fp32 GEMM's; the tensor cores do six plane products for each)
     d["f32_split_x"] = {"flops": 0, "bytes": Tk * h * 4 + 3 * Tk * h * 2}
-    for n in ("f32_split_w1", "f32_split_w3", "f32_split_w2"):
-        d[n] = {"flops": 0, "bytes": e_active * h * f * (4 + 6)}
-    d["f32tc_H1"] = {"flops": 2 * Tk * h * f, "bytes": 3 * e_active * h * f * 2 + 3 * Tk * h * 2 + Tk * f * 4}
+    # W1's planes have their own launch; H1 and H3A split W3 and W2 (the next GEMM's weights)
+    # in a side warp while they run
+    wsplit = e_active * h * f * (4 + 6)
+    d["f32_split_w1"] = {"flops": 0, "bytes": wsplit}
+    d["f32tc_H1"] = {"flops": 2 * Tk * h * f,
+                     "bytes": 3 * e_active * h * f * 2 + 3 * Tk * h * 2 + Tk * f * 4 + wsplit}
     d["f32tc_H3A"] = {"flops": 2 * Tk * h * f,
-                      "bytes": 3 * e_active * h * f * 2 + 3 * Tk * h * 2 + Tk * f * 4 * 3 + 3 * Tk * f * 2}
+                      "bytes": 3 * e_active * h * f * 2 + 3 * Tk * h * 2 + Tk * f * 4 * 3 + 3 * Tk * f * 2 + wsplit}
     d["f32tc_Y"] = {"flops": 2 * Tk * h * f, "bytes": 3 * e_active * h * f * 2 + 3 * Tk * f * 2 + Tk * h * 4}
     d["simt_h1"] = {"flops": 2 * Tk * h * f, "bytes": e_active * Wb + Tk * h * s + Tk * f * s}
     d["simt_h3_swiglu"] = {"flops": 2 * Tk * h * f, "bytes": e_active * Wb + Tk * h * s + 3 * Tk * f * s}

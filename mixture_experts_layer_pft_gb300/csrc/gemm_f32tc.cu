@@ -24,7 +24,8 @@
 // Warp roles (one CTA per SM): warp 0 issues the TMA loads (three A and three B planes per stage),
 // warp 1 owns TMEM (two buffers of the accumulator pair) and issues the MMAs, warps 2-9 drain the
 // accumulators, two warps per TMEM lane quarter each holding its row's 64 running sums of half the
-// token columns.  Every wait is bounded.
+// token columns, and warp 10 splits the next GEMM's weight tensor into its planes meanwhile (the
+// GEMMs are bound by the L2 -> SM stream, with DRAM bandwidth to spare).  Every wait is bounded.
 #include <string.h>
 
 #include "common.cuh"
@@ -44,7 +45,9 @@ constexpr int FBK = 64;        // K per stage (one 128-byte swizzle row of bf16)
 constexpr int kFSteps = 4;     // stages per drain: 256 of K
 constexpr int kFEpiWarps = 8;   // two per TMEM lane quarter, each draining half the columns
 constexpr int kFCols = FBN / 2;  // columns per epilogue warp
-constexpr int kFThreads = 64 + 32 * kFEpiWarps;  // producer, MMA, eight epilogue warps
+constexpr int kFSplitWarp = 2 + kFEpiWarps;  // first of the warps that split the next weight tensor
+constexpr int kFSplitWarps = 1;
+constexpr int kFThreads = 64 + 32 * kFEpiWarps + 32 * kFSplitWarps;  // producer, MMA, epilogue, splitters
 constexpr uint32_t kFBox = 8192;   // one 64 x 64 bf16 box
 constexpr uint32_t kFPlaneA = 2 * kFBox;  // 128 weight columns x 64 K rows
 constexpr uint32_t kFPlaneB = 2 * kFBox;  // 128 token rows x 64 K
@@ -64,10 +67,50 @@ struct F32Params {
   float* a;             // H3A: a = silu(h1) h3, [Tk, M]
   __nv_bfloat16* a_planes;  // H3A: three planes of a, [3][Tk][M]
   long long Tk;
+  // the next GEMM's weight tensor, split into its planes by the splitter warp while this GEMM
+  // runs (nullptr: none): nsrc [E][nper] fp32 -> ndst [3][E][nper] bf16
+  const float* nsrc;
+  __nv_bfloat16* ndst;
+  long long nper;
   int* status;
   unsigned long long wait_ns;
   int withhold;
 };
+
+// The splitter warp's share of the next weight tensor's planes: experts with rows only, eight
+// values a lane, eight items in flight.  Nothing in this GEMM reads them; the next launch does.
+__device__ __noinline__ void split_next_weights(const F32Params& p, const int* s_off, int lane) {
+  // lane: this thread's index among the CTA's 32 * kFSplitWarps splitter threads
+  if (p.nsrc == nullptr) return;
+  constexpr int U = 8;
+  const long long pv = p.nper / 8;  // 8-value items per expert
+  const long long n = (long long)p.E * p.nper;
+  const float4* src = reinterpret_cast<const float4*>(p.nsrc);
+  uint4* d0 = reinterpret_cast<uint4*>(p.ndst);
+  uint4* d1 = reinterpret_cast<uint4*>(p.ndst + n);
+  uint4* d2 = reinterpret_cast<uint4*>(p.ndst + 2 * n);
+  const long long step = (long long)gridDim.x * 32 * kFSplitWarps;
+  for (int e = 0; e < p.E; ++e) {
+    if (s_off[e + 1] == s_off[e]) continue;  // no rows: its planes are never read
+    const long long base = (long long)e * pv;
+    for (long long j0 = (long long)blockIdx.x * 32 * kFSplitWarps + lane; j0 < pv; j0 += step * U) {
+      float4 a[U], b[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const long long j = j0 + u * step;
+        if (j < pv) {
+          a[u] = __ldcs(src + 2 * (base + j));  // read once: keep it out of the GEMM's L2 working set
+          b[u] = __ldcs(src + 2 * (base + j) + 1);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const long long j = j0 + u * step;
+        if (j < pv) split3_vec8(a[u], b[u], d0 + base + j, d1 + base + j, d2 + base + j);
+      }
+    }
+  }
+}
 
 struct FUnit {
   int e, m0, row0, rows, nmma;
@@ -143,7 +186,10 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
   }
   __syncthreads();
   const int total = s_total;
-  if ((int)blockIdx.x >= total) return;  // nothing for this CTA (before any TMEM use)
+  if ((int)blockIdx.x >= total) {  // no unit for this CTA (before any TMEM use): only the splitter works
+    if (warp >= kFSplitWarp) split_next_weights(p, s_off, (warp - kFSplitWarp) * 32 + lane);
+    return;
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kFStages; ++s) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], 1); }
@@ -256,6 +302,9 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
       }
     }
     __syncwarp();
+  } else if (warp >= kFSplitWarp) {
+    // ================================================================ splitters
+    split_next_weights(p, s_off, (warp - kFSplitWarp) * 32 + lane);
   } else {
     // ================================================================ epilogue (warps 2..9)
     const int q = warp & 3;              // TMEM lane quarter
@@ -391,48 +440,50 @@ bool f32tc_supported(int dtype, int h, int f, int E) {
 }
 
 size_t f32tc_scratch(long long Tk, int E, int h, int f) {
-  // token planes of xbuf and of a, and the planes of one expert weight tensor at a time
-  return r256((size_t)3 * Tk * h * 2) + r256((size_t)3 * Tk * f * 2) + r256((size_t)3 * E * h * f * 2);
+  // token planes of xbuf and of a, and two weight-plane buffers: one GEMM reads one while its
+  // splitter warp fills the other for the next GEMM
+  return r256((size_t)3 * Tk * h * 2) + r256((size_t)3 * Tk * f * 2) + 2 * r256((size_t)3 * E * h * f * 2);
 }
 
 int f32tc_expert_ffn(const float* xbuf, const int* offsets, const float* W1, const float* W3, const float* W2,
                      int Tk, int E, int h, int f, float* ybuf, float* h1, float* h3, float* a, void* scratch,
                      int* status, cudaStream_t st) {
   char* sp = static_cast<char*>(scratch);
+  const size_t wbytes = r256((size_t)3 * E * h * f * 2);
   __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(sp);
   __nv_bfloat16* ap = reinterpret_cast<__nv_bfloat16*>(sp + r256((size_t)3 * Tk * h * 2));
-  __nv_bfloat16* wp = reinterpret_cast<__nv_bfloat16*>(sp + r256((size_t)3 * Tk * h * 2) + r256((size_t)3 * Tk * f * 2));
+  char* wbase = sp + r256((size_t)3 * Tk * h * 2) + r256((size_t)3 * Tk * f * 2);
+  __nv_bfloat16* wpA = reinterpret_cast<__nv_bfloat16*>(wbase);            // W1, then W2
+  __nv_bfloat16* wpB = reinterpret_cast<__nv_bfloat16*>(wbase + wbytes);   // W3
   const int blocks = 8 * num_sms();
   const long long per = (long long)h * f;
   split3_rows_kernel<<<blocks, 256, 0, st>>>(xbuf, (long long)Tk * h, xp);
+  count_launch(st);
+  const dim3 wgrid(16, E);
+  split3_experts_kernel<<<wgrid, 256, 0, st>>>(W1, offsets, per, (long long)E * per, wpA);
   count_launch(st);
 
   F32Params g;
   memset(&g, 0, sizeof(g));
   g.offsets = offsets; g.E = E; g.Tk = Tk; g.status = status;
-  bool ok = make_plane_maps(g.mapB, xp, Tk, h) && make_plane_maps(g.mapA, wp, (long long)E * h, f);
+  g.M = f; g.K = h; g.nper = per;
+  // h1 = xbuf W1, while W3 is split into the second buffer
+  bool ok = make_plane_maps(g.mapB, xp, Tk, h) && make_plane_maps(g.mapA, wpA, (long long)E * h, f);
   if (!ok) return -1;
-  g.M = f; g.K = h;
-  // h1 = xbuf W1
-  const dim3 wgrid(16, E);
-  split3_experts_kernel<<<wgrid, 256, 0, st>>>(W1, offsets, per, (long long)E * per, wp);
-  count_launch(st);
-  g.out = h1;
+  g.out = h1; g.nsrc = W3; g.ndst = wpB;
   if (flaunch<H1>(g, st)) return -1;
-  // h3 = xbuf W3, a = silu(h1) h3 and its planes
-  split3_experts_kernel<<<wgrid, 256, 0, st>>>(W3, offsets, per, (long long)E * per, wp);
-  count_launch(st);
-  g.out = h3; g.h1 = h1; g.a = a; g.a_planes = ap;
+  // h3 = xbuf W3, a = silu(h1) h3 and its planes, while W2 is split into the first buffer
+  ok = make_plane_maps(g.mapA, wpB, (long long)E * h, f);
+  if (!ok) return -1;
+  g.out = h3; g.h1 = h1; g.a = a; g.a_planes = ap; g.nsrc = W2; g.ndst = wpA;
   if (flaunch<H3A>(g, st)) return -1;
   // y = a W2
   F32Params d;
   memset(&d, 0, sizeof(d));
   d.offsets = offsets; d.E = E; d.Tk = Tk; d.status = status;
-  ok = make_plane_maps(d.mapB, ap, Tk, f) && make_plane_maps(d.mapA, wp, (long long)E * f, h);
+  ok = make_plane_maps(d.mapB, ap, Tk, f) && make_plane_maps(d.mapA, wpA, (long long)E * f, h);
   if (!ok) return -1;
   d.M = h; d.K = f;
-  split3_experts_kernel<<<wgrid, 256, 0, st>>>(W2, offsets, per, (long long)E * per, wp);
-  count_launch(st);
   d.out = ybuf;
   return flaunch<Y>(d, st);
 }
