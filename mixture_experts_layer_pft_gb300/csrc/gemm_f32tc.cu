@@ -25,7 +25,10 @@
 // warp 1 owns TMEM (two buffers of the accumulator pair) and issues the MMAs, warps 2-9 drain the
 // accumulators, two warps per TMEM lane quarter each holding its row's 64 running sums of half the
 // token columns, and warp 10 splits the next GEMM's weight tensor into its planes meanwhile (the
-// GEMMs are bound by the L2 -> SM stream, with DRAM bandwidth to spare).  Every wait is bounded.
+// GEMMs are bound by the L2 -> SM stream, with DRAM bandwidth to spare).  That split is a queue of
+// 4096-value chunks taken with an atomic counter: the side warp takes chunks while the CTA's GEMM
+// warps work, and once they are done (TMEM released) all eleven warps drain what is left, so a
+// short GEMM never waits on one warp's split.  Every wait is bounded.
 #include <string.h>
 
 #include "common.cuh"
@@ -45,9 +48,10 @@ constexpr int FBK = 64;        // K per stage (one 128-byte swizzle row of bf16)
 constexpr int kFSteps = 4;     // stages per drain: 256 of K
 constexpr int kFEpiWarps = 8;   // two per TMEM lane quarter, each draining half the columns
 constexpr int kFCols = FBN / 2;  // columns per epilogue warp
-constexpr int kFSplitWarp = 2 + kFEpiWarps;  // first of the warps that split the next weight tensor
-constexpr int kFSplitWarps = 1;
-constexpr int kFThreads = 64 + 32 * kFEpiWarps + 32 * kFSplitWarps;  // producer, MMA, epilogue, splitters
+constexpr int kFSplitWarp = 2 + kFEpiWarps;  // the side warp that splits the next weight tensor
+constexpr int kFGemmWarps = 2 + kFEpiWarps;  // producer, MMA, epilogue
+constexpr int kFThreads = 32 * kFGemmWarps + 32;
+constexpr int kSplitItem = 4096;  // values of one chunk of the next weight tensor's split
 constexpr uint32_t kFBox = 8192;   // one 64 x 64 bf16 box
 constexpr uint32_t kFPlaneA = 2 * kFBox;  // 128 weight columns x 64 K rows
 constexpr uint32_t kFPlaneB = 2 * kFBox;  // 128 token rows x 64 K
@@ -67,46 +71,53 @@ struct F32Params {
   float* a;             // H3A: a = silu(h1) h3, [Tk, M]
   __nv_bfloat16* a_planes;  // H3A: three planes of a, [3][Tk][M]
   long long Tk;
-  // the next GEMM's weight tensor, split into its planes by the splitter warp while this GEMM
-  // runs (nullptr: none): nsrc [E][nper] fp32 -> ndst [3][E][nper] bf16
+  // the next GEMM's weight tensor, split into its planes by this launch (nullptr: none):
+  // nsrc [E][nper] fp32 -> ndst [3][E][nper] bf16, nper a multiple of kSplitItem; chunks are
+  // taken with split_ctr, zero at launch
   const float* nsrc;
   __nv_bfloat16* ndst;
   long long nper;
+  int* split_ctr;
   int* status;
   unsigned long long wait_ns;
   int withhold;
 };
 
-// The splitter warp's share of the next weight tensor's planes: experts with rows only, eight
-// values a lane, eight items in flight.  Nothing in this GEMM reads them; the next launch does.
-__device__ __noinline__ void split_next_weights(const F32Params& p, const int* s_off, int lane) {
-  // lane: this thread's index among the CTA's 32 * kFSplitWarps splitter threads
+// Chunks of the next weight tensor's planes, over the experts with rows (s_act[0..nact)), taken
+// from the launch's counter by whole warps until none are left, or until *stop reaches
+// kFGemmWarps (the side warp: the CTA's GEMM warps are done and the whole CTA takes over).
+// Nothing in this GEMM reads the planes; the next launch does.
+__device__ __noinline__ void split_next_weights(const F32Params& p, const int* s_act, int nact, int lane,
+                                                const volatile int* stop) {
   if (p.nsrc == nullptr) return;
+  constexpr int G8 = kSplitItem / 8;  // 8-value groups of a chunk: 16 a lane, in two rounds of 8
   constexpr int U = 8;
-  const long long pv = p.nper / 8;  // 8-value items per expert
+  const int ipe = (int)(p.nper / kSplitItem);
+  const int nitems = nact * ipe;
   const long long n = (long long)p.E * p.nper;
   const float4* src = reinterpret_cast<const float4*>(p.nsrc);
   uint4* d0 = reinterpret_cast<uint4*>(p.ndst);
   uint4* d1 = reinterpret_cast<uint4*>(p.ndst + n);
   uint4* d2 = reinterpret_cast<uint4*>(p.ndst + 2 * n);
-  const long long step = (long long)gridDim.x * 32 * kFSplitWarps;
-  for (int e = 0; e < p.E; ++e) {
-    if (s_off[e + 1] == s_off[e]) continue;  // no rows: its planes are never read
-    const long long base = (long long)e * pv;
-    for (long long j0 = (long long)blockIdx.x * 32 * kFSplitWarps + lane; j0 < pv; j0 += step * U) {
+  while (stop == nullptr || *stop < kFGemmWarps) {
+    int it = 0;
+    if (lane == 0) it = atomicAdd(p.split_ctr, 1);
+    it = __shfl_sync(0xffffffffu, it, 0);
+    if (it >= nitems) break;
+    const long long g0 = (long long)s_act[it / ipe] * (p.nper / 8) + (long long)(it % ipe) * G8;
+#pragma unroll 1
+    for (int r = 0; r < G8 / (32 * U); ++r) {
       float4 a[U], b[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const long long j = j0 + u * step;
-        if (j < pv) {
-          a[u] = __ldcs(src + 2 * (base + j));  // read once: keep it out of the GEMM's L2 working set
-          b[u] = __ldcs(src + 2 * (base + j) + 1);
-        }
+        const long long j = g0 + (r * U + u) * 32 + lane;
+        a[u] = __ldcs(src + 2 * j);  // read once: keep it out of the GEMM's L2 working set
+        b[u] = __ldcs(src + 2 * j + 1);
       }
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const long long j = j0 + u * step;
-        if (j < pv) split3_vec8(a[u], b[u], d0 + base + j, d1 + base + j, d2 + base + j);
+        const long long j = g0 + (r * U + u) * 32 + lane;
+        split3_vec8(a[u], b[u], d0 + j, d1 + j, d2 + j);
       }
     }
   }
@@ -149,7 +160,9 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
   __shared__ volatile int s_abort;
   __shared__ int s_off[kFMaxE + 1];
   __shared__ int s_pref[kFMaxE + 1];
-  __shared__ int s_total;
+  __shared__ int s_act[kFMaxE];  // experts with rows, ascending
+  __shared__ int s_total, s_nact;
+  __shared__ volatile int s_gemm_done;  // GEMM warps past their loops
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t ring = (smem_u32(dsmem) + 1023u) & ~1023u;
@@ -183,11 +196,26 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
       s_pref[p.E] = incl;
       s_total = incl;
     }
+  } else if (warp == 1) {
+    // the experts with rows, in order (ballot compaction)
+    int nact = 0;
+    for (int e0 = 0; e0 < p.E; e0 += 32) {
+      const int e = e0 + lane;
+      const bool act = e < p.E && s_off[e + 1] > s_off[e];
+      const unsigned m = __ballot_sync(0xffffffffu, act);
+      if (act) s_act[nact + __popc(m & ((1u << lane) - 1u))] = e;
+      nact += __popc(m);
+    }
+    if (lane == 0) {
+      s_nact = nact;
+      s_gemm_done = 0;
+    }
   }
   __syncthreads();
   const int total = s_total;
-  if ((int)blockIdx.x >= total) {  // no unit for this CTA (before any TMEM use): only the splitter works
-    if (warp >= kFSplitWarp) split_next_weights(p, s_off, (warp - kFSplitWarp) * 32 + lane);
+  const int nact = s_nact;
+  if ((int)blockIdx.x >= total) {  // no unit for this CTA (before any TMEM use): every warp splits
+    split_next_weights(p, s_act, nact, lane, nullptr);
     return;
   }
 
@@ -247,6 +275,7 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
         while (globaltimer() - t0 < 2000000ull) {
         }
       }
+      atomicAdd((int*)&s_gemm_done, 1);
     }
   } else if (warp == 1) {
     // ================================================================ MMA issuer
@@ -300,11 +329,12 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
       const unsigned long long t0 = globaltimer();
       while (!mbar_try_wait(&drain_bar, 0) && globaltimer() - t0 < kWaitLimitNs) {
       }
+      atomicAdd((int*)&s_gemm_done, 1);
     }
     __syncwarp();
-  } else if (warp >= kFSplitWarp) {
-    // ================================================================ splitters
-    split_next_weights(p, s_off, (warp - kFSplitWarp) * 32 + lane);
+  } else if (warp == kFSplitWarp) {
+    // ================================================================ side splitter
+    split_next_weights(p, s_act, nact, lane, &s_gemm_done);
   } else {
     // ================================================================ epilogue (warps 2..9)
     const int q = warp & 3;              // TMEM lane quarter
@@ -374,6 +404,8 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
           if (cb + i < w.rows) p.out[(size_t)(w.row0 + cb + i) * p.M + m] = run[i];
       }
     }
+    __syncwarp();
+    if (lane == 0) atomicAdd((int*)&s_gemm_done, 1);
   }
 
   tc_fence_before();
@@ -382,6 +414,8 @@ __global__ void __launch_bounds__(kFThreads, 1) f32tc_kernel(const __grid_consta
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512) : "memory");
   }
+  // what is left of the next tensor's split, with every warp
+  split_next_weights(p, s_act, nact, lane, nullptr);
 }
 
 // Three-plane split of the experts' weight matrices, skipping experts without rows: expert
@@ -402,7 +436,8 @@ __global__ void __launch_bounds__(256) split3_experts_kernel(const float* __rest
 
 // The same for n contiguous values (n a multiple of 8): dst[p][i] = plane p of src[i].
 __global__ void __launch_bounds__(256) split3_rows_kernel(const float* __restrict__ src, long long n,
-                                                          __nv_bfloat16* __restrict__ dst) {
+                                                          __nv_bfloat16* __restrict__ dst, int* zero2) {
+  if (zero2 != nullptr && blockIdx.x == 0 && threadIdx.x < 2) zero2[threadIdx.x] = 0;  // the next launches' counters
   const float4* s = reinterpret_cast<const float4*>(src);
   uint4* d0 = reinterpret_cast<uint4*>(dst);
   uint4* d1 = reinterpret_cast<uint4*>(dst + n);
@@ -442,7 +477,7 @@ bool f32tc_supported(int dtype, int h, int f, int E) {
 size_t f32tc_scratch(long long Tk, int E, int h, int f) {
   // token planes of xbuf and of a, and two weight-plane buffers: one GEMM reads one while its
   // splitter warp fills the other for the next GEMM
-  return r256((size_t)3 * Tk * h * 2) + r256((size_t)3 * Tk * f * 2) + 2 * r256((size_t)3 * E * h * f * 2);
+  return r256((size_t)3 * Tk * h * 2) + r256((size_t)3 * Tk * f * 2) + 2 * r256((size_t)3 * E * h * f * 2) + 256;
 }
 
 int f32tc_expert_ffn(const float* xbuf, const int* offsets, const float* W1, const float* W3, const float* W2,
@@ -455,9 +490,10 @@ int f32tc_expert_ffn(const float* xbuf, const int* offsets, const float* W1, con
   char* wbase = sp + r256((size_t)3 * Tk * h * 2) + r256((size_t)3 * Tk * f * 2);
   __nv_bfloat16* wpA = reinterpret_cast<__nv_bfloat16*>(wbase);            // W1, then W2
   __nv_bfloat16* wpB = reinterpret_cast<__nv_bfloat16*>(wbase + wbytes);   // W3
+  int* ctr = reinterpret_cast<int*>(wbase + 2 * wbytes);                    // the two split queues
   const int blocks = 8 * num_sms();
   const long long per = (long long)h * f;
-  split3_rows_kernel<<<blocks, 256, 0, st>>>(xbuf, (long long)Tk * h, xp);
+  split3_rows_kernel<<<blocks, 256, 0, st>>>(xbuf, (long long)Tk * h, xp, ctr);
   count_launch(st);
   const dim3 wgrid(16, E);
   split3_experts_kernel<<<wgrid, 256, 0, st>>>(W1, offsets, per, (long long)E * per, wpA);
@@ -470,12 +506,12 @@ int f32tc_expert_ffn(const float* xbuf, const int* offsets, const float* W1, con
   // h1 = xbuf W1, while W3 is split into the second buffer
   bool ok = make_plane_maps(g.mapB, xp, Tk, h) && make_plane_maps(g.mapA, wpA, (long long)E * h, f);
   if (!ok) return -1;
-  g.out = h1; g.nsrc = W3; g.ndst = wpB;
+  g.out = h1; g.nsrc = W3; g.ndst = wpB; g.split_ctr = ctr;
   if (flaunch<H1>(g, st)) return -1;
   // h3 = xbuf W3, a = silu(h1) h3 and its planes, while W2 is split into the first buffer
   ok = make_plane_maps(g.mapA, wpB, (long long)E * h, f);
   if (!ok) return -1;
-  g.out = h3; g.h1 = h1; g.a = a; g.a_planes = ap; g.nsrc = W2; g.ndst = wpA;
+  g.out = h3; g.h1 = h1; g.a = a; g.a_planes = ap; g.nsrc = W2; g.ndst = wpA; g.split_ctr = ctr + 1;
   if (flaunch<H3A>(g, st)) return -1;
   // y = a W2
   F32Params d;
