@@ -171,6 +171,9 @@ int moe_route_bwd(const void* x, const float* Wg, const float* probs, const int3
  * topk_idx: [T,k] int32, each row k distinct ids in [0,E).  Outputs int32: num_ids [E],
  * offsets [E+1], token_ids [Tk], expert_ids [Tk], slot_of [Tk].  Deterministic.  An id
  * outside [0,E) sets MOE_STATUS_BAD_INDEX and is dropped (the outputs are then incomplete).
+ * An id repeated within a row also sets MOE_STATUS_BAD_INDEX; num_ids and offsets then count
+ * every entry, the copies share one row of token_ids and one row of that expert's bucket stays
+ * unwritten (every write stays inside the arrays).
  * Requires E <= 1024, T*k <= 2^30.
  */
 int moe_pft_build(const int32_t* topk_idx, int T, int E, int k, int32_t* num_ids,

@@ -48,7 +48,6 @@ void launch_gshard_combine(int dtype, const float* cw, const void* ye, int T, in
 
 // pft.cu
 int pft_num_chunks(long long Tk);
-int pft_chunk_size(long long Tk);
 size_t pft_scratch_bytes(long long Tk, int E);
 void launch_pft_build(const int* topk_idx, int T, int E, int k, int* num_ids, int* offsets,
                       int* token_ids, int* expert_ids, int* slot_of, void* ws, cudaStream_t st);

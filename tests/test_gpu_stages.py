@@ -289,6 +289,25 @@ def test_pft_build_all_tokens_to_one_expert(B):
         np.testing.assert_array_equal(npi(out[n]), want[n], err_msg=n)
 
 
+def test_pft_build_flags_an_expert_id_repeated_within_a_row(B):
+    """Rows must hold k distinct ids; a repeat is reported, and every write stays in range."""
+    T, E, k = 300, 8, 3
+    idx = oracle_routing(T, E, k, 5)
+    idx[10, 2] = idx[10, 0]
+    out, ws = run_pft(B, idx, E)
+    assert B.moe_check_status(ws) & B.MOE_STATUS_BAD_INDEX
+    cnt = np.bincount(idx.ravel(), minlength=E)
+    np.testing.assert_array_equal(npi(out["num_ids"]), cnt)
+    slot = npi(out["slot_of"])
+    assert ((slot >= 0) & (slot < T * k)).all()
+    assert slot[10 * k + 2] == slot[10 * k]
+    # every other row is the oracle's build of the same ids with the repeat taken out
+    keep = np.ones(T * k, bool)
+    keep[10 * k + 2] = False
+    tok = npi(out["token_ids"])
+    assert (tok[slot[keep]] == np.repeat(np.arange(T), k)[keep]).all()
+
+
 def test_pft_build_flags_an_out_of_range_expert_id(B):
     idx = oracle_routing(64, 8, 2, 3)
     idx[10, 1] = 8  # an expert id equal to E: reported, not dereferenced
