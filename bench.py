@@ -374,9 +374,7 @@ def kernel_names(stage, n, w):
                      CSRC + "gemm_simt.cu")
     table = {
         "route": route,
-        # few ranges: the count kernel's last CTA also scans; otherwise a scan kernel between
-        "pft_build": ((["pft_count_scan", "pft_scatter"] if n == 2 else ["pft_count", "pft_scan", "pft_scatter"]),
-                      CSRC + "pft.cu"),
+        "pft_build": (["pft_count", "pft_scan", "pft_scatter"], CSRC + "pft.cu"),
         "dispatch": (["dispatch"], CSRC + "gather.cu"),
         "expert_ffn": ((["tc_GATEUP", "tc_DOWN"], CSRC + "gemm_tc.cu") if tc
                        else (["f32_split_x", "f32_split_w1", "f32tc_H1", "f32tc_H3A", "f32tc_Y"],
@@ -386,7 +384,10 @@ def kernel_names(stage, n, w):
         "combine": (["combine"], CSRC + "gather.cu"),
         "combine_bwd": (["combine_bwd"], CSRC + "gather.cu"),
         "expert_ffn_bwd": ((["tc_DA", "tc_DX", "tc_WGRAD13", "tc_WGRAD2"], CSRC + "gemm_tc.cu") if tc
-                           else (["simt_dA", "simt_dX", "simt_dW13", "simt_dW2"], CSRC + "gemm_simt.cu")),
+                           # fp32 with the rows gathered from x: they land in dxbuf first
+                           else ((["simt_dA", "simt_dW13", "simt_dX", "simt_dW2"] if n == 4 else
+                                  ["gather_rows", "simt_dA", "simt_dW13", "simt_dX", "simt_dW2"]),
+                                 CSRC + "gemm_simt.cu")),
         "route_bwd": route_bwd,
         "dispatch_bwd": (["dispatch_bwd"], CSRC + "gather.cu"),
     }
@@ -409,10 +410,10 @@ def kernel_counts(w, T, e_active):
         "router_splitk_reduce": {"flops": 0, "bytes": 2 * T * E * 4},
         "softmax_topk": {"flops": 0, "bytes": 2 * T * E * 4 + 8 * Tk},
         "pft_count": {"flops": 0, "bytes": 4 * Tk},
-        "pft_count_scan": {"flops": 0, "bytes": 4 * Tk + 8 * E},
         "pft_scan": {"flops": 0, "bytes": 8 * E},
         "pft_scatter": {"flops": 0, "bytes": 16 * Tk},
         "dispatch": {"flops": 0, "bytes": T * h * s + Tk * h * s + 4 * Tk},
+        "gather_rows": {"flops": 0, "bytes": T * h * s + Tk * h * s + 4 * Tk},
         "tc_GATEUP": {"flops": 4 * Tk * h * f, "bytes": 2 * e_active * Wb + Tk * h * s + 3 * Tk * f * s},
         "tc_DOWN": {"flops": 2 * Tk * h * f, "bytes": e_active * Wb + Tk * f * s + Tk * h * s},
         "combine": {"flops": 2 * Tk * h, "bytes": Tk * h * s + T * h * s + 8 * Tk},
@@ -933,7 +934,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--fused", action="store_true",
-                    help="fold dispatch into the expert GEMMs (bf16 tensor-core path; rows gathered from x)")
+                    help="fold dispatch into the expert GEMMs (tensor-core paths, bf16 or fp32; rows gathered from x)")
     ap.add_argument("--fold-combine", action="store_true",
                     help="fold the combine into the down projection (bf16 tensor-core path, h % 256 == 0)")
     ap.add_argument("--no-graph", action="store_true",

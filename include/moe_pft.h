@@ -261,9 +261,11 @@ int moe_expert_ffn_bwd(const void* dybuf, const void* xbuf, const void* h1, cons
  * (gate/up in the forward, dW1/dW3 in the backward) load row p as x[token_ids[p]].
  * x: [T,h] dtype.  token_ids: [Tk] int32 from moe_pft_build (an id outside [0,T) reads as a
  * zero row and sets MOE_STATUS_BAD_INDEX, as moe_dispatch does).  Other arguments as in
- * moe_expert_ffn / moe_expert_ffn_bwd.  Runs on the tensor-core engine only: bf16 with h and f
- * multiples of 128 (moe_expert_ffn_gather_supported), and T * h < 2^31; otherwise
- * MOE_ERR_UNSUPPORTED.
+ * moe_expert_ffn / moe_expert_ffn_bwd.  Runs where a tensor-core engine does
+ * (moe_expert_ffn_gather_supported): bf16 or fp32 with h and f multiples of 128, and
+ * T * h < 2^31; otherwise MOE_ERR_UNSUPPORTED.  In fp32 the forward splits the gathered rows
+ * straight into the bf16 planes its GEMMs read; the backward (FMA engine) gathers the rows
+ * into dxbuf, takes dW1/dW3 from them, then overwrites dxbuf with dX.
  */
 int moe_expert_ffn_gather(const void* x, const int32_t* token_ids, int T, const int32_t* offsets,
                           const void* W1, const void* W3, const void* W2, int Tk, int E, int h, int f,

@@ -56,6 +56,12 @@ bool use_tensor_cores(int dtype, int h, int f) {
   return tc_supported(dtype, h, f);
 }
 
+// Shapes whose expert FFN can gather its token rows from x: the bf16 tensor-core engine, and the
+// fp32 forward on the tensor cores (its backward gathers the rows into dxbuf for the FMA engine).
+bool gather_engine(int dtype, int h, int f) {
+  return use_tensor_cores(dtype, h, f) || f32tc_supported(dtype, h, f, 1);
+}
+
 #define REQUIRE(cond, code, msg)                                        \
   do {                                                                  \
     if (!(cond)) return fail(code, msg);                                \
@@ -336,8 +342,8 @@ int expert_ffn_impl(const char* fn, TokenRows xr, const int32_t* offsets, const 
   REQUIRE(ws != nullptr && ws_bytes >= moe_workspace_size(MOE_OP_EXPERT_FFN, Tk, h, E, 1, f, dtype),
           MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace too small");
   if (Tk == 0) return MOE_OK;
-  REQUIRE(xr.xbuf != nullptr || use_tensor_cores(dtype, h, f), MOE_ERR_UNSUPPORTED,
-          "moe_expert_ffn_gather: needs the tensor-core engine (bf16, h and f multiples of 128)");
+  REQUIRE(xr.xbuf != nullptr || gather_engine(dtype, h, f), MOE_ERR_UNSUPPORTED,
+          "moe_expert_ffn_gather: needs a tensor-core engine (bf16 or fp32, h and f multiples of 128)");
   if (xr.xbuf == nullptr) {
     REQUIRE(xr.T >= 1, MOE_ERR_INVALID_ARG, "moe_expert_ffn_gather: need T >= 1");
     REQUIRE((long long)xr.T * h < (1LL << 31), MOE_ERR_UNSUPPORTED, "moe_expert_ffn_gather: T * h >= 2^31");
@@ -350,10 +356,11 @@ int expert_ffn_impl(const char* fn, TokenRows xr, const int32_t* offsets, const 
       return tc_failure(fn);
   } else if (f32tc_supported(dtype, h, f, E)) {
     REQUIRE(aligned16(ws), MOE_ERR_WORKSPACE, "moe_expert_ffn: workspace not 16-byte aligned");
-    if (f32tc_expert_ffn(static_cast<const float*>(xr.xbuf), offsets, static_cast<const float*>(W1),
-                         static_cast<const float*>(W3), static_cast<const float*>(W2), Tk, E, h, f,
-                         static_cast<float*>(ybuf), static_cast<float*>(h1), static_cast<float*>(h3),
-                         static_cast<float*>(a), static_cast<char*>(ws) + sizeof(WsHeader), status_of(ws), st) != 0)
+    if (f32tc_expert_ffn(static_cast<const float*>(xr.xbuf), static_cast<const float*>(xr.x), xr.token_ids, xr.T,
+                         offsets, static_cast<const float*>(W1), static_cast<const float*>(W3),
+                         static_cast<const float*>(W2), Tk, E, h, f, static_cast<float*>(ybuf),
+                         static_cast<float*>(h1), static_cast<float*>(h3), static_cast<float*>(a),
+                         static_cast<char*>(ws) + sizeof(WsHeader), status_of(ws), st) != 0)
       return tc_failure(fn);
   } else {
     simt_expert_ffn(dtype, xr.xbuf, offsets, W1, W3, W2, Tk, E, h, f, ybuf, h1, h3, a, st);
@@ -380,8 +387,8 @@ int expert_ffn_bwd_impl(const char* fn, const void* dybuf, TokenRows xr, const v
     cudaMemsetAsync(dW2, 0, wb, st);
     return check_launch(fn);
   }
-  REQUIRE(xr.xbuf != nullptr || use_tensor_cores(dtype, h, f), MOE_ERR_UNSUPPORTED,
-          "moe_expert_ffn_bwd_gather: needs the tensor-core engine (bf16, h and f multiples of 128)");
+  REQUIRE(xr.xbuf != nullptr || gather_engine(dtype, h, f), MOE_ERR_UNSUPPORTED,
+          "moe_expert_ffn_bwd_gather: needs a tensor-core engine (bf16 or fp32, h and f multiples of 128)");
   if (xr.xbuf == nullptr) {
     REQUIRE(xr.T >= 1, MOE_ERR_INVALID_ARG, "moe_expert_ffn_bwd_gather: need T >= 1");
     REQUIRE((long long)xr.T * h < (1LL << 31), MOE_ERR_UNSUPPORTED, "moe_expert_ffn_bwd_gather: T * h >= 2^31");
@@ -397,7 +404,14 @@ int expert_ffn_bwd_impl(const char* fn, const void* dybuf, TokenRows xr, const v
                           dh1, dh3, status_of(ws), st) != 0)
       return tc_failure(fn);
   } else {
-    simt_expert_ffn_bwd(dtype, dybuf, xr.xbuf, h1, h3, a, offsets, W1, W3, W2, Tk, E, h, f, dxbuf, dW1,
+    // the gathered fp32 backward: the FMA engine reads the token rows from dxbuf, gathered there
+    // first; it takes dW1/dW3 (their only reader) before dX overwrites them
+    const void* rows = xr.xbuf;
+    if (rows == nullptr) {
+      launch_dispatch(dtype, xr.x, xr.token_ids, xr.T, Tk, h, dxbuf, status_of(ws), st);
+      rows = dxbuf;
+    }
+    simt_expert_ffn_bwd(dtype, dybuf, rows, h1, h3, a, offsets, W1, W3, W2, Tk, E, h, f, dxbuf, dW1,
                         dW3, dW2, dh1, dh3, st);
   }
   return check_launch(fn);
@@ -465,7 +479,7 @@ int moe_expert_ffn_fused(const void* xbuf, const void* x, const int32_t* token_i
 }
 
 int moe_expert_ffn_gather_supported(int h, int f, int dtype) {
-  return dtype_ok(dtype) && h >= 8 && f >= 8 && use_tensor_cores(dtype, h, f) ? 1 : 0;
+  return dtype_ok(dtype) && h >= 8 && f >= 8 && gather_engine(dtype, h, f) ? 1 : 0;
 }
 
 int moe_combine(const void* ybuf, const int32_t* slot_of, const float* topk_w, int T, int k,

@@ -446,6 +446,43 @@ __global__ void __launch_bounds__(256) split3_rows_kernel(const float* __restric
     split3_vec8(__ldg(s + 2 * i), __ldg(s + 2 * i + 1), d0 + i, d1 + i, d2 + i);
 }
 
+// The dispatch folded into the split of the token rows: dst[p][row] = plane p of
+// x[token_ids[row]], a CTA per row at a time with the next row's id loaded ahead.  An id outside
+// [0,T) gives zero planes and sets MOE_STATUS_BAD_INDEX, as moe_dispatch does.  Also zeroes the
+// next launches' two split counters (zero2).
+__global__ void __launch_bounds__(256) split3_gather_kernel(const float* __restrict__ x,
+                                                            const int* __restrict__ token_ids, int T,
+                                                            long long Tk, int h, __nv_bfloat16* __restrict__ dst,
+                                                            int* zero2, int* status) {
+  if (blockIdx.x == 0 && threadIdx.x < 2) zero2[threadIdx.x] = 0;
+  const int hv = h / 8;  // 8-value items per row
+  const long long n = Tk * h;
+  uint4* d0 = reinterpret_cast<uint4*>(dst);
+  uint4* d1 = reinterpret_cast<uint4*>(dst + n);
+  uint4* d2 = reinterpret_cast<uint4*>(dst + 2 * n);
+  long long row = blockIdx.x;
+  int t = row < Tk ? __ldg(token_ids + row) : 0;
+  for (; row < Tk; row += gridDim.x) {
+    const long long nxt = row + gridDim.x;
+    const int tn = nxt < Tk ? __ldg(token_ids + nxt) : 0;
+    const long long o = row * hv;
+    if ((unsigned)t < (unsigned)T) {
+      const float4* s = reinterpret_cast<const float4*>(x + (size_t)t * h);
+      for (int c = threadIdx.x; c < hv; c += blockDim.x)
+        split3_vec8(__ldg(s + 2 * c), __ldg(s + 2 * c + 1), d0 + o + c, d1 + o + c, d2 + o + c);
+    } else {
+      if (threadIdx.x == 0) flag_status(status, MOE_STATUS_BAD_INDEX);
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = threadIdx.x; c < hv; c += blockDim.x) {
+        d0[o + c] = z;
+        d1[o + c] = z;
+        d2[o + c] = z;
+      }
+    }
+    t = tn;
+  }
+}
+
 template <int MODE>
 int flaunch(const F32Params& p0, cudaStream_t st) {
   F32Params p = p0;
@@ -480,9 +517,9 @@ size_t f32tc_scratch(long long Tk, int E, int h, int f) {
   return r256((size_t)3 * Tk * h * 2) + r256((size_t)3 * Tk * f * 2) + 2 * r256((size_t)3 * E * h * f * 2) + 256;
 }
 
-int f32tc_expert_ffn(const float* xbuf, const int* offsets, const float* W1, const float* W3, const float* W2,
-                     int Tk, int E, int h, int f, float* ybuf, float* h1, float* h3, float* a, void* scratch,
-                     int* status, cudaStream_t st) {
+int f32tc_expert_ffn(const float* xbuf, const float* x, const int* token_ids, int T, const int* offsets,
+                     const float* W1, const float* W3, const float* W2, int Tk, int E, int h, int f, float* ybuf,
+                     float* h1, float* h3, float* a, void* scratch, int* status, cudaStream_t st) {
   char* sp = static_cast<char*>(scratch);
   const size_t wbytes = r256((size_t)3 * E * h * f * 2);
   __nv_bfloat16* xp = reinterpret_cast<__nv_bfloat16*>(sp);
@@ -493,7 +530,8 @@ int f32tc_expert_ffn(const float* xbuf, const int* offsets, const float* W1, con
   int* ctr = reinterpret_cast<int*>(wbase + 2 * wbytes);                    // the two split queues
   const int blocks = 8 * num_sms();
   const long long per = (long long)h * f;
-  split3_rows_kernel<<<blocks, 256, 0, st>>>(xbuf, (long long)Tk * h, xp, ctr);
+  if (xbuf != nullptr) split3_rows_kernel<<<blocks, 256, 0, st>>>(xbuf, (long long)Tk * h, xp, ctr);
+  else split3_gather_kernel<<<blocks, 256, 0, st>>>(x, token_ids, T, Tk, h, xp, ctr, status);
   count_launch(st);
   const dim3 wgrid(16, E);
   split3_experts_kernel<<<wgrid, 256, 0, st>>>(W1, offsets, per, (long long)E * per, wpA);

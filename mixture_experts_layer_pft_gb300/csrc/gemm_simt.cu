@@ -470,6 +470,14 @@ void expert_ffn_bwd_t(const void* dybuf, const void* xbuf, const void* h1, const
   da.M = Tk; da.N = f; da.offsets = offsets; da.G = E;
   da.C = dh1; da.C2 = dh3; da.ldc = f; da.X1 = h1; da.X2 = h3;
   run<T, T, T, false, true, false, EPI_DSWIGLU>(da, st);
+  // dW1[e] = X^T dh1, dW3[e] = X^T dh3 (K = the expert's rows).  It runs before dX: the gathered
+  // backward passes its token rows in dxbuf, which dX then overwrites.
+  Args w13 = blank();
+  w13.A0 = xbuf; w13.lda = h; w13.M = h;
+  w13.B0 = dh1; w13.B1 = dh3; w13.ldb = f; w13.N = f;
+  w13.offsets = offsets; w13.G = E;
+  w13.C = dW1; w13.C2 = dW3; w13.ldc = f; w13.strideC = (long long)h * f;
+  run<T, T, T, true, false, true, EPI_STORE2>(w13, st);
   // dX = dh1 W1^T + dh3 W3^T (W1[e] stored [h,f] = [N,K])
   Args dx = blank();
   dx.A0 = dh1; dx.A1 = dh3; dx.lda = f; dx.K0 = f; dx.K1 = f;
@@ -477,13 +485,6 @@ void expert_ffn_bwd_t(const void* dybuf, const void* xbuf, const void* h1, const
   dx.M = Tk; dx.N = h; dx.offsets = offsets; dx.G = E;
   dx.C = dxbuf; dx.ldc = h;
   run<T, T, T, false, true, false, EPI_STORE>(dx, st);
-  // dW1[e] = X^T dh1, dW3[e] = X^T dh3 (K = the expert's rows)
-  Args w13 = blank();
-  w13.A0 = xbuf; w13.lda = h; w13.M = h;
-  w13.B0 = dh1; w13.B1 = dh3; w13.ldb = f; w13.N = f;
-  w13.offsets = offsets; w13.G = E;
-  w13.C = dW1; w13.C2 = dW3; w13.ldc = f; w13.strideC = (long long)h * f;
-  run<T, T, T, true, false, true, EPI_STORE2>(w13, st);
   // dW2[e] = a^T dY
   Args w2 = blank();
   w2.A0 = a; w2.lda = f; w2.M = f;

@@ -85,13 +85,14 @@ int tc_router_bwd(const void* x, const float* Wg, const float* d_logits, int T, 
                   float* dWg, float* dx_router, void* scratch, bool dl_planes_ready, int* status, cudaStream_t st);
 
 // gemm_f32tc.cu -- the fp32 expert forward on tcgen05 over exact three-plane bf16 splits (h and f
-// multiples of 128).  The scratch (token planes of xbuf and a, one weight tensor's planes) follows
-// the workspace header.
+// multiples of 128).  The scratch (token planes of the rows and of a, two weight-plane buffers,
+// two split counters) follows the workspace header.  The token rows are xbuf, or, with xbuf
+// NULL, x[token_ids[p]] (T rows of x).
 bool f32tc_supported(int dtype, int h, int f, int E);
 size_t f32tc_scratch(long long Tk, int E, int h, int f);
-int f32tc_expert_ffn(const float* xbuf, const int* offsets, const float* W1, const float* W3, const float* W2,
-                     int Tk, int E, int h, int f, float* ybuf, float* h1, float* h3, float* a, void* scratch,
-                     int* status, cudaStream_t st);
+int f32tc_expert_ffn(const float* xbuf, const float* x, const int* token_ids, int T, const int* offsets,
+                     const float* W1, const float* W3, const float* W2, int Tk, int E, int h, int f, float* ybuf,
+                     float* h1, float* h3, float* a, void* scratch, int* status, cudaStream_t st);
 
 // gemm_tc.cu -- tcgen05/TMEM/TMA grouped GEMMs (bf16; h and f multiples of 128)
 bool tc_supported(int dtype, int h, int f);

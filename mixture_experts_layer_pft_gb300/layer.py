@@ -17,12 +17,14 @@ class LayerBuffers:
     """Device buffers of one layer.
 
     With ``fused`` the expert GEMMs gather their token rows from x (the library's
-    moe_expert_ffn_gather / moe_expert_ffn_bwd_gather: bf16, h and f multiples of 128), so the
-    dispatched buffer xbuf is never written and ``xbuf`` is None.  With ``fold_combine`` the down
-    projection also writes y (moe_expert_ffn_fused; h a multiple of 256), so no combine call
-    runs.  Either way the results are the same bits as the separate calls.  The defaults are
-    the separate calls: the gathered loads, 16-byte copies from one producer warp, keep too few
-    bytes in flight to match the tensor loads of a dispatched buffer.
+    moe_expert_ffn_gather / moe_expert_ffn_bwd_gather: bf16 or fp32, h and f multiples of 128),
+    so the dispatched buffer xbuf is never written and ``xbuf`` is None.  With ``fold_combine``
+    the down projection also writes y (moe_expert_ffn_fused; bf16, h a multiple of 256), so no
+    combine call runs.  Either way the results are the same bits as the separate calls.  The
+    defaults are the separate calls: in bf16 the gathered loads, 16-byte copies from one producer
+    warp, keep too few bytes in flight to match the tensor loads of a dispatched buffer.  In fp32
+    the gathered forward is the faster one (its row split replaces both the dispatch copy and the
+    split of xbuf).
     """
 
     def __init__(self, T: int, h: int, E: int, k: int, f: int, dtype: torch.dtype, device="cuda",
@@ -30,9 +32,9 @@ class LayerBuffers:
                  fused: bool = False, fold_combine: bool = False):
         self.T, self.h, self.E, self.k, self.f, self.dtype = T, h, E, k, f, dtype
         if (fused or fold_combine) and not B.moe_expert_ffn_gather_supported(h, f, dtype):
-            raise ValueError("fused layer needs bf16 with h and f multiples of 128")
-        if fold_combine and h % 256 != 0:
-            raise ValueError("the combine fold needs h a multiple of 256")
+            raise ValueError("fused layer needs bf16 or fp32 with h and f multiples of 128")
+        if fold_combine and (h % 256 != 0 or dtype != torch.bfloat16):
+            raise ValueError("the combine fold needs bf16 and h a multiple of 256")
         self.fused = bool(fused)
         self.fold_combine = bool(fold_combine)
         self.gate, self.renorm = gate, renorm

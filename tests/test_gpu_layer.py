@@ -425,6 +425,30 @@ def test_fused_layer_equals_dispatched_layer(M, cfg):
             assert torch.equal(o[n], t), n
 
 
+@pytest.mark.parametrize("shape", [("longseq", 2048, 2048, 128, 2, 2048, True, False),
+                                   ("fp32-fwd-bwd", 600, 256, 12, 3, 384, False, True)])
+def test_fused_fp32_layer_equals_dispatched_layer(M, shape):
+    """fp32 on the tensor cores: the layer whose expert FFN gathers its rows from x (the forward
+    splits them into planes, the backward gathers them into dxbuf) gives the same bits as the
+    layer with a dispatch call, forward only at the long-sequence shape and fwd+bwd."""
+    layer, workloads = M
+    name, T, h, E, k, f, skew, bwd = shape
+    w = workloads.Workload(name, T, h, E, k, f, "f32", skew, bwd, 40 + T)
+    inp = workloads.make_inputs(w, "cuda")
+    outs = []
+    for fused in (False, True):
+        b = layer.LayerBuffers(T, h, E, k, f, torch.float32, backward=bwd, fused=fused)
+        assert (b.xbuf is None) == fused
+        layer.step(inp, b)
+        torch.cuda.synchronize()
+        assert binding_status(b) == 0
+        names = ("ybuf", "h1", "h3", "a", "y") + (("dxbuf", "dW1", "dW3", "dW2", "dWg", "dx") if bwd else ())
+        outs.append({n: getattr(b, n).clone() for n in names})
+        del b
+    for n, t in outs[0].items():
+        assert torch.equal(outs[1][n], t), n
+
+
 @pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
 def test_empty_batch_layer(M, dt):
     """A step over zero tokens runs every stage, leaves nothing to route or combine and gives

@@ -237,7 +237,7 @@ def run_pft(B, idx_np, E):
 @pytest.mark.parametrize("T,E,k,skew", [(1, 8, 2, False), (37, 8, 2, False), (2048, 64, 6, False),
                                         (4096, 128, 6, True), (4096, 256, 8, False), (5000, 7, 7, False),
                                         (333, 1, 1, False), (16384, 128, 2, True), (131072, 256, 8, False),
-                                        (999, 1000, 3, False)])
+                                        (999, 1000, 3, False), (200000, 16, 1, False), (40000, 1024, 2, False)])
 def test_pft_build_bitexact(B, T, E, k, skew):
     idx = oracle_routing(T, E, k, 100 + T, skew)
     out, ws = run_pft(B, idx, E)
@@ -586,7 +586,7 @@ def test_expert_ffn_forward_and_backward(B, T, h, E, k, f, dt, skew):
     assert B.moe_check_status(ws) == 0
 
 
-GATHER_SHAPES = [s for s in EXPERT_SHAPES if s[5] == torch.bfloat16 and s[1] % 128 == 0 and s[4] % 128 == 0]
+GATHER_SHAPES = [s for s in EXPERT_SHAPES if s[1] % 128 == 0 and s[4] % 128 == 0]  # bf16 and fp32
 
 
 @pytest.mark.parametrize("bad_id", [False, True])
@@ -594,7 +594,8 @@ GATHER_SHAPES = [s for s in EXPERT_SHAPES if s[5] == torch.bfloat16 and s[1] % 1
 def test_gathered_expert_ffn_equals_dispatch_then_ffn(B, T, h, E, k, f, dt, skew, bad_id):
     """The expert GEMMs that gather their token rows from x give the same bits as dispatching
     xbuf first, forward and backward; an out-of-range token id reads as a zero row and sets the
-    status bit on both paths."""
+    status bit on both paths.  In fp32 the forward splits the gathered rows straight into planes
+    and the backward gathers them into dxbuf ahead of dW1/dW3."""
     from mixture_experts_layer_pft_gb300.workloads import random_tensor
 
     assert B.moe_expert_ffn_gather_supported(h, f, dt)
@@ -630,10 +631,12 @@ def test_gathered_expert_ffn_equals_dispatch_then_ffn(B, T, h, E, k, f, dt, skew
 
 
 def test_gathered_expert_ffn_rejects_the_simt_engine(B):
-    """fp32 (FMA engine) has no gathered form: the call reports MOE_ERR_UNSUPPORTED."""
-    assert not B.moe_expert_ffn_gather_supported(256, 256, torch.float32)
+    """Shapes only the FMA engine takes (f not a multiple of 128) have no gathered form: the
+    call reports MOE_ERR_UNSUPPORTED."""
+    assert B.moe_expert_ffn_gather_supported(256, 256, torch.float32)
+    assert not B.moe_expert_ffn_gather_supported(256, 192, torch.float32)
     assert not B.moe_expert_ffn_gather_supported(256, 192, torch.bfloat16)
-    T, h, E, k, f = 16, 256, 4, 2, 256
+    T, h, E, k, f = 16, 256, 4, 2, 192
     x = torch.zeros(T, h, device="cuda")
     tok = torch.zeros(T * k, dtype=torch.int32, device="cuda")
     off = torch.zeros(E + 1, dtype=torch.int32, device="cuda")
@@ -644,7 +647,7 @@ def test_gathered_expert_ffn_rejects_the_simt_engine(B):
         B.moe_expert_ffn_gather(x, tok, off, W, W, W.transpose(1, 2).contiguous(), o, o, o, o, ws)
 
 
-FOLD_SHAPES = [s for s in GATHER_SHAPES if s[1] % 256 == 0]
+FOLD_SHAPES = [s for s in GATHER_SHAPES if s[5] == torch.bfloat16 and s[1] % 256 == 0]
 
 
 @pytest.mark.parametrize("gathered", [False, True])
