@@ -175,6 +175,73 @@ class CapturedStep:
         self.graph.replay()
 
 
+class HostPipeline:
+    """Layer steps over batches in pinned host memory, with the copies off the critical path.
+
+    Two device slots hold the tokens (x, and dy for the backward) of consecutive steps: step
+    i + 1's upload runs on a copy stream into the other slot while step i computes, and y and dx
+    download on a second copy stream while later work runs.  The current stream orders the
+    compute: a step waits for its own upload, and for the download of the previous step's y
+    (and dx) before it overwrites b.y (and b.dx).  ``submit`` returns at once.  ``finish`` makes
+    the current stream wait for every download, so the host buffers of every submitted step are
+    complete once the current stream is.
+
+    ``inp`` holds the weights (and the router bias); its x and dy are slot 0.  The host buffers
+    passed to ``submit`` must stay untouched until the current stream passes ``finish``.
+    """
+
+    def __init__(self, inp: dict, b: LayerBuffers):
+        self.b = b
+        self.inp = inp
+        dev = inp["x"].device
+        self.x = [inp["x"], torch.empty_like(inp["x"])]
+        self.dy = [inp["dy"], torch.empty_like(inp["dy"])] if b.backward else [None, None]
+        self.up = torch.cuda.Stream(device=dev)
+        self.down = torch.cuda.Stream(device=dev)
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        self.slot_free = [ev(), ev()]   # the compute that last read a slot is done
+        self.ready = [ev(), ev()]       # a slot's upload is done
+        self.y_done, self.y_free = ev(), ev()
+        self.dx_done, self.dx_free = ev(), ev()
+        cur = torch.cuda.current_stream()
+        for e in self.slot_free + [self.y_free, self.dx_free]:
+            e.record(cur)
+        self.i = 0
+
+    def submit(self, hx: torch.Tensor, hy: torch.Tensor, hdy: torch.Tensor | None = None,
+               hdx: torch.Tensor | None = None):
+        b, s = self.b, self.i % 2
+        cur = torch.cuda.current_stream()
+        self.up.wait_event(self.slot_free[s])
+        with torch.cuda.stream(self.up):
+            self.x[s].copy_(hx, non_blocking=True)
+            if b.backward:
+                self.dy[s].copy_(hdy, non_blocking=True)
+            self.ready[s].record(self.up)
+        inp = dict(self.inp, x=self.x[s], dy=self.dy[s])
+        cur.wait_event(self.ready[s])
+        cur.wait_event(self.y_free)  # the previous step's y has left b.y
+        forward(inp, b)
+        self.y_done.record(cur)
+        self.down.wait_event(self.y_done)
+        with torch.cuda.stream(self.down):
+            hy.copy_(b.y, non_blocking=True)
+            self.y_free.record(self.down)
+        if b.backward:
+            cur.wait_event(self.dx_free)  # the previous step's dx has left b.dx
+            backward(inp, inp["dy"], b)
+            self.dx_done.record(cur)
+            self.down.wait_event(self.dx_done)
+            with torch.cuda.stream(self.down):
+                hdx.copy_(b.dx, non_blocking=True)
+                self.dx_free.record(self.down)
+        self.slot_free[s].record(cur)
+        self.i += 1
+
+    def finish(self):
+        torch.cuda.current_stream().wait_stream(self.down)
+
+
 class GShardBuffers:
     """Device buffers of the capacity-buffer (GShard-style) forward at capacity C: the masks
     [T,E,C], the padded expert buffers [E*C, ...] and the padded segment offsets e*C.  The gate's

@@ -382,6 +382,40 @@ def test_host_buffer_step_equals_device_step(M, cfg):
             assert torch.equal(hdx, want_dx)
 
 
+@pytest.mark.parametrize("cfg", [0, 1, 4])
+def test_host_pipeline_equals_device_steps(M, cfg):
+    """HostPipeline over four different batches (two device slots, uploads and downloads on
+    copy streams beside the compute): each batch's y and dx are the bits of a device-resident
+    step on that batch."""
+    layer, workloads = M
+    w = workloads.WORKLOADS[cfg]
+    T = min(w.T, 2048)
+    batches = []
+    for i in range(4):  # the same weights, different tokens; one copy of the weights kept
+        inp = workloads.make_inputs(w, "cuda", T=T, token_seed=500 + i)
+        batches.append(inp if i == 0 else dict(batches[0], x=inp["x"], dy=inp["dy"]))
+        del inp
+    b = layer.LayerBuffers(T, w.h, w.E, w.k, w.f, w.torch_dtype(), backward=w.backward)
+    want = []
+    for inp in batches:
+        layer.step(inp, b)
+        torch.cuda.synchronize()
+        want.append((b.y.cpu(), b.dx.cpu() if w.backward else None))
+    host = [(inp["x"].cpu().pin_memory(), inp["dy"].cpu().pin_memory()) for inp in batches]
+    outs = [(torch.zeros_like(hx).pin_memory(), torch.zeros_like(hx).pin_memory() if w.backward else None)
+            for hx, _ in host]
+    weights = dict(batches[0], x=torch.zeros_like(batches[0]["x"]), dy=torch.zeros_like(batches[0]["dy"]))
+    pipe = layer.HostPipeline(weights, b)
+    for (hx, hdy), (hy, hdx) in zip(host, outs):
+        pipe.submit(hx, hy, hdy, hdx)
+    pipe.finish()
+    torch.cuda.current_stream().synchronize()
+    for i, ((hy, hdx), (wy, wdx)) in enumerate(zip(outs, want)):
+        assert torch.equal(hy, wy), i
+        if w.backward:
+            assert torch.equal(hdx, wdx), i
+
+
 def test_captured_step_replays_the_same_bits(M):
     """CapturedStep (the step as one CUDA graph) reproduces the stream-launched step exactly."""
     layer, workloads = M
