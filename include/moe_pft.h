@@ -20,8 +20,8 @@
  *     probabilities, gate weights and their gradients) are always fp32.  Arithmetic
  *     accumulates in fp32; each stored tensor is rounded once (round to nearest even).
  *   - `ws` is a workspace of at least moe_workspace_size(op, ...) bytes.  Its first 256 bytes
- *     hold a sticky device status word and counters: zero them once with moe_status_reset
- *     before the first call.  One workspace sized for the largest op may serve every op on
+ *     hold a sticky device status word (the rest is unused): zero them once with
+ *     moe_status_reset before the first call.  One workspace sized for the largest op may serve every op on
  *     one stream; calls that share a workspace must not overlap on the GPU.
  *   - Return value: MOE_OK, or a negative MOE_ERR_* code for errors found on the host before
  *     any launch (bad argument, unsupported shape or alignment, small workspace) or reported
@@ -84,7 +84,7 @@ enum moe_op {
 /* Workspace bytes `op` needs at these sizes (always >= 256, a multiple of 256). */
 size_t moe_workspace_size(int op, int T, int h, int E, int k, int f, int dtype);
 
-/* Zero the status word and counters at the start of `ws` (asynchronous on `stream`). */
+/* Zero the status word at the start of `ws` (asynchronous on `stream`). */
 int moe_status_reset(void* ws, void* stream);
 
 /* Synchronise `stream`, read the status word into *code (host) and return MOE_OK when it is
@@ -198,7 +198,7 @@ int moe_pft_build(const int32_t* topk_idx, int T, int E, int k, int32_t* num_ids
  *     the id of the CUDA context it belongs to; after a device reset (a new primary context) the
  *     next call looks it up again, so that call too should come before any stream capture.
  *   - Shared state: every call on a device uses the same array.  Each call clears the array's
- *     header (status word and counter) on `stream` before its kernels run, so calls queued one
+ *     header (its status word) on `stream` before its kernels run, so calls queued one
  *     after another on one stream are safe; calls that overlap on the GPU (different streams,
  *     or different host threads without ordering) race and corrupt each other's results.
  *   - Errors: an expert id outside [0,E) is dropped and its slot_of entry set to -1, as in

@@ -12,8 +12,7 @@ namespace moe {
 // Layout of the 256-byte workspace header.
 struct WsHeader {
   int status;           // sticky MOE_STATUS_* bits
-  unsigned pft_done;    // PFT build: chunks that finished their histogram (reset by the last)
-  int pad[62];
+  int pad[63];          // unused
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
