@@ -19,7 +19,8 @@
 //   H1     h1^T [f x n]     W1[e] planes [h, f]                   xbuf planes [Tk, h]                 h
 //   H3A    h3^T [f x n]     W3[e] planes [h, f]                   xbuf planes                         h
 //   Y      y^T  [h x n]     W2[e] planes [f, h]                   a planes [Tk, f]                    f
-// H3A's epilogue reads h1 back and writes h3, a = silu(h1) h3 and the three planes of a.
+// H3A's epilogue reads h1 back and writes h3, a = silu(h1) h3 and the three planes of a.  The
+// token planes come from xbuf, or, with the dispatch folded in, straight from x[token_ids[p]].
 //
 // Warp roles (one CTA per SM): warp 0 issues the TMA loads (three A and three B planes per stage),
 // warp 1 owns TMEM (two buffers of the accumulator pair) and issues the MMAs, warps 2-9 drain the
@@ -513,7 +514,7 @@ bool f32tc_supported(int dtype, int h, int f, int E) {
 
 size_t f32tc_scratch(long long Tk, int E, int h, int f) {
   // token planes of xbuf and of a, and two weight-plane buffers: one GEMM reads one while its
-  // splitter warp fills the other for the next GEMM
+  // side warp (then the whole CTA) fills the other for the next GEMM
   return r256((size_t)3 * Tk * h * 2) + r256((size_t)3 * Tk * f * 2) + 2 * r256((size_t)3 * E * h * f * 2) + 256;
 }
 

@@ -15,10 +15,12 @@
 //      per entry in a per-expert bitmap over its tokens (bit t of expert e: token t chose e).
 //      Because a token's k experts are distinct, an entry's rank among its expert's entries of
 //      the tile is the number of bits below its own: a popcount of its word plus the prefix of
-//      the words before it, which one pass per expert computes.  slot_of is written in index
-//      order; token_ids and expert_ids are read off the bitmap word by word in expert order, so
-//      consecutive lanes write consecutive rows of a bucket.  A repeated id inside a row (which
-//      the bitmap would merge) is reported as a bad index.
+//      the words before it, which one pass per expert computes (each word's cell then holds the
+//      global row of its first entry).  slot_of is written in index order; token_ids goes through
+//      a tile-sorted copy in shared memory, so consecutive lanes write consecutive rows of a
+//      bucket; expert_ids depends on offsets alone and each CTA fills its share of it as plain
+//      runs.  A repeated id inside a row (which the bitmap would merge) is reported as a bad
+//      index.
 #include "common.cuh"
 #include "internal.h"
 
