@@ -237,7 +237,8 @@ def run_pft(B, idx_np, E):
 @pytest.mark.parametrize("T,E,k,skew", [(1, 8, 2, False), (37, 8, 2, False), (2048, 64, 6, False),
                                         (4096, 128, 6, True), (4096, 256, 8, False), (5000, 7, 7, False),
                                         (333, 1, 1, False), (16384, 128, 2, True), (131072, 256, 8, False),
-                                        (999, 1000, 3, False), (200000, 16, 1, False), (40000, 1024, 2, False)])
+                                        (999, 1000, 3, False), (200000, 16, 1, False), (40000, 1024, 2, False),
+                                        (257, 600, 300, False)])
 def test_pft_build_bitexact(B, T, E, k, skew):
     idx = oracle_routing(T, E, k, 100 + T, skew)
     out, ws = run_pft(B, idx, E)
