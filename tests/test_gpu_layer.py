@@ -565,6 +565,35 @@ def test_random_bf16_layers(M, T, h, E, k, f, skew):
     assert binding_status(b) == 0
 
 
+@pytest.mark.parametrize("T,h,E,k,f,skew", _random_layer_shapes(8, 4242))
+def test_random_fp32_layers(M, T, h, E, k, f, skew):
+    """Seeded random fp32 shapes (h and f multiples of 128: the forward on the tensor cores over
+    exact bf16 planes, the backward on the FMA engine): the layer against the oracle at the fp32
+    tolerance, and the layer with the rows gathered from x bit for bit against it."""
+    layer, workloads = M
+    w = workloads.Workload("random-fp32", T, h, E, k, f, "f32", skew, True, T + h + E + 1)
+    inp = workloads.make_inputs(w, "cuda")
+    b = layer.LayerBuffers(T, h, E, k, f, torch.float32)
+    layer.step(inp, b)
+    torch.cuda.synchronize()
+    assert binding_status(b) == 0
+    x, Wg = np64(inp["x"]), np64(inp["Wg"])
+    bias = None if inp["bias"] is None else np64(inp["bias"])
+    exact = O.router_logits(x, Wg, bias, "f64")
+    una = routing_checks(b, exact, k)
+    W1, W3, W2, dy = np64(inp["W1"]), np64(inp["W3"]), np64(inp["W2"]), np64(inp["dy"])
+    fw = O.layer_forward(x, Wg, W1, W3, W2, k, bias, "f32")
+    bw = O.layer_backward(fw, x, Wg, W1, W3, W2, dy, "f32")
+    check_layer_against_oracle(b, fw, bw, una, npi(b.topk_idx), O.topk(exact, k), E, "f32")
+    ref = {n: getattr(b, n).clone() for n in ("y", "h1", "h3", "a", "dx", "dW1", "dW3", "dW2", "dWg")}
+    bf = layer.LayerBuffers(T, h, E, k, f, torch.float32, fused=True)
+    layer.step(inp, bf)
+    torch.cuda.synchronize()
+    assert binding_status(bf) == 0
+    for n, t in ref.items():
+        assert torch.equal(getattr(bf, n), t), n
+
+
 def binding_status(b):
     from mixture_experts_layer_pft_gb300 import binding
 

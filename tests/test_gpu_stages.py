@@ -252,6 +252,32 @@ def test_pft_build_bitexact(B, T, E, k, skew):
         np.testing.assert_array_equal(npi(out2[n]), want[n])
 
 
+def _random_pft_shapes(n, seed):
+    """Seeded (T, E, k, skew): T log-uniform up to 60000, E up to 1024, k up to min(E, 16), with
+    T * E kept small enough for the oracle's top-k."""
+    g = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        E = int(g.integers(1, 1025))
+        k = int(g.integers(1, min(E, 16) + 1))
+        T = int(np.exp(g.uniform(0, np.log(60000))))
+        if T * E <= 20_000_000:
+            out.append((max(T, 1), E, k, bool(g.random() < 0.3)))
+    return out
+
+
+@pytest.mark.parametrize("T,E,k,skew", _random_pft_shapes(16, 31337))
+def test_pft_build_random_shapes(B, T, E, k, skew):
+    """Seeded random shapes (bitmap tiles of every width, ranges of one to several tiles):
+    bit for bit against the oracle."""
+    idx = oracle_routing(T, E, k, 7 * T + E, skew)
+    out, ws = run_pft(B, idx, E)
+    want = O.pft_build(idx, E)
+    for n in ("num_ids", "offsets", "token_ids", "expert_ids", "slot_of"):
+        np.testing.assert_array_equal(npi(out[n]), want[n], err_msg=n)
+    assert B.moe_check_status(ws) == 0
+
+
 def test_pft_build_at_the_scaled_benchmark_size(B):
     """T = 2^20 tokens, k = 8, E = 256 (8.4 M rows), where the oracle's plain loops would take
     minutes: properties that fix the arrays uniquely.  The pairs (token_ids[p], expert_ids[p]) are
