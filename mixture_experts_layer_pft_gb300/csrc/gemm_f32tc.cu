@@ -100,9 +100,10 @@ __device__ __noinline__ void split_next_weights(const F32Params& p, const int* s
   uint4* d0 = reinterpret_cast<uint4*>(p.ndst);
   uint4* d1 = reinterpret_cast<uint4*>(p.ndst + n);
   uint4* d2 = reinterpret_cast<uint4*>(p.ndst + 2 * n);
-  while (stop == nullptr || *stop < kFGemmWarps) {
-    int it = 0;
-    if (lane == 0) it = atomicAdd(p.split_ctr, 1);
+  for (;;) {
+    // lane 0 alone reads the stop flag and takes the chunk, so the warp stays converged
+    int it = nitems;
+    if (lane == 0 && (stop == nullptr || *stop < kFGemmWarps)) it = atomicAdd(p.split_ctr, 1);
     it = __shfl_sync(0xffffffffu, it, 0);
     if (it >= nitems) break;
     const long long g0 = (long long)s_act[it / ipe] * (p.nper / 8) + (long long)(it % ipe) * G8;
