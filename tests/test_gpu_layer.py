@@ -293,6 +293,31 @@ def test_full_size_layer_sampled(M, cfg, ntok, nexp):
     check_sampled_experts(b, inp, w, exact, una, nexp, 100 + cfg, dn)
 
 
+def test_full_size_fused_fp32_forward_sampled(M):
+    """The long-sequence fp32 forward at full size (T = 16384) with the dispatch folded into the
+    row split: 64 unambiguous tokens row by row against the oracle, and every output bit for bit
+    against the layer with the dispatch call."""
+    layer, workloads = M
+    w = workloads.WORKLOADS[4]
+    inp = workloads.make_inputs(w, "cuda")
+    outs = []
+    for fused in (False, True):
+        b = layer.LayerBuffers(w.T, w.h, w.E, w.k, w.f, torch.float32, backward=False, fused=fused)
+        layer.step(inp, b)
+        torch.cuda.synchronize()
+        assert binding_status(b) == 0
+        outs.append(b)
+    ref, b = outs
+    for n in ("ybuf", "h1", "h3", "a", "y"):
+        assert torch.equal(getattr(b, n), getattr(ref, n)), n
+    x, Wg = np64(inp["x"]), np64(inp["Wg"])
+    bias = None if inp["bias"] is None else np64(inp["bias"])
+    una = routing_checks(b, O.router_logits(x, Wg, bias, "f64"), w.k)
+    S = _sample_unambiguous(64, una, 44)
+    assert len(S) >= 64, f"only {len(S)} unambiguous sampled tokens"
+    check_sampled_tokens(b, inp, w, S, "f32")
+
+
 @pytest.mark.parametrize("T,h,E,k,f,dt", [(1, 128, 8, 2, 64, torch.float32), (5, 64, 4, 4, 16, torch.bfloat16),
                                           (33, 72, 12, 12, 24, torch.float32), (17, 256, 4, 1, 128, torch.bfloat16),
                                           (300, 256, 4, 4, 256, torch.bfloat16)])  # k = E on the tensor cores
