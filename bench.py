@@ -859,7 +859,7 @@ def run_ours(args, w):
         # copy streams beside the compute.  Every step's copies are inside the timed region; the
         # first upload and the last download are exposed.  No L2 flush between these steps: the
         # weights every step reads (and the per-step traffic) are far larger than L2.
-        pipe = layer.HostPipeline(inp, b)
+        pipe = layer.HostPipeline(inp, b, graphs=not args.no_graph)
         for _ in range(args.warmup):
             pipe.submit(hx, hy, hdy, hdx)
         pipe.finish()
@@ -881,8 +881,9 @@ def run_ours(args, w):
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "ms_per_step": e2e_ms,
                "copies": "pinned host buffers; layer.HostPipeline overlaps step i+1's upload and step i's "
-                         "downloads with the compute (two device slots for x and dy), all inside the timed "
-                         "region; no L2 flush between steps (weights larger than L2)"}
+                         "downloads with the compute (two device slots for x, dy, y and dx, each slot's step "
+                         "one captured CUDA graph), all inside the timed region; no L2 flush between steps "
+                         "(weights larger than L2)"}
         del pipe
 
     # ---------------------------------------------------------------- CPU oracle baseline (rank 0, N = 1)

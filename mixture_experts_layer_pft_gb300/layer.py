@@ -3,7 +3,9 @@
 ``LayerBuffers`` allocates every device buffer of the layer once (PyTorch owns the memory);
 ``forward`` and ``backward`` issue the stage calls in order on the current stream.  Each stage
 runs in the library's kernels; this module only sequences them.  ``step_host`` runs a step whose
-tokens live in pinned host memory, and ``CapturedStep`` replays a captured step as one CUDA graph.
+tokens live in pinned host memory, ``HostPipeline`` runs a stream of such steps with the copies
+beside the compute of neighbouring steps, and ``CapturedStep`` replays a captured step as one CUDA
+graph.
 """
 
 from __future__ import annotations
@@ -180,31 +182,51 @@ class HostPipeline:
 
     Two device slots hold the tokens (x, and dy for the backward) of consecutive steps: step
     i + 1's upload runs on a copy stream into the other slot while step i computes, and y and dx
-    download on a second copy stream while later work runs.  The current stream orders the
-    compute: a step waits for its own upload, and for the download of the previous step's y
-    (and dx) before it overwrites b.y (and b.dx).  ``submit`` returns at once.  ``finish`` makes
-    the current stream wait for every download, so the host buffers of every submitted step are
-    complete once the current stream is.
+    download on a second copy stream while later work runs.  ``submit`` returns at once.
+    ``finish`` makes the current stream wait for every download, so the host buffers of every
+    submitted step are complete once the current stream is.
+
+    With ``graphs`` (the default) each slot's step is captured once as a CUDA graph that writes
+    the slot's own y (and dx): a step waits for its upload and for the download of the outputs
+    its slot held two steps back, and then replays as one launch.  Without it the calls are
+    issued one by one on the current stream, y downloads while the backward runs, and a step
+    waits for the previous step's y (and dx) to leave b.y (and b.dx) before overwriting them.
 
     ``inp`` holds the weights (and the router bias); its x and dy are slot 0.  The host buffers
     passed to ``submit`` must stay untouched until the current stream passes ``finish``.
     """
 
-    def __init__(self, inp: dict, b: LayerBuffers):
+    def __init__(self, inp: dict, b: LayerBuffers, graphs: bool = True):
         self.b = b
         self.inp = inp
         dev = inp["x"].device
-        self.x = [inp["x"], torch.empty_like(inp["x"])]
-        self.dy = [inp["dy"], torch.empty_like(inp["dy"])] if b.backward else [None, None]
+        bwd = b.backward
+        self.x = [inp["x"], torch.zeros_like(inp["x"])]
+        self.dy = [inp["dy"], torch.zeros_like(inp["dy"])] if bwd else [None, None]
         self.up = torch.cuda.Stream(device=dev)
         self.down = torch.cuda.Stream(device=dev)
         ev = lambda: torch.cuda.Event()  # noqa: E731
         self.slot_free = [ev(), ev()]   # the compute that last read a slot is done
         self.ready = [ev(), ev()]       # a slot's upload is done
+        self.out_done, self.out_free = [ev(), ev()], [ev(), ev()]  # graphs: a slot's outputs
         self.y_done, self.y_free = ev(), ev()
         self.dx_done, self.dx_free = ev(), ev()
+        self.graphs = None
+        if graphs:
+            self.y = [b.y, torch.zeros_like(b.y)]
+            self.dx = [b.dx, torch.zeros_like(b.dx)] if bwd else [None, None]
+            self.graphs = []
+            for sl in range(2):
+                b.y = self.y[sl]
+                if bwd:
+                    b.dx = self.dx[sl]
+                inp_s = dict(inp, x=self.x[sl], dy=self.dy[sl])
+                self.graphs.append(CapturedStep(lambda inp_s=inp_s: step(inp_s, b)))
+            b.y = self.y[0]
+            if bwd:
+                b.dx = self.dx[0]
         cur = torch.cuda.current_stream()
-        for e in self.slot_free + [self.y_free, self.dx_free]:
+        for e in self.slot_free + self.out_free + [self.y_free, self.dx_free]:
             e.record(cur)
         self.i = 0
 
@@ -218,8 +240,21 @@ class HostPipeline:
             if b.backward:
                 self.dy[s].copy_(hdy, non_blocking=True)
             self.ready[s].record(self.up)
-        inp = dict(self.inp, x=self.x[s], dy=self.dy[s])
         cur.wait_event(self.ready[s])
+        if self.graphs is not None:
+            cur.wait_event(self.out_free[s])  # this slot's outputs of two steps back have left
+            self.graphs[s].replay()
+            self.out_done[s].record(cur)
+            self.slot_free[s].record(cur)
+            self.down.wait_event(self.out_done[s])
+            with torch.cuda.stream(self.down):
+                hy.copy_(self.y[s], non_blocking=True)
+                if b.backward:
+                    hdx.copy_(self.dx[s], non_blocking=True)
+                self.out_free[s].record(self.down)
+            self.i += 1
+            return
+        inp = dict(self.inp, x=self.x[s], dy=self.dy[s])
         cur.wait_event(self.y_free)  # the previous step's y has left b.y
         forward(inp, b)
         self.y_done.record(cur)

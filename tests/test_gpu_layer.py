@@ -407,8 +407,9 @@ def test_host_buffer_step_equals_device_step(M, cfg):
             assert torch.equal(hdx, want_dx)
 
 
+@pytest.mark.parametrize("graphs", [True, False])
 @pytest.mark.parametrize("cfg", [0, 1, 4])
-def test_host_pipeline_equals_device_steps(M, cfg):
+def test_host_pipeline_equals_device_steps(M, cfg, graphs):
     """HostPipeline over four different batches (two device slots, uploads and downloads on
     copy streams beside the compute): each batch's y and dx are the bits of a device-resident
     step on that batch."""
@@ -430,7 +431,7 @@ def test_host_pipeline_equals_device_steps(M, cfg):
     outs = [(torch.zeros_like(hx).pin_memory(), torch.zeros_like(hx).pin_memory() if w.backward else None)
             for hx, _ in host]
     weights = dict(batches[0], x=torch.zeros_like(batches[0]["x"]), dy=torch.zeros_like(batches[0]["dy"]))
-    pipe = layer.HostPipeline(weights, b)
+    pipe = layer.HostPipeline(weights, b, graphs=graphs)
     for (hx, hdy), (hy, hdx) in zip(host, outs):
         pipe.submit(hx, hy, hdy, hdx)
     pipe.finish()
