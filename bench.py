@@ -344,6 +344,27 @@ def run_reference(args, w):
     return 0
 
 
+def oracle_single_thread(args):
+    """The reference arm's sample (one step) in a child process whose BLAS may use one thread:
+    the oracle on one core beside the all-core figure."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--config", str(args.config),
+           "--steps", "1", "--warmup", "0"]
+    if args.tokens:
+        cmd += ["--tokens", str(args.tokens)]
+    if args.experts:
+        cmd += ["--experts", str(args.experts)]
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    for k in ("RANK", "LOCAL_RANK", "WORLD_SIZE"):
+        env.pop(k, None)
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=300)
+        line = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")][-1]
+        return {"value": line["value"], "unit": line["unit"], "cores": 1, "kind": "oracle",
+                "sample": line["cpu_baseline"]["sample"] + ", one BLAS thread"}
+    except Exception as e:  # noqa: BLE001 -- a baseline, not the product: report and go on
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+
+
 def workload_desc(w):
     return (f"{w.name}: T={w.T} tokens, h={w.h}, E={w.E}, top-k={w.k}, SwiGLU f={w.f}, "
             f"{w.dtype}{' (fp32 gating)' if w.dtype == 'bf16' else ''}, "
@@ -896,6 +917,8 @@ def run_ours(args, w):
                "sample": f"one {'forward+backward' if w.backward else 'forward'} of a seeded {Ts} of {w.T} "
                          f"tokens and the {n_exp} experts they reach (the benchmark's own inputs), fp64 "
                          f"numpy/OpenBLAS, {ts[0]:.1f} s; value = sample FLOPs / time"}
+        if not args.no_single_thread:
+            cpu["single_thread"] = oracle_single_thread(args)
 
     # ---------------------------------------------------------------- scaled PFT build and the T = 16384 run
     pft_scaled = None if args.no_pft_scaled else measure_pft_scaled(binding, flush, peaks)
@@ -965,6 +988,8 @@ def main(argv=None):
     ap.add_argument("--no-graph", action="store_true",
                     help="time steps as one host call per stage instead of a CUDA graph replay")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-single-thread", action="store_true",
+                    help="skip the one-thread oracle timing beside the all-core cpu_baseline")
     ap.add_argument("--no-pft-scaled", action="store_true",
                     help="skip the PFT build at T = 2^20, k = 8, E = 256")
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count T")
